@@ -1,0 +1,25 @@
+"""Error-feedback gradient compression on GB300 (sm_103a).
+
+The compute lives in ``libefgrad.so`` (hand-written CUDA behind a C ABI,
+declared in ``include/efgrad.h``).  ``binding`` marshals torch tensors to
+that ABI; it loads the library on first use and raises if it was not built,
+so there is no fallback path.  ``workloads`` holds the seeded synthetic
+inputs.
+"""
+
+from .binding import (  # noqa: F401
+    EFError,
+    IDX_BITMAP,
+    IDX_INT32,
+    APPLY_MOMENTUM,
+    APPLY_SGD,
+    library,
+    library_path,
+    sign_aggregate_apply,
+    sign_compress,
+    sparse_aggregate_apply,
+    topk_compress,
+    topk_workspace_size,
+    aggregate_workspace_size,
+    workspace_status,
+)

@@ -1,0 +1,233 @@
+/*
+ * efgrad.h -- C ABI of libefgrad: error-feedback gradient compression on
+ * GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [SPARSE] "梯度稀疏化：只传输重要的梯度元素" (Gradient sparsification:
+ *            transmit only the important gradient elements).
+ *   [ONEBIT] "1bit Adam梯度压缩技术原理与分布式训练优化" (1-bit Adam gradient
+ *            compression: principle and distributed-training optimisation).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Pointers named h_* are host memory; every other buffer pointer is
+ *   device memory of the current CUDA device.  The caller owns all buffers.
+ *   The library allocates no device memory, keeps no pointer after a call
+ *   returns, and keeps no state between calls other than a per-thread
+ *   profiling hook (ef_profile_events) and a per-thread last CUDA error.
+ *   Scratch memory comes from a caller-provided workspace whose size the
+ *   matching *_workspace_size query returns; it must be 256-byte aligned and
+ *   may be reused by the next call on the same stream.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  Calls enqueue work on it and return without
+ *   synchronising; no device-to-host read-back happens inside a call.
+ * Numbers.  Every float is IEEE-754 binary32; every arithmetic step is a
+ *   single round-to-nearest-even operation, never a fused multiply-add, in
+ *   the order stated per function, so results are reproducible bit for bit.
+ * Alignment.  Float / int32 / uint32 buffers must be 4-byte aligned.  The
+ *   kernels use 16-byte vector accesses where the addresses allow it and
+ *   scalar accesses otherwise; results do not depend on the path taken.
+ * Errors.  Every call returns an ef_status.  Argument errors are detected on
+ *   the host before anything is enqueued and leave every output untouched.
+ *   Conditions that only the device can see (a bounded wait that ran out, a
+ *   malformed packet) are written to a status word inside the workspace and
+ *   read with ef_workspace_status().
+ */
+#ifndef EFGRAD_H
+#define EFGRAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ef_status;
+
+#define EF_OK                  0
+#define EF_ERR_NULL            1  /* a required pointer is NULL                        */
+#define EF_ERR_SIZE            2  /* n < 0, or a size limit below is exceeded          */
+#define EF_ERR_K               3  /* k < 0 or k > its segment's length                 */
+#define EF_ERR_SEGMENTS        4  /* offsets do not rise monotonically from 0 to n     */
+#define EF_ERR_ALIAS           5  /* an output overlaps a buffer it must not overlap   */
+#define EF_ERR_WORKSPACE       6  /* workspace NULL, misaligned or too small           */
+#define EF_ERR_WORKERS         7  /* W < 1 or W > EF_MAX_WORKERS                       */
+#define EF_ERR_ARG             8  /* unknown enum value, or a non-finite scalar        */
+#define EF_ERR_ALIGN           9  /* a pointer is not 4-byte aligned                   */
+#define EF_ERR_ARCH           10  /* the current device is not compute capability 10.3 */
+#define EF_ERR_CUDA           11  /* a CUDA call failed; see ef_last_cuda_error()      */
+#define EF_ERR_DEVICE_TIMEOUT 12  /* device-side: a bounded inter-block wait ran out   */
+#define EF_ERR_PACKET         13  /* device-side: packet indices not strictly ascending,
+                                     out of range, or a bitmap whose population count
+                                     differs from the stated k                         */
+
+#define EF_IDX_INT32   0  /* packet = fp32 values[k] + int32 global indices[k]        */
+#define EF_IDX_BITMAP  1  /* packet = fp32 values[k] + uint32 bitmap[ceil(n/32)]      */
+
+#define EF_APPLY_SGD       0  /* w <- w - eta * G                                    */
+#define EF_APPLY_MOMENTUM  1  /* m <- beta1 * m + (1 - beta1) * G                      */
+
+#define EF_MAX_WORKERS 64
+#define EF_ABI_VERSION 1
+
+/* Library ABI version (EF_ABI_VERSION of the build). */
+int32_t ef_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+const char* ef_status_string(ef_status s);
+
+/* cudaError_t of the last failed CUDA call made by this thread inside the
+ * library (0 if none). */
+int32_t ef_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------
+ * Top-k error feedback, sender side.
+ *
+ * [SPARSE] §详细算法流程 steps 2-5, applied to each segment (tensor)
+ * independently as §分层阈值与自适应稀疏率 and §分层自适应Top-k describe:
+ *   g      = g_raw + e                     (step 2, e_0 = 0)
+ *   S_s    = the k_s elements of segment s with the largest |g|; ties in |g|
+ *            go to the lower index, and |g| is compared as the float's bit
+ *            pattern with the sign cleared, so NaN ranks above +Inf and +0
+ *            ties -0                        (step 3, §Top-k 稀疏化)
+ *   e'     = g off S, +0.0 on S             (step 4: e = g - g~)
+ *   packet = (g[i], i) for i in S           (step 5, §梯度稀疏化的基本原理 step 3)
+ *
+ * g_raw        [n] fp32, read only.
+ * e            [n] fp32, in: e_{t-1}, out: e_t (updated in place).
+ * n            elements in the flat buffer, 0 <= n; with EF_IDX_INT32 also
+ *              n <= 2^31 so that every global index fits an int32.
+ * nseg         number of segments, >= 1.
+ * h_seg_offsets[nseg+1] host, 0 = off[0] <= off[1] <= ... <= off[nseg] = n;
+ *              segment s is [off[s], off[s+1]), at most 2^31 - 1 elements.
+ * h_seg_k[nseg] host, 0 <= k_s <= segment length.
+ * idx_format   EF_IDX_INT32 or EF_IDX_BITMAP ([SPARSE] §索引编码压缩).
+ * out_values   [sum k] fp32: segment 0's entries first; within a segment in
+ *              ascending index order, so the packet ascends globally.
+ * out_indices  [sum k] int32 global indices (INT32 format; NULL for BITMAP).
+ * out_bitmap   [ceil(n/32)] uint32 (BITMAP format; NULL for INT32): bit i%32
+ *              of word i/32 is set iff i is selected; padding bits are 0.
+ * workspace    device scratch of at least ef_topk_workspace_size() bytes.
+ * Outputs must not overlap g_raw, e, the workspace or each other; g_raw and
+ * e must not overlap.  The result is unique (the order above is total), so it
+ * does not depend on the launch configuration.
+ * ---------------------------------------------------------------------- */
+ef_status ef_topk_workspace_size(int64_t n, int32_t nseg,
+                                 const int64_t* h_seg_offsets,
+                                 const int64_t* h_seg_k, int32_t idx_format,
+                                 size_t* bytes);
+
+ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
+                           int32_t nseg, const int64_t* h_seg_offsets,
+                           const int64_t* h_seg_k, int32_t idx_format,
+                           float* out_values, int32_t* out_indices,
+                           uint32_t* out_bitmap, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * 1-bit sign error feedback, sender side.
+ *
+ * [ONEBIT] §2.1 量化与误差补偿机制:
+ *   v      = RN(g + eps)
+ *   bit    = !(v < 0)            (sign(0) = +1, also for -0 and NaN)
+ *   s      = bit ? +1 : -1       (the quantised gradient ghat)
+ *   Delta  = RN(v - s)
+ *   c      = RN(1 - beta1)
+ *   eps'   = RN(RN(beta1 * eps) + RN(c * Delta))
+ *
+ * g        [n] fp32 gradient, read only.
+ * eps      [n] fp32 error buffer, in: eps_{t-1}, out: eps_t (in place).
+ * beta1    EMA coefficient (the pages use 0.9); must be finite.
+ * out_bits [ceil(n/32)] uint32: bit i%32 of word i/32 is element i's bit;
+ *          padding bits 0.  Must not overlap g or eps; g and eps must not
+ *          overlap.
+ * ---------------------------------------------------------------------- */
+ef_status ef_sign_compress(const float* g, float* eps, int64_t n, float beta1,
+                           uint32_t* out_bits, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Receive side for top-k packets.
+ *
+ * [SPARSE] §详细算法流程 steps 6-7 (and the receiver of §梯度稀疏化的基本原理):
+ *   G[i] = (((+0 + p_0[i]) + p_1[i]) + ... + p_{W-1}[i])   worker order,
+ *          where p_w[i] is worker w's packet value at i or absent (no term)
+ *   w[i] = RN(w[i] - RN(eta * G[i]))   at every i some packet contains;
+ *          elsewhere w is not accessed (and would be unchanged: G = 0).
+ *
+ * W           number of workers' packets, 1 <= W <= EF_MAX_WORKERS.
+ * idx_format  EF_IDX_INT32 or EF_IDX_BITMAP, the same for all packets.
+ * h_values[W] host array of device pointers to fp32 values[k_w].
+ * h_indices[W] host array of device pointers to int32 indices[k_w], strictly
+ *             ascending within a packet, each in [0, n) (INT32; else NULL).
+ * h_bitmaps[W] host array of device pointers to uint32 bitmaps[ceil(n/32)]
+ *             (BITMAP; else NULL); values follow the set bits in order.
+ * h_k[W]      host, entries per packet, 0 <= k_w <= n.
+ * n           length of the dense gradient / parameter vector.
+ * eta         learning rate, finite.
+ * G           [n] fp32 dense aggregated gradient, written in full; may be
+ *             NULL to skip the dense write (then only touched w change).
+ * w           [n] fp32 parameters, updated in place.
+ * workspace   device scratch of at least ef_aggregate_workspace_size().
+ * Malformed packets (unsorted, out-of-range index, bitmap population count
+ * different from k_w) are never read out of bounds; they set EF_ERR_PACKET
+ * in the workspace status and the outputs are then unspecified.
+ * ---------------------------------------------------------------------- */
+ef_status ef_aggregate_workspace_size(int32_t W, int32_t idx_format, int64_t n,
+                                      size_t* bytes);
+
+ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
+                                 const float* const* h_values,
+                                 const int32_t* const* h_indices,
+                                 const uint32_t* const* h_bitmaps,
+                                 const int64_t* h_k, int64_t n, float eta,
+                                 float* G, float* w, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Receive side for 1-bit packets.
+ *
+ * G[i] = sum over workers of (bit_w[i] ? +1 : -1), added in worker order onto
+ *        +0 (exact small integers), the sum of [SPARSE] §详细算法流程 step 6
+ *        applied to [ONEBIT] sign packets; then
+ *   EF_APPLY_SGD:       w[i] = RN(w[i] - RN(eta * G[i]))   ([SPARSE] step 7)
+ *   EF_APPLY_MOMENTUM:  m[i] = RN(RN(beta1 * m[i]) + RN(RN(1 - beta1) * G[i]))
+ *                       ([ONEBIT] §2.2 动量修正策略; with W = 1, G = ghat)
+ *
+ * h_bits[W]   host array of device pointers to uint32 bits[ceil(n/32)].
+ * mode        EF_APPLY_SGD or EF_APPLY_MOMENTUM; eta / beta1 finite (the one
+ *             the mode does not use is ignored).
+ * G           [n] fp32, written in full; may be NULL.
+ * w_or_m      [n] fp32 parameters (SGD) or momentum (MOMENTUM), in place.
+ * ---------------------------------------------------------------------- */
+ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bits,
+                               int64_t n, int32_t mode, float eta, float beta1,
+                               float* G, float* w_or_m, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Device-side status of the last call that used `workspace`: synchronises
+ * `stream`, then copies the status word (EF_OK, EF_ERR_DEVICE_TIMEOUT or
+ * EF_ERR_PACKET) to *device_status.  Each call that takes a workspace resets
+ * the word when it starts.
+ * ---------------------------------------------------------------------- */
+ef_status ef_workspace_status(const void* workspace, void* stream,
+                              int32_t* device_status);
+
+/* ------------------------------------------------------------------------
+ * Profiling hook (per calling thread).  While set, every launch of kernel
+ * `kernel_id` made by this thread is bracketed by cudaEventRecord(start) and
+ * cudaEventRecord(stop) on the call's stream, so the caller can time that
+ * one kernel with its own events.  Pass NULL events to clear.
+ * ---------------------------------------------------------------------- */
+#define EF_KERNEL_TOPK_FUSED   1  /* compensate + residual write + candidates */
+#define EF_KERNEL_SIGN         2  /* 1-bit compress                           */
+#define EF_KERNEL_SPARSE_APPLY 3  /* dense tile merge + SGD                   */
+#define EF_KERNEL_SIGN_APPLY   4  /* 1-bit aggregate + SGD / momentum         */
+ef_status ef_profile_events(int32_t kernel_id, void* start_event,
+                            void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EFGRAD_H */

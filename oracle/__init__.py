@@ -1,0 +1,22 @@
+"""CPU oracle for error-feedback gradient compression.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline / reference legs of ``bench.py``, never by the product
+library or its binding.  See ``ef_oracle.py`` for sources and readings.
+"""
+
+from .ef_oracle import (  # noqa: F401
+    abs_key,
+    compensate,
+    decode_signs,
+    onebit_momentum,
+    pack_bits,
+    packet_indices,
+    sgd_apply,
+    sign_aggregate,
+    sign_ef_step,
+    sparse_aggregate,
+    topk_ef_step,
+    topk_indices,
+    unpack_bits,
+)

@@ -1,0 +1,298 @@
+"""Plain CPU oracle for error-feedback gradient compression.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import this module.  The CUDA library and its Python binding
+never import it, and it imports nothing from them: the two sides share no
+code, no helpers and no constants.  Inputs reach both sides from the seeded
+generators in ``error_feedback_gradient_gb300/workloads.py``, which hold none
+of the arithmetic below.
+
+Sources (web pages, cited by title and section):
+
+* [SPARSE] "梯度稀疏化：只传输重要的梯度元素" ("Gradient sparsification:
+  transmit only the important gradient elements"), freeguideonline.com
+  tutorial.  Sections used: 梯度稀疏化的基本原理 (basic principle: select the
+  k largest |g|, send values + indices, the receiver sums by index);
+  必不可少的误差补偿 (error compensation); Top-k 稀疏化; 分层阈值与自适应稀疏率
+  and 分层自适应Top-k (each tensor selects independently); 详细算法流程
+  (the seven-step algorithm: steps 2-7); 索引编码压缩 (bitmap index).
+* [ONEBIT] "1bit Adam梯度压缩技术原理与分布式训练优化" ("1-bit Adam gradient
+  compression: principle and distributed-training optimisation"),
+  intelliparadigm.com article.  Sections used: 2.1 量化与误差补偿机制 (sign
+  quantisation, quantisation error, EMA error buffer); 2.2 动量修正策略
+  (momentum on the quantised gradient).
+
+Precision.  Both pages work with FP32 gradients ([ONEBIT] §1 assumes FP32,
+[SPARSE] §为什么要做梯度压缩 counts 32-bit floats), so every array here is
+float32 and every arithmetic operation is a single IEEE-754 float32 operation
+rounded to nearest-even.  numpy evaluates each ufunc separately, so no
+multiply-add is ever fused; the operation order written in each function is
+the order used.
+
+Readings taken where the pages are silent (each repeated where it is used):
+
+* ties in |g| go to the lower index, and |g| is compared as the IEEE bit
+  pattern with the sign bit cleared (so NaN ranks above +Inf, +0 ties -0);
+* a packet lists its entries in ascending index order, with global int32
+  indices into the flat buffer (or, in bitmap form, one bit per element,
+  element i at bit i % 32 of word i // 32, padding bits 0);
+* the residual at a selected position is +0.0;
+* sign(0) = +1 (also for -0 and NaN): a bit is 1 unless v < 0;
+* the receiver adds packets in worker order 0..W-1 starting from +0.0 and
+  does not average;
+* (1 - beta1) is formed in float32 before it multiplies.
+
+Parity pins for every function live in ``tests/test_oracle_pins.py``; no
+function here is parity-unpinned.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+U32 = np.uint32
+U64 = np.uint64
+
+# --------------------------------------------------------------------------
+# small helpers (bit layout, ordering key)
+# --------------------------------------------------------------------------
+
+
+def abs_key(g: np.ndarray) -> np.ndarray:
+    """Ordering key for |g|: the float32 bit pattern with the sign bit cleared.
+
+    For non-NaN values this uint32 is monotone in |g| ([SPARSE] §Top-k 稀疏化
+    ranks elements by absolute value).
+    """
+    g = np.ascontiguousarray(g, dtype=F32)
+    return g.view(U32) & U32(0x7FFFFFFF)
+
+
+def pack_bits(flags: np.ndarray) -> np.ndarray:
+    """Pack a boolean vector 32 to a uint32 word, element i -> bit i % 32 of
+    word i // 32 (least significant bit first), padding bits 0."""
+    flags = np.asarray(flags, dtype=bool).ravel()
+    n = flags.size
+    nw = (n + 31) // 32
+    padded = np.zeros(nw * 32, dtype=bool)
+    padded[:n] = flags
+    cols = padded.reshape(nw, 32)
+    words = np.zeros(nw, dtype=U32)
+    for j in range(32):
+        words |= cols[:, j].astype(U32) << U32(j)
+    return words
+
+
+def unpack_bits(words: np.ndarray, n: int) -> np.ndarray:
+    """Inverse of :func:`pack_bits` for the first ``n`` elements."""
+    words = np.asarray(words, dtype=U32).ravel()
+    nw = (n + 31) // 32
+    if words.size < nw:
+        raise ValueError("bit vector too short")
+    out = np.zeros((nw, 32), dtype=bool)
+    for j in range(32):
+        out[:, j] = ((words[:nw] >> U32(j)) & U32(1)).astype(bool)
+    return out.ravel()[:n]
+
+
+# --------------------------------------------------------------------------
+# top-k error feedback  ([SPARSE] 详细算法流程, steps 2-5)
+# --------------------------------------------------------------------------
+
+
+def compensate(g_raw: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """Step 2: g = g_raw + e (the carried residual is added back).
+
+    [SPARSE] §必不可少的误差补偿 and §详细算法流程 step 2; e starts at 0.
+    """
+    return np.add(np.asarray(g_raw, F32), np.asarray(e, F32), dtype=F32)
+
+
+def topk_indices(g: np.ndarray, k: int) -> np.ndarray:
+    """Step 3: the k elements of largest |g|, returned in ascending index order.
+
+    [SPARSE] §梯度稀疏化的基本原理 step 2 and §Top-k 稀疏化: keep the k
+    entries of largest absolute value, zero the rest.  The pages do not say
+    which entry wins a tie; the lower index does.
+
+    The selection is the plain definition: order every element by
+    (|g| descending, index ascending) and keep the first k.  That order is
+    encoded in one unsigned 64-bit number per element,
+    ``abs_key << 32 | (2**32 - 1 - index)``, whose descending order is exactly
+    the order above (a larger key wins; for equal keys the lower index has the
+    larger low word).  numpy's partition (a library selection routine) then
+    puts the k largest of those numbers last; their low words give back the
+    indices.  Requires len(g) < 2**32.
+    """
+    g = np.ascontiguousarray(g, dtype=F32)
+    n = g.size
+    if k < 0 or k > n:
+        raise ValueError(f"k={k} outside [0, {n}]")
+    if k == 0:
+        return np.zeros(0, dtype=np.int64)
+    if n >= 2**32:
+        raise ValueError("segment too long for the 64-bit rank encoding")
+    rank = abs_key(g).astype(U64) << U64(32)
+    rank |= U64(0xFFFFFFFF) - np.arange(n, dtype=U64)
+    rank.partition(n - k)
+    top = rank[n - k:]
+    idx = (U64(0xFFFFFFFF) - (top & U64(0xFFFFFFFF))).astype(np.int64)
+    idx.sort()
+    return idx
+
+
+def topk_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
+    """One layerwise top-k error-feedback step over a flat fp32 buffer.
+
+    [SPARSE] §详细算法流程 steps 2-5, applied independently to every segment
+    (tensor) as §分层阈值与自适应稀疏率 / §分层自适应Top-k prescribe:
+
+    2. g = g_raw + e_prev
+    3. g~ keeps the k_s largest |g| of segment s, zero elsewhere
+    4. e = g - g~  (= g off the selection, +0.0 on it)
+    5. pack the non-zeros of g~ with their indices
+
+    ``seg_offsets`` has nseg+1 entries (0 ... n); ``seg_k`` has nseg.
+    Packets list segment 0's entries first, each segment in ascending index
+    order, so the whole packet is in ascending global index order.
+
+    Returns a dict with ``values`` (float32[sum k]), ``indices`` (int32
+    global indices, only for ``idx_format == "int32"``), ``bitmap``
+    (uint32[ceil(n/32)], only for ``"bitmap"``) and ``e`` (the new residual,
+    float32[n]).
+    """
+    g_raw = np.ascontiguousarray(g_raw, dtype=F32)
+    e_prev = np.ascontiguousarray(e, dtype=F32)
+    n = g_raw.size
+    if e_prev.size != n:
+        raise ValueError("g_raw and e differ in length")
+    offs = [int(x) for x in seg_offsets]
+    ks = [int(x) for x in seg_k]
+    if len(offs) != len(ks) + 1 or offs[0] != 0 or offs[-1] != n:
+        raise ValueError("segment table does not span [0, n)")
+
+    g = compensate(g_raw, e_prev)                         # step 2
+    e_new = g.copy()                                      # step 4 off the selection
+    picked = []
+    for s, k in enumerate(ks):
+        a, b = offs[s], offs[s + 1]
+        if b < a:
+            raise ValueError("segment offsets must not decrease")
+        picked.append(topk_indices(g[a:b], k) + a)        # step 3
+    sel = np.concatenate(picked) if picked else np.zeros(0, np.int64)
+    values = g[sel].copy()                                # step 5 (values)
+    e_new[sel] = F32(0.0)                                 # step 4 on the selection
+    out = {"values": values, "e": e_new}
+    if idx_format == "int32":
+        if n > 2**31:
+            raise ValueError("int32 indices need n <= 2**31")
+        out["indices"] = sel.astype(np.int32)
+    elif idx_format == "bitmap":
+        flags = np.zeros(n, dtype=bool)
+        flags[sel] = True
+        out["bitmap"] = pack_bits(flags)
+    else:
+        raise ValueError(idx_format)
+    return out
+
+
+# --------------------------------------------------------------------------
+# 1-bit sign error feedback  ([ONEBIT] §2.1, §2.2)
+# --------------------------------------------------------------------------
+
+
+def sign_ef_step(g, eps, beta1: float):
+    """One 1-bit error-feedback step ([ONEBIT] §2.1 量化与误差补偿机制).
+
+    v      = g_t + eps_{t-1}
+    ghat_t = sign(v)                   (+1 unless v < 0; sign(0) = +1)
+    Delta  = v - ghat_t
+    eps_t  = beta1 * eps_{t-1} + (1 - beta1) * Delta
+
+    Float32 sequence: v = RN(g + eps); d = RN(v - s); c = RN(1 - beta1);
+    eps' = RN(RN(beta1 * eps) + RN(c * d)).
+
+    Returns (bits uint32[ceil(n/32)], eps' float32[n]).
+    """
+    g = np.ascontiguousarray(g, dtype=F32)
+    eps = np.ascontiguousarray(eps, dtype=F32)
+    b1 = F32(beta1)
+    c = np.subtract(F32(1.0), b1, dtype=F32)
+    v = np.add(g, eps, dtype=F32)
+    bit = ~(v < F32(0.0))
+    s = np.where(bit, F32(1.0), F32(-1.0)).astype(F32)
+    delta = np.subtract(v, s, dtype=F32)
+    eps_new = np.add(np.multiply(b1, eps, dtype=F32),
+                     np.multiply(c, delta, dtype=F32), dtype=F32)
+    return pack_bits(bit), eps_new
+
+
+def decode_signs(bits, n: int) -> np.ndarray:
+    """The +1 / -1 vector a sign packet stands for (bit 1 -> +1)."""
+    return np.where(unpack_bits(bits, n), F32(1.0), F32(-1.0)).astype(F32)
+
+
+def onebit_momentum(m, ghat, beta1: float) -> np.ndarray:
+    """[ONEBIT] §2.2 动量修正策略: m_t = beta1 * m_{t-1} + (1 - beta1) * ghat_t.
+
+    Float32 sequence: m' = RN(RN(beta1 * m) + RN(RN(1 - beta1) * ghat)).
+    """
+    m = np.ascontiguousarray(m, dtype=F32)
+    ghat = np.ascontiguousarray(ghat, dtype=F32)
+    b1 = F32(beta1)
+    c = np.subtract(F32(1.0), b1, dtype=F32)
+    return np.add(np.multiply(b1, m, dtype=F32),
+                  np.multiply(c, ghat, dtype=F32), dtype=F32)
+
+
+# --------------------------------------------------------------------------
+# receive side  ([SPARSE] 详细算法流程 steps 6-7)
+# --------------------------------------------------------------------------
+
+
+def packet_indices(packet, n: int) -> np.ndarray:
+    """Global indices of a packet, from its int32 list or its bitmap."""
+    if packet.get("indices") is not None:
+        return np.asarray(packet["indices"], dtype=np.int64)
+    return np.flatnonzero(unpack_bits(packet["bitmap"], n)).astype(np.int64)
+
+
+def sparse_aggregate(packets, n: int) -> np.ndarray:
+    """Step 6: sum the W workers' sparse gradients by index into a dense G.
+
+    [SPARSE] §梯度稀疏化的基本原理 (receiver adds values of equal index) and
+    §详细算法流程 step 6.  Packets are added in worker order 0..W-1 onto a
+    +0.0 vector, one float32 add per (worker, index); no averaging.
+    """
+    G = np.zeros(n, dtype=F32)
+    for p in packets:
+        idx = packet_indices(p, n)
+        vals = np.asarray(p["values"], dtype=F32)
+        if vals.size != idx.size:
+            raise ValueError("packet values and indices differ in length")
+        if idx.size and np.any(np.diff(idx) <= 0):
+            raise ValueError("packet indices must be strictly ascending")
+        G[idx] = np.add(G[idx], vals, dtype=F32)
+    return G
+
+
+def sign_aggregate(bit_vectors, n: int) -> np.ndarray:
+    """Step 6 for 1-bit packets: G = sum over workers of the decoded +-1 signs,
+    added in worker order (exact: small integers)."""
+    G = np.zeros(n, dtype=F32)
+    for bits in bit_vectors:
+        G = np.add(G, decode_signs(bits, n), dtype=F32)
+    return G
+
+
+def sgd_apply(w, G, eta: float) -> np.ndarray:
+    """Step 7: w_{t+1} = w_t - eta * G  (float32: RN(w - RN(eta * G))).
+
+    [SPARSE] §详细算法流程 step 7.  Where G == 0 the result equals w bit for
+    bit, so untouched parameters keep their exact value.
+    """
+    w = np.ascontiguousarray(w, dtype=F32)
+    G = np.ascontiguousarray(G, dtype=F32)
+    return np.subtract(w, np.multiply(F32(eta), G, dtype=F32), dtype=F32)

@@ -1,0 +1,487 @@
+"""Pins for the CPU oracle, independent of the oracle's own code.
+
+Each test ties an oracle function to something other than itself: the
+hand-computed worked examples under tests/golden/ (with their citations),
+brute force over tiny inputs with Python's own sort and the float's bit
+pattern read through ``struct``, exact rational arithmetic (``fractions``)
+on inputs where every float32 operation is exact, a library routine
+(torch's stable sort), closed forms and invariants.  The last group plants
+plausible mistakes into copies of the oracle and checks that the pins fail.
+"""
+
+import json
+import math
+import os
+import random
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import ef_oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F32 = np.float32
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _f(x):
+    return float(x) if not isinstance(x, str) else float(x)
+
+
+def _arr(xs):
+    return np.array([_f(x) for x in xs], dtype=F32)
+
+
+def _bits_of(x: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", x))[0]
+
+
+def _close(a, b, rel=1e-6):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    scale = max(np.max(np.abs(b)), 1e-30)
+    return np.max(np.abs(a - b)) <= rel * scale
+
+
+# ---------------------------------------------------------------------------
+# top-k
+# ---------------------------------------------------------------------------
+
+
+def check_topk_golden(topk_step=None):
+    topk_step = topk_step or oracle.topk_ef_step
+    fx = _load("topk_two_steps.json")
+    e = np.zeros(6, F32)
+    for st in fx["steps"]:
+        out = topk_step(_arr(st["g_raw"]), e, [0, 6], [fx["k"]])
+        assert out["indices"].tolist() == st["indices"]
+        assert out["values"].tolist() == st["values"]
+        assert out["e"].tolist() == st["e"]
+        e = out["e"]
+
+
+def test_topk_worked_example():
+    check_topk_golden()
+
+
+def _brute_topk(vals, k):
+    """Python sort of (-|x| bit pattern, index): the definition, by brute force."""
+    keyed = sorted(range(len(vals)),
+                   key=lambda i: (-(_bits_of(vals[i]) & 0x7FFFFFFF), i))
+    return sorted(keyed[:k])
+
+
+def _tiny_cases(rng):
+    levels = [0.0, -0.0, 1.0, -1.0, 0.5, -0.5, 2.0, 1e-30, -1e-30, 3.0e38]
+    for n in list(range(1, 17)) + [31, 32, 33, 47, 64]:
+        yield [rng.choice(levels) for _ in range(n)]               # many ties
+        yield [rng.uniform(-1, 1) for _ in range(n)]               # distinct
+        yield [rng.choice([0.25, -0.25]) for _ in range(n)]        # all one key
+        yield [float("inf") if i % 7 == 3 else rng.gauss(0, 1) for i in range(n)]
+
+
+def check_topk_bruteforce(topk_indices=None):
+    topk_indices = topk_indices or oracle.topk_indices
+    rng = random.Random(7)
+    for vals in _tiny_cases(rng):
+        g = np.array(vals, dtype=F32)
+        gl = [float(x) for x in g]        # values after float32 rounding
+        for k in range(len(vals) + 1):
+            assert topk_indices(g, k).tolist() == _brute_topk(gl, k), (gl, k)
+
+
+def test_topk_bruteforce_tiny():
+    check_topk_bruteforce()
+
+
+def test_topk_nan_ranks_above_inf():
+    g = np.array([1.0, np.inf, np.nan, -np.inf, 2.0], dtype=F32)
+    assert oracle.topk_indices(g, 1).tolist() == [2]
+    assert oracle.topk_indices(g, 3).tolist() == [1, 2, 3]
+
+
+def test_topk_matches_torch_stable_sort():
+    """Library routine: torch's stable descending sort of the |g| key gives
+    the same index set (stable => lower index first among ties)."""
+    rng = np.random.default_rng(3)
+    for n, k in [(1000, 10), (4097, 41), (20000, 20), (5000, 5000), (777, 0)]:
+        g = (rng.standard_t(3, n) * 1e-3).astype(F32)
+        g[rng.integers(0, n, n // 10)] = F32(1e-3)          # plant ties
+        g[rng.integers(0, n, n // 20)] = F32(-1e-3)
+        key = torch.from_numpy(g.view(np.uint32).astype(np.int64) & 0x7FFFFFFF)
+        order = torch.sort(key, descending=True, stable=True).indices[:k]
+        want = torch.sort(order).values.numpy()
+        assert np.array_equal(oracle.topk_indices(g, k), want)
+
+
+def test_topk_invariants():
+    rng = np.random.default_rng(11)
+    n = 30011
+    offs = [0, 5, 6, 1000, 1000, 17000, n]
+    ks = [5, 1, 37, 0, 160, 13011]
+    g_raw = (rng.standard_t(3, n) * 1e-3).astype(F32)
+    g_raw[::97] = F32(2e-3)                                  # ties across segments
+    e = (rng.standard_normal(n) * 1e-4).astype(F32)
+    out = oracle.topk_ef_step(g_raw, e, offs, ks)
+    g = (g_raw.astype(np.float64) + e.astype(np.float64)).astype(F32)  # exact-rounded sum
+    idx = out["indices"].astype(np.int64)
+    assert idx.size == sum(ks)
+    assert np.all(np.diff(idx) > 0)
+    dense = np.zeros(n, F32)
+    dense[idx] = out["values"]
+    # g~ + e' == g elementwise (values equal; the selected residual is +0)
+    assert np.array_equal(dense + out["e"], g)
+    assert np.all(out["e"][idx].view(np.uint32) == 0)
+    key = g.view(np.uint32) & np.uint32(0x7FFFFFFF)
+    for s, k in enumerate(ks):
+        a, b = offs[s], offs[s + 1]
+        sel = idx[(idx >= a) & (idx < b)]
+        assert sel.size == k
+        rest = np.setdiff1d(np.arange(a, b), sel)
+        if k and rest.size:
+            kmin = key[sel].min()
+            assert kmin >= key[rest].max()
+            # on the boundary key, every unselected index lies above every selected one
+            tied_sel = sel[key[sel] == kmin]
+            tied_rest = rest[key[rest] == kmin]
+            if tied_rest.size:
+                assert tied_sel.max() < tied_rest.min()
+
+
+def test_topk_telescoping_exact():
+    """Error feedback delays but never loses gradient ([SPARSE] §必不可少的误差补偿):
+    sum_t g~_t + e_T = sum_t g_raw_t, exact here because every value is a
+    small binary fraction (all float32 additions are exact)."""
+    rng = np.random.default_rng(5)
+    n, k, T = 257, 9, 12
+    e = np.zeros(n, F32)
+    sent = np.zeros(n, np.float64)
+    total = np.zeros(n, np.float64)
+    for _ in range(T):
+        g_raw = (rng.integers(-64, 65, n) / 64.0).astype(F32)
+        out = oracle.topk_ef_step(g_raw, e, [0, n], [k], "bitmap")
+        idx = np.flatnonzero(oracle.unpack_bits(out["bitmap"], n))
+        sent[idx] += out["values"].astype(np.float64)
+        total += g_raw.astype(np.float64)
+        e = out["e"]
+    assert np.array_equal(sent + e.astype(np.float64), total)
+
+
+def test_topk_edge_cases():
+    g = np.array([3.0, -1.0, 2.0, -0.0, 0.0], dtype=F32)
+    e = np.zeros(5, F32)
+    out = oracle.topk_ef_step(g, e, [0, 5], [0])            # k = 0: nothing sent
+    assert out["values"].size == 0 and np.array_equal(out["e"], g)
+    out = oracle.topk_ef_step(g, e, [0, 5], [5])            # k = n: everything sent
+    assert out["indices"].tolist() == [0, 1, 2, 3, 4]
+    assert np.all(out["e"].view(np.uint32) == 0)
+    out = oracle.topk_ef_step(np.full(9, 0.5, F32), np.zeros(9, F32), [0, 9], [4])
+    assert out["indices"].tolist() == [0, 1, 2, 3]           # all equal: lowest indices
+    out = oracle.topk_ef_step(np.zeros(0, F32), np.zeros(0, F32), [0, 0], [0])
+    assert out["values"].size == 0
+    with pytest.raises(ValueError):
+        oracle.topk_ef_step(g, e, [0, 5], [6])
+
+
+def test_layerwise_equals_separate_tensors():
+    """[SPARSE] §分层自适应Top-k: each tensor selects on its own, so one
+    layerwise call equals one call per tensor (indices shifted)."""
+    rng = np.random.default_rng(2)
+    sizes, ks = [7, 100, 1, 64], [2, 10, 1, 0]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    g = rng.standard_normal(offs[-1]).astype(F32)
+    e = rng.standard_normal(offs[-1]).astype(F32)
+    whole = oracle.topk_ef_step(g, e, offs, ks)
+    for s in range(len(sizes)):
+        a, b = offs[s], offs[s + 1]
+        part = oracle.topk_ef_step(g[a:b], e[a:b], [0, b - a], [ks[s]])
+        m = (whole["indices"] >= a) & (whole["indices"] < b)
+        assert np.array_equal(whole["indices"][m] - a, part["indices"])
+        assert np.array_equal(whole["values"][m], part["values"])
+        assert np.array_equal(whole["e"][a:b], part["e"])
+
+
+def test_bitmap_packet_equals_index_packet():
+    rng = np.random.default_rng(9)
+    n = 1000
+    g = rng.standard_normal(n).astype(F32)
+    z = np.zeros(n, F32)
+    a = oracle.topk_ef_step(g, z, [0, 300, n], [5, 17], "int32")
+    b = oracle.topk_ef_step(g, z, [0, 300, n], [5, 17], "bitmap")
+    assert np.array_equal(np.flatnonzero(oracle.unpack_bits(b["bitmap"], n)), a["indices"])
+    assert np.array_equal(a["values"], b["values"])
+    assert np.array_equal(a["e"], b["e"])
+
+
+# ---------------------------------------------------------------------------
+# bit layout
+# ---------------------------------------------------------------------------
+
+
+def check_pack_bits(pack=None):
+    pack = pack or oracle.pack_bits
+    rng = random.Random(1)
+    for n in [1, 3, 31, 32, 33, 64, 65, 100]:
+        flags = [rng.random() < 0.4 for _ in range(n)]
+        want = [0] * ((n + 31) // 32)
+        for i, f in enumerate(flags):
+            if f:
+                want[i // 32] |= 1 << (i % 32)
+        assert pack(np.array(flags)).tolist() == want
+    assert pack(np.array([True, False, True, True])).tolist() == [13]
+
+
+def test_pack_bits_lsb_first():
+    check_pack_bits()
+    flags = np.random.default_rng(0).random(77) < 0.5
+    assert np.array_equal(oracle.unpack_bits(oracle.pack_bits(flags), 77), flags)
+
+
+# ---------------------------------------------------------------------------
+# 1-bit sign error feedback and momentum
+# ---------------------------------------------------------------------------
+
+
+def check_sign_golden(sign_step=None, momentum=None):
+    sign_step = sign_step or oracle.sign_ef_step
+    momentum = momentum or oracle.onebit_momentum
+    fx = _load("sign_two_steps.json")
+    eps = np.zeros(4, F32)
+    m = np.zeros(4, F32)
+    for st in fx["steps"]:
+        words, eps = sign_step(_arr(st["g"]), eps, fx["beta1"])
+        assert words.tolist() == st["words"]
+        assert _close(eps, _arr(st["eps"]))
+        m = momentum(m, oracle.decode_signs(words, 4), fx["beta1"])
+        assert _close(m, _arr(st["m"]))
+
+
+def test_sign_worked_example():
+    check_sign_golden()
+
+
+def test_sign_bits_definition():
+    """bit = 1 unless g + eps < 0: sign(0) = +1 for +0 and -0; NaN gives 1."""
+    g = np.array([0.0, -0.0, -1e-45, 1e-45, np.nan, -np.inf, np.inf, -2.0, 2.0], F32)
+    words, _ = oracle.sign_ef_step(g, np.zeros_like(g), 0.9)
+    want = sum(1 << i for i, x in enumerate(g.tolist()) if not (x < 0))
+    assert words.tolist() == [want]
+    # eps shifts the decision: g + eps crosses zero
+    words, _ = oracle.sign_ef_step(np.array([0.5, -0.5], F32),
+                                   np.array([-1.0, 1.0], F32), 0.9)
+    assert words.tolist() == [0b10]
+
+
+def _sign_exact(g, eps, beta1):
+    """The §2.1 formulas in exact rational arithmetic."""
+    v = [Fraction(a) + Fraction(b) for a, b in zip(g, eps)]
+    s = [Fraction(-1) if x < 0 else Fraction(1) for x in v]
+    d = [x - y for x, y in zip(v, s)]
+    b1 = Fraction(beta1)
+    return s, [b1 * Fraction(e) + (1 - b1) * dd for e, dd in zip(eps, d)]
+
+
+def test_sign_exact_rational():
+    """Binary-fraction inputs and beta1 in {0.5, 0.75}: every float32 step is
+    exact, so the oracle must equal the formulas evaluated in Fractions."""
+    rng = random.Random(4)
+    for beta1 in (0.5, 0.75, 0.0, 1.0):
+        n = 70
+        eps = np.zeros(n, F32)
+        m = np.zeros(n, F32)
+        m_exact = [Fraction(0)] * n
+        for _ in range(4):
+            g = np.array([rng.randint(-32, 32) / 16 for _ in range(n)], F32)
+            s, eps_exact = _sign_exact(g.tolist(), eps.tolist(), beta1)
+            words, eps = oracle.sign_ef_step(g, eps, beta1)
+            assert [Fraction(x) for x in eps.tolist()] == eps_exact
+            assert oracle.decode_signs(words, n).tolist() == [float(x) for x in s]
+            b1 = Fraction(beta1)
+            m_exact = [b1 * a + (1 - b1) * b for a, b in zip(m_exact, s)]
+            m = oracle.onebit_momentum(m, oracle.decode_signs(words, n), beta1)
+            assert [Fraction(x) for x in m.tolist()] == m_exact
+
+
+def test_sign_closed_forms():
+    rng = np.random.default_rng(8)
+    g = rng.standard_normal(1000).astype(F32)
+    eps = rng.standard_normal(1000).astype(F32)
+    v = (g + eps).astype(F32)
+    s = np.where(v < 0, F32(-1), F32(1))
+    _, e0 = oracle.sign_ef_step(g, eps, 0.0)     # beta1 = 0: eps' = Delta
+    assert np.array_equal(e0, (v - s).astype(F32))
+    _, e1 = oracle.sign_ef_step(g, eps, 1.0)     # beta1 = 1: eps' = eps
+    assert np.array_equal(e1, eps)
+
+
+def test_one_minus_beta1_in_float32():
+    # 1 - float32(0.9) = 0.10000002384185791015625 exactly (Sterbenz)
+    _, eps = oracle.sign_ef_step(np.array([-1.0], F32), np.zeros(1, F32), 0.9)
+    # v = -1, s = -1, Delta = 0 -> eps' = 0
+    assert eps.tolist() == [0.0]
+    m = oracle.onebit_momentum(np.zeros(1, F32), np.ones(1, F32), 0.9)
+    assert m.tolist() == [0.10000002384185791015625]
+
+
+# ---------------------------------------------------------------------------
+# receive side
+# ---------------------------------------------------------------------------
+
+
+def _packets(ex):
+    return [{"indices": np.array(p["indices"], np.int32), "values": _arr(p["values"])}
+            for p in ex["packets"]]
+
+
+def check_aggregate_golden(aggregate=None, sgd=None):
+    aggregate = aggregate or oracle.sparse_aggregate
+    sgd = sgd or oracle.sgd_apply
+    fx = _load("aggregate_examples.json")
+    for ex in fx["examples"]:
+        G = aggregate(_packets(ex), ex["n"])
+        assert G.tolist() == [float(x) for x in ex["G"]], ex["name"]
+        if "G_signbit" in ex:
+            assert np.signbit(G).tolist() == ex["G_signbit"]
+        w = sgd(_arr(ex["w0"]), G, ex["eta"])
+        want = _arr(ex["w"])
+        if ex["name"] == "two_workers":
+            assert _close(w, want)
+            assert w[5] == 1.0 and w[0] == 1.0
+        else:
+            assert w.view(np.uint32).tolist() == want.view(np.uint32).tolist()
+
+
+def test_aggregate_worked_examples():
+    check_aggregate_golden()
+
+
+def test_aggregate_exact_rational():
+    rng = random.Random(12)
+    n, W = 300, 5
+    packets, exact = [], [Fraction(0)] * n
+    for _ in range(W):
+        idx = sorted(rng.sample(range(n), rng.randint(0, 60)))
+        vals = [rng.randint(-1000, 1000) / 256 for _ in idx]
+        packets.append({"indices": np.array(idx, np.int32), "values": np.array(vals, F32)})
+        for i, v in zip(idx, vals):
+            exact[i] += Fraction(v)
+    G = oracle.sparse_aggregate(packets, n)
+    assert [Fraction(x) for x in G.tolist()] == exact
+    w0 = np.array([rng.randint(-100, 100) / 8 for _ in range(n)], F32)
+    w = oracle.sgd_apply(w0, G, 0.25)
+    assert [Fraction(x) for x in w.tolist()] == [
+        Fraction(a) - Fraction(1, 4) * b for a, b in zip(w0.tolist(), exact)]
+
+
+def test_aggregate_single_worker_is_scatter():
+    rng = np.random.default_rng(6)
+    n = 5000
+    idx = np.sort(rng.choice(n, 300, replace=False)).astype(np.int32)
+    vals = rng.standard_normal(300).astype(F32)
+    G = oracle.sparse_aggregate([{"indices": idx, "values": vals}], n)
+    want = np.zeros(n, F32)
+    want[idx] = vals
+    assert np.array_equal(G, want)
+
+
+def test_sgd_leaves_untouched_bitwise():
+    w = np.array([1.5, -0.0, 0.0, np.inf, 3.0e-45], F32)
+    out = oracle.sgd_apply(w, np.zeros(5, F32), 0.37)
+    assert out.view(np.uint32).tolist() == w.view(np.uint32).tolist()
+
+
+def test_aggregate_rejects_unsorted():
+    with pytest.raises(ValueError):
+        oracle.sparse_aggregate([{"indices": np.array([3, 1], np.int32),
+                                  "values": np.ones(2, F32)}], 5)
+
+
+def test_sign_aggregate_counts():
+    rng = random.Random(3)
+    n, W = 77, 6
+    flags = [[rng.random() < 0.5 for _ in range(n)] for _ in range(W)]
+    G = oracle.sign_aggregate([oracle.pack_bits(np.array(f)) for f in flags], n)
+    want = [sum(1 if flags[w][i] else -1 for w in range(W)) for i in range(n)]
+    assert G.tolist() == [float(x) for x in want]
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: the pins above must catch them
+# ---------------------------------------------------------------------------
+
+
+def _topk_ties_to_higher_index(g, k):
+    g = np.ascontiguousarray(g, dtype=F32)
+    n = g.size
+    if k == 0:
+        return np.zeros(0, np.int64)
+    rank = (oracle.abs_key(g).astype(np.uint64) << np.uint64(32)) | np.arange(n, dtype=np.uint64)
+    rank.partition(n - k)
+    return np.sort((rank[n - k:] & np.uint64(0xFFFFFFFF)).astype(np.int64))
+
+
+def _topk_signed_not_abs(g, k):
+    g = np.ascontiguousarray(g, dtype=F32)
+    if k == 0:
+        return np.zeros(0, np.int64)
+    order = np.argsort(-g.astype(np.float64), kind="stable")
+    return np.sort(order[:k])
+
+
+def _pack_msb_first(flags):
+    flags = np.asarray(flags, dtype=bool)
+    words = oracle.pack_bits(flags)
+    return np.array([int(f"{int(w):032b}"[::-1], 2) for w in words], np.uint32)
+
+
+def _sign_step_wrong_ema(g, eps, beta1):
+    bits, _ = oracle.sign_ef_step(g, eps, beta1)
+    v = (g + eps).astype(F32)
+    s = np.where(v < 0, F32(-1), F32(1))
+    # mistake: the two EMA weights swapped
+    return bits, ((F32(1) - F32(beta1)) * eps + F32(beta1) * (v - s)).astype(F32)
+
+
+def _sign_zero_is_zero(g, eps, beta1):
+    # mistake: torch-style sign(0) = 0 would mark 0 as "not positive"
+    v = (np.asarray(g, F32) + np.asarray(eps, F32)).astype(F32)
+    bits = oracle.pack_bits(v > 0)
+    _, e = oracle.sign_ef_step(g, eps, beta1)
+    return bits, e
+
+
+def _aggregate_reverse_order(packets, n):
+    return oracle.sparse_aggregate(list(reversed(packets)), n)
+
+
+def _sgd_wrong_sign(w, G, eta):
+    return (np.asarray(w, F32) + F32(eta) * np.asarray(G, F32)).astype(F32)
+
+
+@pytest.mark.parametrize("check,kwargs", [
+    (check_topk_bruteforce, {"topk_indices": _topk_ties_to_higher_index}),
+    (check_topk_bruteforce, {"topk_indices": _topk_signed_not_abs}),
+    (check_pack_bits, {"pack": _pack_msb_first}),
+    (check_sign_golden, {"sign_step": _sign_step_wrong_ema}),
+    (check_sign_golden, {"sign_step": _sign_zero_is_zero}),
+    (check_aggregate_golden, {"aggregate": _aggregate_reverse_order}),
+    (check_aggregate_golden, {"sgd": _sgd_wrong_sign}),
+])
+def test_pins_catch_planted_mistakes(check, kwargs):
+    with pytest.raises(AssertionError):
+        check(**kwargs)
+
+
+def test_topk_golden_catches_dropped_residual():
+    def no_feedback(g_raw, e, offs, ks, idx_format="int32"):
+        return ef_oracle.topk_ef_step(g_raw, np.zeros_like(e), offs, ks, idx_format)
+    with pytest.raises(AssertionError):
+        check_topk_golden(no_feedback)
