@@ -33,7 +33,9 @@ the order used.
 Readings taken where the pages are silent (each repeated where it is used):
 
 * ties in |g| go to the lower index, and |g| is compared as the IEEE bit
-  pattern with the sign bit cleared (so NaN ranks above +Inf, +0 ties -0);
+  pattern with the sign bit cleared (so +0 ties -0); every NaN ranks above
+  +Inf and all NaNs tie whatever their payload (NaN payload bits are not
+  part of any result: two NaNs compare equal);
 * a packet lists its entries in ascending index order, with global int32
   indices into the flat buffer (or, in bitmap form, one bit per element,
   element i at bit i % 32 of word i // 32, padding bits 0);
@@ -64,10 +66,13 @@ def abs_key(g: np.ndarray) -> np.ndarray:
     """Ordering key for |g|: the float32 bit pattern with the sign bit cleared.
 
     For non-NaN values this uint32 is monotone in |g| ([SPARSE] §Top-k 稀疏化
-    ranks elements by absolute value).
+    ranks elements by absolute value).  Every NaN gets the largest key,
+    0x7FFFFFFF, so NaNs rank above +Inf and tie with each other.
     """
     g = np.ascontiguousarray(g, dtype=F32)
-    return g.view(U32) & U32(0x7FFFFFFF)
+    key = g.view(U32) & U32(0x7FFFFFFF)
+    key[np.isnan(g)] = U32(0x7FFFFFFF)
+    return key
 
 
 def pack_bits(flags: np.ndarray) -> np.ndarray:

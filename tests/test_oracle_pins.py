@@ -72,10 +72,13 @@ def test_topk_worked_example():
     check_topk_golden()
 
 
+def _brute_key(x):
+    return 0x7FFFFFFF if math.isnan(x) else (_bits_of(x) & 0x7FFFFFFF)
+
+
 def _brute_topk(vals, k):
     """Python sort of (-|x| bit pattern, index): the definition, by brute force."""
-    keyed = sorted(range(len(vals)),
-                   key=lambda i: (-(_bits_of(vals[i]) & 0x7FFFFFFF), i))
+    keyed = sorted(range(len(vals)), key=lambda i: (-_brute_key(vals[i]), i))
     return sorted(keyed[:k])
 
 
@@ -86,6 +89,7 @@ def _tiny_cases(rng):
         yield [rng.uniform(-1, 1) for _ in range(n)]               # distinct
         yield [rng.choice([0.25, -0.25]) for _ in range(n)]        # all one key
         yield [float("inf") if i % 7 == 3 else rng.gauss(0, 1) for i in range(n)]
+        yield [float("nan") if i % 5 == 1 else rng.choice(levels) for i in range(n)]
 
 
 def check_topk_bruteforce(topk_indices=None):
@@ -106,6 +110,11 @@ def test_topk_nan_ranks_above_inf():
     g = np.array([1.0, np.inf, np.nan, -np.inf, 2.0], dtype=F32)
     assert oracle.topk_indices(g, 1).tolist() == [2]
     assert oracle.topk_indices(g, 3).tolist() == [1, 2, 3]
+    # NaNs tie whatever their payload: the lower index wins
+    raw = np.array([0x7FC00000, 0x7FC00001, 0xFFC00000, 0x7F800001, 0x3F800000], np.uint32)
+    g = raw.view(F32)
+    assert oracle.topk_indices(g, 2).tolist() == [0, 1]
+    assert oracle.topk_indices(g, 4).tolist() == [0, 1, 2, 3]
 
 
 def test_topk_matches_torch_stable_sort():
