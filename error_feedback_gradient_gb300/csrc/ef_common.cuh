@@ -1,0 +1,278 @@
+// Shared internals of libefgrad: device helpers (scans, bounded decoupled
+// look-back, block radix select) and host helpers (status, profiling hook,
+// device properties).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "efgrad.h"
+
+namespace ef {
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+  size_t max_smem_optin = 0;
+};
+
+// Properties of the current device (cached per device).  Returns EF_OK,
+// EF_ERR_ARCH (not compute capability 10.3) or EF_ERR_CUDA.
+ef_status current_device(DeviceInfo* out);
+
+// Record the failing CUDA error for ef_last_cuda_error() and map to a status.
+ef_status cuda_fail(cudaError_t err);
+
+// Check the last launch; returns EF_OK or EF_ERR_CUDA.
+ef_status check_launch();
+
+// Profiling hook: record the thread's start/stop event for `kernel_id`
+// around a launch, if set.
+void prof_begin(int kernel_id, cudaStream_t s);
+void prof_end(int kernel_id, cudaStream_t s);
+
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  if (!a || !b || abytes == 0 || bbytes == 0) return false;
+  uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bbytes && y < x + abytes;
+}
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Every workspace starts with this header; `status` is what
+// ef_workspace_status() reports.
+struct alignas(256) WsHeader {
+  int32_t status;
+  uint32_t reserved[63];
+};
+
+// ---------------------------------------------------------------------------
+// device side
+// ---------------------------------------------------------------------------
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t abs_key(float x) {
+  return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_volatile(const int32_t* p) {
+  return *reinterpret_cast<const volatile int32_t*>(p);
+}
+
+// Warp inclusive scan of a uint32.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const unsigned lane = lane_id();
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t t = __shfl_up_sync(kFull, v, o);
+    if (lane >= (unsigned)o) v += t;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Block exclusive scan of a uint32 (blockDim.x a multiple of 32, <= 1024).
+// `scratch` holds >= 33 words of shared memory.  Returns the exclusive prefix;
+// *total receives the block sum.  Contains __syncthreads().
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch,
+                                                    uint32_t* total) {
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const unsigned nwarps = blockDim.x >> 5;
+  uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < nwarps ? scratch[lane] : 0u;
+    uint32_t wi = warp_incl_scan(w);
+    if (lane < nwarps) scratch[lane] = wi - w;
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  uint32_t res = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
+// ---------------------------------------------------------------------------
+// Decoupled look-back (single-pass prefix over ordered tiles).
+//
+// A tile's state word holds a 2-bit flag in bits 63..62 and a 62-bit payload
+// that adds without carries between its fields.  Tile ids are handed out in
+// order by an atomic ticket, so every predecessor of a running tile is itself
+// running or finished and the wait always ends; it is still bounded by a
+// wall-clock limit, after which the status word gets EF_ERR_DEVICE_TIMEOUT
+// and the tile proceeds with what it has (no hang, outputs unspecified).
+// ---------------------------------------------------------------------------
+
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagIncl = 2ull << 62;
+constexpr uint64_t kPayloadMask = (1ull << 62) - 1;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Called by all 32 lanes of ONE warp.  `states` indexes tiles globally;
+// the chain of this tile starts at `first` (exclusive prefix 0 there).
+// Publishes this tile's aggregate, looks back, publishes the inclusive prefix
+// and returns the exclusive prefix (same value in every lane).
+__device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile,
+                                                  int64_t first, uint64_t agg,
+                                                  int32_t* status) {
+  const unsigned lane = lane_id();
+  if (tile == first) {
+    if (lane == 0) st_release(&states[tile], kFlagIncl | agg);
+    return 0;
+  }
+  if (lane == 0) st_release(&states[tile], kFlagAgg | agg);
+  uint64_t excl = 0;
+  int64_t base = tile - 1;
+  const uint64_t t0 = global_ns();
+  bool gave_up = false;
+  while (base >= first) {
+    const int64_t t = base - (int64_t)lane;
+    uint64_t s = (t >= first) ? ld_acquire(&states[t]) : kFlagIncl;
+    uint32_t spins = 0;
+    while (__any_sync(kFull, (s >> 62) == 0)) {
+      if ((s >> 62) == 0) s = ld_acquire(&states[t]);
+      if ((++spins & 63u) == 0) {
+        int bad = 0;
+        if (lane == 0)
+          bad = (global_ns() - t0 > kWaitLimitNs) || (ld_volatile(status) != 0) ||
+                spins > (1u << 26);
+        bad = __shfl_sync(kFull, bad, 0);
+        if (bad) {
+          if (lane == 0) set_status(status, EF_ERR_DEVICE_TIMEOUT);
+          gave_up = true;
+          break;
+        }
+      }
+      __nanosleep(32);
+    }
+    if (gave_up) break;
+    const unsigned incl = __ballot_sync(kFull, (s >> 62) == 2);
+    if (incl) {
+      const int stop = __ffs(incl) - 1;
+      uint64_t v = (lane <= (unsigned)stop) ? (s & kPayloadMask) : 0;
+      excl += warp_sum_u64(v);
+      break;
+    }
+    excl += warp_sum_u64(s & kPayloadMask);
+    base -= 32;
+  }
+  if (lane == 0) st_release(&states[tile], kFlagIncl | ((excl + agg) & kPayloadMask));
+  return excl;
+}
+
+// ---------------------------------------------------------------------------
+// Block radix select over keys in shared memory.
+//
+// Finds the k-th largest (1 <= k <= n) key T of keys[0..n), each key taken as
+// its low 31 bits (so float bit patterns give |x| keys): after the call,
+// gt = #keys > T and need = k - gt (>= 1 keys equal to T are taken, lowest
+// positions first).  Digits: bits 30..20 (2048 bins), 19..10, 9..0.
+// `hist` holds 2048 words of shared memory, `scratch` >= 40 words.
+// All threads of the block must call it.
+// ---------------------------------------------------------------------------
+
+struct SelectResult {
+  uint32_t T;
+  uint32_t gt;
+  uint32_t need;
+};
+
+// Given a histogram of `nbins` bins in shared memory and a rank `krem`
+// (1-based, counted from the top bin), find the bin b holding that rank and
+// the count of entries in bins above it.  All threads call it; results are
+// returned to every thread.
+__device__ __forceinline__ void block_find_bin(const uint32_t* hist, int nbins, uint32_t krem,
+                                               uint32_t* scratch, uint32_t* bin_out,
+                                               uint32_t* above_out) {
+  const int per = (nbins + blockDim.x - 1) / blockDim.x;
+  // thread t owns positions [t*per, (t+1)*per) counted from the top bin
+  uint32_t local = 0;
+  for (int q = threadIdx.x * per; q < (int)(threadIdx.x + 1) * per && q < nbins; ++q)
+    local += hist[nbins - 1 - q];
+  uint32_t total;
+  uint32_t excl = block_excl_scan(local, scratch, &total);
+  if (excl < krem && krem <= excl + local) {
+    uint32_t cum = excl;
+    for (int q = threadIdx.x * per; q < (int)(threadIdx.x + 1) * per && q < nbins; ++q) {
+      const uint32_t c = hist[nbins - 1 - q];
+      if (cum + c >= krem) {
+        scratch[36] = (uint32_t)(nbins - 1 - q);
+        scratch[37] = cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  *bin_out = scratch[36];
+  *above_out = scratch[37];
+  __syncthreads();
+}
+
+__device__ __forceinline__ SelectResult block_radix_select(const uint32_t* keys, int n, uint32_t k,
+                                                           uint32_t* hist, uint32_t* scratch) {
+  const int shifts[3] = {20, 10, 0};
+  const int widths[3] = {11, 10, 10};
+  uint32_t prefix = 0, krem = k, gt = 0;
+  for (int p = 0; p < 3; ++p) {
+    const int shift = shifts[p], nb = 1 << widths[p];
+    const int hi = shift + widths[p];  // bits above this digit are fixed
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t key = keys[i] & 0x7FFFFFFFu;
+      if (hi >= 31 || (key >> hi) == (prefix >> hi))
+        atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    uint32_t bin, above;
+    block_find_bin(hist, nb, krem, scratch, &bin, &above);
+    prefix |= bin << shift;
+    gt += above;
+    krem -= above;
+  }
+  return SelectResult{prefix, gt, krem};
+}
+
+}  // namespace ef

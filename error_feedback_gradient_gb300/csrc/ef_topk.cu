@@ -1,0 +1,773 @@
+// Top-k error feedback, sender side ("梯度稀疏化：只传输重要的梯度元素",
+// §详细算法流程 steps 2-5, per tensor as §分层自适应Top-k describes):
+//   g = g_raw + e;  S = k largest |g| (ties -> lower index);
+//   e' = g off S, +0 on S;  packet = (g[i], i) for i in S, ascending i.
+//
+// Segments of at most kSmallMax elements are finished by one CTA each with
+// the whole segment in shared memory (compensate, 3-digit radix select,
+// ordered emit).  Longer segments take the streaming path, batched over all
+// such segments of a call:
+//   1. prepare  (one CTA per segment): sample 32768 compensated keys and take
+//      a conservative lower threshold T_lo from them (only a speed-up: the
+//      result never depends on it).
+//   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e;
+//      every key >= T_lo is appended, in index order, to a per-segment
+//      candidate list via warp ballots and a bounded decoupled look-back.
+//      The last CTA checks each list: between k and its capacity -> select
+//      on the list; otherwise (T_lo too high or overflow) -> select on the
+//      whole segment, which is always correct, only slower.
+//   3. select   (x3): radix select on 11/10/10-bit digits of the keys of
+//      each list, shared-memory histograms merged into one per segment; the
+//      last CTA of each pass fixes that digit.  Result: the k-th key T and
+//      need = k - #(key > T).
+//   4. emit     ordered compaction of the list: an entry is taken when
+//      key > T, or key == T and fewer than `need` equal keys precede it;
+//      position = #(key > T before it) + min(#(key == T before it), need).
+//      Writes values, int32 indices or bitmap bits, and e = +0 there.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "ef_common.cuh"
+
+namespace ef {
+namespace {
+
+constexpr int kSmallMax = 32768;
+constexpr int kSmallThreads = 1024;
+constexpr int kTile = 8192;  // elements per fused-pass tile (8 warps x 1024)
+constexpr int kFusedThreads = 256;
+constexpr int kSample = 32768;
+constexpr int kPrepThreads = 1024;
+constexpr int kChunk = 4096;  // list entries per select / emit chunk
+constexpr int kSelThreads = 512;
+constexpr int kEmitThreads = 256;  // 8 warps x 16 rounds x 32 lanes = kChunk
+constexpr int kMaxLarge = 128;     // segments per streaming batch
+constexpr int kMaxSmall = 512;     // segments per small-path launch
+constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
+
+static_assert(kFusedThreads / 32 * 1024 == kTile, "tile layout");
+static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
+
+struct SmallSeg {
+  int64_t off;
+  int64_t out_off;
+  int32_t len;
+  int32_t k;
+};
+
+struct SmallBatch {
+  SmallSeg seg[kMaxSmall];
+};
+
+struct LargeSeg {
+  int64_t off, len, k, out_off;
+  int64_t cand_base, cap;
+  int64_t tile_base;  // global id of the segment's first fused tile
+  int64_t q_first;    // index of that tile in aligned kTile units
+  int64_t rank;       // sample rank for T_lo (0: no candidates, > kSample: all)
+};
+
+struct LargeBatch {
+  LargeSeg seg[kMaxLarge];
+};
+
+struct SegState {
+  LargeSeg d;
+  uint32_t t_lo;
+  uint32_t mode;  // 0: select on candidates, 1: select on the whole segment
+  int64_t list_len;
+  int64_t chunk_base;
+  uint32_t prefix;  // radix-select digits fixed so far (= T after pass 3)
+  uint32_t krem;    // rank still to find inside the prefix (= need)
+  uint32_t gt;
+  uint32_t pad;
+};
+
+struct alignas(256) Ctl {
+  uint32_t fused_ticket, fused_done;
+  uint32_t emit_ticket;
+  uint32_t sel_done[3];
+  int64_t total_chunks;
+};
+
+struct IO {
+  const float* g_raw;
+  float* e;
+  float* out_values;
+  int32_t* out_indices;
+  uint32_t* out_bitmap;
+  int32_t* status;
+};
+
+// Writes packet entry `pos` (must lie below `limit`, the segment's packet end;
+// anything else would be a library defect and is recorded, not written).
+__device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t pos, int64_t limit,
+                                         float v) {
+  if (pos >= limit) {
+    set_status(io.status, EF_ERR_INTERNAL);
+    return;
+  }
+  io.out_values[pos] = v;
+  if (io.out_indices) io.out_indices[pos] = (int32_t)gidx;
+  if (io.out_bitmap) atomicOr(io.out_bitmap + (gidx >> 5), 1u << (gidx & 31));
+  io.e[gidx] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// small segments: one CTA holds the whole segment
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kSmallThreads)
+topk_small(SmallBatch b, IO io, int keys_words) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* gbits = sm;
+  uint32_t* hist = sm + keys_words;
+  uint32_t* scratch = hist + 2048;
+  const SmallSeg sg = b.seg[blockIdx.x];
+  const int len = sg.len;
+  const float* gr = io.g_raw + sg.off;
+  float* e = io.e + sg.off;
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    const float x = __fadd_rn(gr[i], e[i]);
+    e[i] = x;
+    gbits[i] = __float_as_uint(x);
+  }
+  __syncthreads();
+  if (sg.k == 0) return;
+  const SelectResult r = block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch);
+  uint32_t run_gt = 0, run_eq = 0;
+  for (int r0 = 0; r0 < len; r0 += blockDim.x) {
+    const int i = r0 + threadIdx.x;
+    const bool in = i < len;
+    const uint32_t bits = in ? gbits[i] : 0u;
+    const uint32_t key = bits & 0x7FFFFFFFu;
+    const bool gt = in && key > r.T;
+    const bool eq = in && key == r.T;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(((uint32_t)gt << 16) | (uint32_t)eq, scratch, &tot);
+    const uint32_t gt_before = run_gt + (ex >> 16);
+    const uint32_t eq_before = run_eq + (ex & 0xFFFFu);
+    if (gt || (eq && eq_before < r.need)) {
+      const int64_t pos = sg.out_off + gt_before + min(eq_before, r.need);
+      emit_one(io, sg.off + i, pos, sg.out_off + sg.k, __uint_as_float(bits));
+    }
+    run_gt += tot >> 16;
+    run_eq += tot & 0xFFFFu;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// streaming path
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kPrepThreads)
+topk_prepare(LargeBatch b, int nseg, IO io, SegState* st) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* keys = sm;
+  uint32_t* hist = sm + kSample;
+  uint32_t* scratch = hist + 2048;
+  const int s = blockIdx.x;
+  if (s >= nseg) return;
+  const LargeSeg d = b.seg[s];
+  uint32_t t_lo;
+  if (d.rank <= 0) {
+    t_lo = kNoCandidate;
+  } else if (d.rank > kSample) {
+    t_lo = 0;
+  } else {
+    for (int j = threadIdx.x; j < kSample; j += blockDim.x) {
+      const int64_t p = d.off + ((2 * (int64_t)j + 1) * d.len) / (2 * (int64_t)kSample);
+      keys[j] = abs_key(__fadd_rn(io.g_raw[p], io.e[p]));
+    }
+    __syncthreads();
+    t_lo = block_radix_select(keys, kSample, (uint32_t)d.rank, hist, scratch).T;
+  }
+  if (threadIdx.x == 0) {
+    SegState v;
+    v.d = d;
+    v.t_lo = t_lo;
+    v.mode = 0;
+    v.list_len = 0;
+    v.chunk_base = 0;
+    v.prefix = 0;
+    v.krem = (uint32_t)d.k;
+    v.gt = 0;
+    v.pad = 0;
+    st[s] = v;
+  }
+}
+
+__device__ __forceinline__ int find_seg(const int64_t* base, int nseg, int64_t x) {
+  int lo = 0, hi = nseg - 1;  // largest s with base[s] <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void set4(float4& v, int c, float x) {
+  if (c == 0) v.x = x; else if (c == 1) v.y = x; else if (c == 2) v.z = x; else v.w = x;
+}
+__device__ __forceinline__ float get4(const float4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 2)
+topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
+           uint2* cand, Ctl* ctl, int phase, int vec) {
+  __shared__ int64_t s_base[kMaxLarge + 1];
+  __shared__ uint32_t s_wcnt[kFusedThreads / 32];
+  __shared__ uint32_t s_woff[kFusedThreads / 32];
+  __shared__ int64_t s_tile;
+  __shared__ uint64_t s_excl;
+  __shared__ int s_last;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_base[i] = st[i].d.tile_base;
+  if (threadIdx.x == 0) s_base[nseg] = total_tiles;
+
+  for (;;) {
+    if (threadIdx.x == 0) s_tile = atomicAdd(&ctl->fused_ticket, 1u);
+    __syncthreads();
+    const int64_t tile = s_tile;
+    if (tile >= total_tiles) break;
+    const int seg = find_seg(s_base, nseg, tile);
+    const int64_t a = st[seg].d.off, bnd = a + st[seg].d.len;
+    const int64_t tbase = s_base[seg];
+    const uint32_t t_lo = st[seg].t_lo;
+    const int64_t q0 = (st[seg].d.q_first + (tile - tbase)) * kTile + warp * 1024;
+
+    float4 gr[8], ee[8];
+    bool full[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int64_t i = q0 + r * 128 + lane * 4 - phase;
+      full[r] = vec && i >= a && i + 4 <= bnd;
+      if (full[r]) {
+        gr[r] = __ldcs(reinterpret_cast<const float4*>(io.g_raw + i));
+        ee[r] = __ldcs(reinterpret_cast<const float4*>(io.e + i));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool in = i + c >= a && i + c < bnd;
+          set4(gr[r], c, in ? io.g_raw[i + c] : 0.0f);
+          set4(ee[r], c, in ? io.e[i + c] : 0.0f);
+        }
+      }
+    }
+    uint32_t mask = 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int64_t i = q0 + r * 128 + lane * 4 - phase;
+      float4 g;
+      g.x = __fadd_rn(gr[r].x, ee[r].x);
+      g.y = __fadd_rn(gr[r].y, ee[r].y);
+      g.z = __fadd_rn(gr[r].z, ee[r].z);
+      g.w = __fadd_rn(gr[r].w, ee[r].w);
+      gr[r] = g;
+      if (full[r]) {
+        __stcs(reinterpret_cast<float4*>(io.e + i), g);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          mask |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << (r * 4 + c);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool in = i + c >= a && i + c < bnd;
+          if (in) {
+            io.e[i + c] = get4(g, c);
+            mask |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << (r * 4 + c);
+          }
+        }
+      }
+    }
+    uint32_t wcnt = __popc(mask);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wcnt += __shfl_xor_sync(kFull, wcnt, o);
+    if (lane == 0) s_wcnt[warp] = wcnt;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t c = lane < kFusedThreads / 32 ? s_wcnt[lane] : 0u;
+      const uint32_t inc = warp_incl_scan(c);
+      if (lane < kFusedThreads / 32) s_woff[lane] = inc - c;
+      const uint32_t agg = __shfl_sync(kFull, inc, 31);
+      const uint64_t excl = lookback_warp(tstate, tile, tbase, agg, io.status);
+      if (lane == 0) s_excl = excl;
+    }
+    __syncthreads();
+    if (wcnt) {  // warp-uniform
+      const int64_t cap = st[seg].d.cap;
+      uint2* out = cand + st[seg].d.cand_base;
+      int64_t run = (int64_t)s_excl + s_woff[warp];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t nib = (mask >> (r * 4)) & 0xFu;
+        const uint32_t cnt = __popc(nib);
+        const uint32_t inc = warp_incl_scan(cnt);
+        int64_t pos = run + inc - cnt;
+        const int64_t i = q0 + r * 128 + lane * 4 - phase;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if ((nib >> c) & 1u) {
+            if (pos < cap)
+              out[pos] = make_uint2((uint32_t)(i + c - a), __float_as_uint(get4(gr[r], c)));
+            ++pos;
+          }
+        }
+        run += __shfl_sync(kFull, inc, 31);
+      }
+    }
+    __syncthreads();
+  }
+
+  // The last CTA to finish decides, per segment, which list the select runs on.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ctl->fused_done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+    const LargeSeg& d = st[s].d;
+    const uint64_t w = ld_acquire(&tstate[s_base[s + 1] - 1]);
+    const int64_t c = (w >> 62) == 2 ? (int64_t)(w & kPayloadMask) : -1;
+    uint32_t mode = (c >= d.k && c <= d.cap) ? 0u : 1u;
+    int64_t len = mode == 0 ? c : d.len;
+    if (d.k == 0) { mode = 0; len = 0; }
+    st[s].mode = mode;
+    st[s].list_len = len;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    for (int s = 0; s < nseg; ++s) {
+      st[s].chunk_base = acc;
+      acc += (st[s].list_len + kChunk - 1) / kChunk;
+    }
+    ctl->total_chunks = acc;
+  }
+}
+
+// Entry j of a segment's select list: (local index, float bits), taken from
+// the candidate list (mode 0) or straight from the segment (mode 1).
+struct ListRef {
+  uint32_t mode;
+  int64_t cand_base, off, len;
+};
+
+__device__ __forceinline__ ListRef list_ref(const SegState* st, int seg) {
+  ListRef r;
+  r.mode = st[seg].mode;
+  r.cand_base = st[seg].d.cand_base;
+  r.off = st[seg].d.off;
+  r.len = st[seg].list_len;
+  return r;
+}
+
+__device__ __forceinline__ uint32_t list_bits(const ListRef& l, const IO& io, const uint2* cand,
+                                              int64_t j, uint32_t* local) {
+  if (l.mode == 0) {
+    const uint2 v = cand[l.cand_base + j];
+    *local = v.x;
+    return v.y;
+  }
+  *local = (uint32_t)j;
+  return __float_as_uint(io.e[l.off + j]);
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, Ctl* ctl,
+            int pass) {
+  __shared__ uint32_t sh[2048];
+  __shared__ int64_t s_cb[kMaxLarge + 1];
+  __shared__ uint32_t scratch[64];
+  __shared__ int s_last;
+  const int shift = pass == 0 ? 20 : (pass == 1 ? 10 : 0);
+  const int nb = pass == 0 ? 2048 : 1024;
+  const int hi = shift + (pass == 0 ? 11 : 10);
+  const int64_t total = *reinterpret_cast<volatile int64_t*>(&ctl->total_chunks);
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_cb[i] = st[i].chunk_base;
+  if (threadIdx.x == 0) s_cb[nseg] = total;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) sh[b] = 0;
+  __syncthreads();
+  for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
+    const int seg = find_seg(s_cb, nseg, c);
+    const ListRef l = list_ref(st, seg);
+    const uint32_t prefix = st[seg].prefix;
+    const int64_t j0 = (c - s_cb[seg]) * kChunk;
+    const int64_t j1 = min(j0 + (int64_t)kChunk, l.len);
+    for (int64_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+      uint32_t local;
+      const uint32_t key = list_bits(l, io, cand, j, &local) & 0x7FFFFFFFu;
+      if (hi >= 31 || (key >> hi) == (prefix >> hi))
+        atomicAdd(&sh[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+      const uint32_t v = sh[b];
+      if (v) {
+        atomicAdd(&ghist[(int64_t)seg * 2048 + b], v);
+        sh[b] = 0;
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ctl->sel_done[pass], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int seg = 0; seg < nseg; ++seg) {
+    if (st[seg].d.k == 0) continue;
+    uint32_t* gh = ghist + (int64_t)seg * 2048;
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+      sh[b] = *reinterpret_cast<volatile uint32_t*>(&gh[b]);
+      gh[b] = 0;
+    }
+    __syncthreads();
+    uint32_t bin, above;
+    block_find_bin(sh, nb, st[seg].krem, scratch, &bin, &above);
+    if (threadIdx.x == 0) {
+      st[seg].prefix |= bin << shift;
+      st[seg].krem -= above;
+      st[seg].gt += above;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kEmitThreads)
+topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ctl* ctl) {
+  __shared__ int64_t s_cb[kMaxLarge + 1];
+  __shared__ uint32_t s_wgt[kEmitThreads / 32], s_weq[kEmitThreads / 32];
+  __shared__ uint32_t s_ogt[kEmitThreads / 32], s_oeq[kEmitThreads / 32];
+  __shared__ int64_t s_c;
+  __shared__ uint64_t s_excl;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int64_t total = *reinterpret_cast<volatile int64_t*>(&ctl->total_chunks);
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_cb[i] = st[i].chunk_base;
+  if (threadIdx.x == 0) s_cb[nseg] = total;
+  for (;;) {
+    if (threadIdx.x == 0) s_c = atomicAdd(&ctl->emit_ticket, 1u);
+    __syncthreads();
+    const int64_t c = s_c;
+    if (c >= total) break;
+    const int seg = find_seg(s_cb, nseg, c);
+    const ListRef l = list_ref(st, seg);
+    const uint32_t T = st[seg].prefix, need = st[seg].krem;
+    const int64_t seg_off = st[seg].d.off, out_off = st[seg].d.out_off;
+    const int64_t out_end = out_off + st[seg].d.k;
+    const int64_t jw = (c - s_cb[seg]) * kChunk + warp * 512;
+    uint32_t vb[16], loc[16];
+    uint32_t gtm = 0, eqm = 0;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int64_t j = jw + r * 32 + lane;
+      if (j < l.len) {
+        vb[r] = list_bits(l, io, cand, j, &loc[r]);
+        const uint32_t key = vb[r] & 0x7FFFFFFFu;
+        gtm |= (uint32_t)(key > T) << r;
+        eqm |= (uint32_t)(key == T) << r;
+      } else {
+        vb[r] = 0;
+        loc[r] = 0;
+      }
+    }
+    uint32_t cg = __popc(gtm), ce = __popc(eqm);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cg += __shfl_xor_sync(kFull, cg, o);
+      ce += __shfl_xor_sync(kFull, ce, o);
+    }
+    if (lane == 0) {
+      s_wgt[warp] = cg;
+      s_weq[warp] = ce;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t a = lane < kEmitThreads / 32 ? s_wgt[lane] : 0u;
+      const uint32_t b = lane < kEmitThreads / 32 ? s_weq[lane] : 0u;
+      const uint32_t ia = warp_incl_scan(a), ib = warp_incl_scan(b);
+      if (lane < kEmitThreads / 32) {
+        s_ogt[lane] = ia - a;
+        s_oeq[lane] = ib - b;
+      }
+      const uint64_t agg = ((uint64_t)__shfl_sync(kFull, ia, 31) << 31) |
+                           (uint64_t)__shfl_sync(kFull, ib, 31);
+      const uint64_t excl = lookback_warp(cstate, c, s_cb[seg], agg, io.status);
+      if (lane == 0) s_excl = excl;
+    }
+    __syncthreads();
+    if (cg | ce) {  // warp-uniform
+      uint32_t run_gt = (uint32_t)(s_excl >> 31) + s_ogt[warp];
+      uint32_t run_eq = (uint32_t)(s_excl & 0x7FFFFFFFu) + s_oeq[warp];
+      const unsigned lt = lanemask_lt();
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const bool g = (gtm >> r) & 1u, q = (eqm >> r) & 1u;
+        const unsigned bg = __ballot_sync(kFull, g), bq = __ballot_sync(kFull, q);
+        const uint32_t gt_before = run_gt + __popc(bg & lt);
+        const uint32_t eq_before = run_eq + __popc(bq & lt);
+        if (g || (q && eq_before < need)) {
+          const int64_t pos = out_off + gt_before + min(eq_before, need);
+          emit_one(io, seg_off + loc[r], pos, out_end, __uint_as_float(vb[r]));
+        }
+        run_gt += __popc(bg);
+        run_eq += __popc(bq);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host planning
+// ---------------------------------------------------------------------------
+
+struct Batch {
+  std::vector<LargeSeg> segs;
+  int64_t max_tiles = 0;   // upper bound over address phases
+  int64_t max_chunks = 0;  // every list at its longest (whole segment)
+  int64_t cand_total = 0;
+};
+
+struct Plan {
+  std::vector<SmallSeg> small;
+  int small_max_len = 0;
+  std::vector<Batch> batches;
+  int64_t total_k = 0;
+  // workspace regions (byte offsets); batches reuse the same regions
+  size_t off_ctl = 0, off_st = 0, off_hist = 0, off_tiles = 0, off_chunks = 0, off_cand = 0;
+  size_t ctl_clear_bytes = 0;  // bytes cleared from off_ctl before each batch
+  size_t bytes = 0;
+};
+
+int64_t sample_rank(int64_t k, int64_t len) {
+  if (k <= 0) return 0;
+  const double m = (double)k * kSample / (double)len;
+  const double r = std::ceil(m + 5.0 * std::sqrt(m) + 10.0);
+  return r > (double)kSample ? (int64_t)kSample + 1 : (int64_t)r;
+}
+
+ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* ks,
+                    int32_t idx_format, Plan* p) {
+  if (n < 0) return EF_ERR_SIZE;
+  if (nseg < 1) return EF_ERR_SEGMENTS;
+  if (!offs || !ks) return EF_ERR_NULL;
+  if (idx_format != EF_IDX_INT32 && idx_format != EF_IDX_BITMAP) return EF_ERR_ARG;
+  if (idx_format == EF_IDX_INT32 && n > (int64_t(1) << 31)) return EF_ERR_SIZE;
+  if (offs[0] != 0 || offs[nseg] != n) return EF_ERR_SEGMENTS;
+  int64_t out_off = 0;
+  Batch cur;
+  for (int32_t s = 0; s < nseg; ++s) {
+    const int64_t a = offs[s], b = offs[s + 1];
+    if (b < a) return EF_ERR_SEGMENTS;
+    const int64_t len = b - a;
+    if (len > (int64_t(1) << 31) - 1) return EF_ERR_SIZE;
+    const int64_t k = ks[s];
+    if (k < 0 || k > len) return EF_ERR_K;
+    if (len == 0) continue;
+    if (len <= kSmallMax) {
+      p->small.push_back(SmallSeg{a, out_off, (int32_t)len, (int32_t)k});
+      p->small_max_len = std::max<int>(p->small_max_len, (int)len);
+    } else {
+      LargeSeg d{};
+      d.off = a;
+      d.len = len;
+      d.k = k;
+      d.out_off = out_off;
+      d.cap = std::min<int64_t>(len, 4 * k + 65536);
+      d.cand_base = cur.cand_total;
+      d.rank = sample_rank(k, len);
+      cur.cand_total += d.cap;
+      cur.max_tiles += (len + kTile - 1) / kTile + 1;
+      cur.max_chunks += (len + kChunk - 1) / kChunk;
+      cur.segs.push_back(d);
+      if ((int)cur.segs.size() == kMaxLarge) {
+        p->batches.push_back(cur);
+        cur = Batch();
+      }
+    }
+    out_off += k;
+  }
+  if (!cur.segs.empty()) p->batches.push_back(cur);
+  p->total_k = out_off;
+
+  int64_t tiles = 0, chunks = 0, cands = 0;
+  for (const Batch& b : p->batches) {
+    tiles = std::max(tiles, b.max_tiles);
+    chunks = std::max(chunks, b.max_chunks);
+    cands = std::max(cands, b.cand_total);
+  }
+  size_t off = sizeof(WsHeader);
+  if (!p->batches.empty()) {
+    p->off_ctl = off;
+    off += sizeof(Ctl);
+    p->off_st = off;
+    off = round_up(off + sizeof(SegState) * kMaxLarge, 256);
+    p->off_hist = off;
+    off = round_up(off + (size_t)kMaxLarge * 2048 * 4, 256);
+    p->off_tiles = off;
+    off = round_up(off + (size_t)tiles * 8, 256);
+    p->off_chunks = off;
+    off = round_up(off + (size_t)chunks * 8, 256);
+    p->ctl_clear_bytes = off - p->off_ctl;
+    p->off_cand = off;
+    off = round_up(off + (size_t)cands * 8, 256);
+  }
+  p->bytes = off;
+  return EF_OK;
+}
+
+std::once_flag g_attr_once[64];
+ef_status g_attr_status[64];
+
+ef_status set_attributes(int dev) {
+  if (dev < 0 || dev >= 64) return EF_ERR_ARCH;
+  std::call_once(g_attr_once[dev], [&]() {
+    const int small_smem = (kSmallMax + 2048 + 64) * 4;
+    const int prep_smem = (kSample + 2048 + 64) * 4;
+    cudaError_t e1 = cudaFuncSetAttribute(topk_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          small_smem);
+    cudaError_t e2 = cudaFuncSetAttribute(topk_prepare,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+    g_attr_status[dev] = (e1 == cudaSuccess && e2 == cudaSuccess)
+                             ? EF_OK
+                             : cuda_fail(e1 != cudaSuccess ? e1 : e2);
+  });
+  return g_attr_status[dev];
+}
+
+}  // namespace
+}  // namespace ef
+
+extern "C" ef_status ef_topk_workspace_size(int64_t n, int32_t nseg, const int64_t* h_seg_offsets,
+                                            const int64_t* h_seg_k, int32_t idx_format,
+                                            size_t* bytes) {
+  if (!bytes) return EF_ERR_NULL;
+  ef::Plan p;
+  ef_status st = ef::make_plan(n, nseg, h_seg_offsets, h_seg_k, idx_format, &p);
+  if (st != EF_OK) return st;
+  *bytes = p.bytes;
+  return EF_OK;
+}
+
+extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, int32_t nseg,
+                                      const int64_t* h_seg_offsets, const int64_t* h_seg_k,
+                                      int32_t idx_format, float* out_values,
+                                      int32_t* out_indices, uint32_t* out_bitmap,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace ef;
+  Plan p;
+  ef_status st = make_plan(n, nseg, h_seg_offsets, h_seg_k, idx_format, &p);
+  if (st != EF_OK) return st;
+  const bool bitmap = idx_format == EF_IDX_BITMAP;
+  if (!workspace) return EF_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < p.bytes)
+    return EF_ERR_WORKSPACE;
+  if (n > 0 && (!g_raw || !e)) return EF_ERR_NULL;
+  if (p.total_k > 0 && !out_values) return EF_ERR_NULL;
+  if (!bitmap && p.total_k > 0 && !out_indices) return EF_ERR_NULL;
+  if (bitmap && n > 0 && !out_bitmap) return EF_ERR_NULL;
+  if (!bitmap && out_bitmap) return EF_ERR_ARG;
+  if (bitmap && out_indices) return EF_ERR_ARG;
+  if ((g_raw && !aligned4(g_raw)) || (e && !aligned4(e)) || (out_values && !aligned4(out_values)) ||
+      (out_indices && !aligned4(out_indices)) || (out_bitmap && !aligned4(out_bitmap)))
+    return EF_ERR_ALIGN;
+  const size_t fb = (size_t)n * 4, kb = (size_t)p.total_k * 4, wb = (size_t)((n + 31) / 32) * 4;
+  const void* outs[2] = {out_values, bitmap ? (const void*)out_bitmap : (const void*)out_indices};
+  const size_t outb[2] = {kb, bitmap ? wb : kb};
+  if (overlaps(g_raw, fb, e, fb)) return EF_ERR_ALIAS;
+  for (int i = 0; i < 2; ++i) {
+    if (overlaps(outs[i], outb[i], g_raw, fb) || overlaps(outs[i], outb[i], e, fb) ||
+        overlaps(outs[i], outb[i], workspace, p.bytes))
+      return EF_ERR_ALIAS;
+  }
+  if (overlaps(outs[0], outb[0], outs[1], outb[1])) return EF_ERR_ALIAS;
+  if (overlaps(workspace, p.bytes, g_raw, fb) || overlaps(workspace, p.bytes, e, fb))
+    return EF_ERR_ALIAS;
+
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != EF_OK) return st;
+  int devid = 0;
+  cudaGetDevice(&devid);
+  if ((st = set_attributes(devid)) != EF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  cudaError_t err = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (n == 0) return EF_OK;
+  if (bitmap) {
+    err = cudaMemsetAsync(out_bitmap, 0, wb, s);
+    if (err != cudaSuccess) return cuda_fail(err);
+  }
+  IO io{g_raw, e, out_values, bitmap ? nullptr : out_indices, bitmap ? out_bitmap : nullptr,
+        reinterpret_cast<int32_t*>(ws)};
+
+  // small segments
+  for (size_t i0 = 0; i0 < p.small.size(); i0 += kMaxSmall) {
+    const size_t cnt = std::min<size_t>(kMaxSmall, p.small.size() - i0);
+    SmallBatch sb;
+    int maxlen = 0;
+    for (size_t i = 0; i < cnt; ++i) {
+      sb.seg[i] = p.small[i0 + i];
+      maxlen = std::max(maxlen, sb.seg[i].len);
+    }
+    const int keys_words = (maxlen + 3) & ~3;
+    const size_t smem = (size_t)(keys_words + 2048 + 64) * 4;
+    topk_small<<<(unsigned)cnt, kSmallThreads, smem, s>>>(sb, io, keys_words);
+    if ((st = check_launch()) != EF_OK) return st;
+  }
+
+  // streaming path
+  const int phase_g = (int)((reinterpret_cast<uintptr_t>(g_raw) >> 2) & 3u);
+  const int phase_e = (int)((reinterpret_cast<uintptr_t>(e) >> 2) & 3u);
+  const int vec = phase_g == phase_e ? 1 : 0;
+  const int phase = vec ? phase_g : 0;
+  Ctl* ctl = reinterpret_cast<Ctl*>(ws + p.off_ctl);
+  SegState* sst = reinterpret_cast<SegState*>(ws + p.off_st);
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(ws + p.off_hist);
+  uint64_t* tstate = reinterpret_cast<uint64_t*>(ws + p.off_tiles);
+  uint64_t* cstate = reinterpret_cast<uint64_t*>(ws + p.off_chunks);
+  uint2* cand = reinterpret_cast<uint2*>(ws + p.off_cand);
+  for (Batch& b : p.batches) {
+    LargeBatch lb;
+    int64_t tiles = 0;
+    const int nsg = (int)b.segs.size();
+    for (int i = 0; i < nsg; ++i) {
+      LargeSeg d = b.segs[i];
+      const int64_t qa = d.off + phase, qb = d.off + d.len + phase;
+      d.q_first = qa / kTile;
+      d.tile_base = tiles;
+      tiles += (qb - 1) / kTile - d.q_first + 1;
+      lb.seg[i] = d;
+    }
+    err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
+    if (err != cudaSuccess) return cuda_fail(err);
+    const size_t prep_smem = (size_t)(kSample + 2048 + 64) * 4;
+    topk_prepare<<<nsg, kPrepThreads, prep_smem, s>>>(lb, nsg, io, sst);
+    if ((st = check_launch()) != EF_OK) return st;
+    const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * 2);
+    prof_begin(EF_KERNEL_TOPK_FUSED, s);
+    topk_fused<<<fgrid, kFusedThreads, 0, s>>>(io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
+    if ((st = check_launch()) != EF_OK) return st;
+    prof_end(EF_KERNEL_TOPK_FUSED, s);
+    const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 2));
+    for (int pass = 0; pass < 3; ++pass) {
+      topk_select<<<sgrid, kSelThreads, 0, s>>>(io, sst, nsg, cand, ghist, ctl, pass);
+      if ((st = check_launch()) != EF_OK) return st;
+    }
+    const int egrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 4));
+    topk_emit<<<egrid, kEmitThreads, 0, s>>>(io, sst, nsg, cand, cstate, ctl);
+    if ((st = check_launch()) != EF_OK) return st;
+  }
+  return EF_OK;
+}

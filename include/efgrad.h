@@ -39,6 +39,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define EF_API __attribute__((visibility("default")))
+#else
+#define EF_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -61,6 +67,8 @@ typedef int32_t ef_status;
 #define EF_ERR_PACKET         13  /* device-side: packet indices not strictly ascending,
                                      out of range, or a bitmap whose population count
                                      differs from the stated k                         */
+#define EF_ERR_INTERNAL       14  /* device-side: a consistency check failed (a library
+                                     defect); the offending write was skipped           */
 
 #define EF_IDX_INT32   0  /* packet = fp32 values[k] + int32 global indices[k]        */
 #define EF_IDX_BITMAP  1  /* packet = fp32 values[k] + uint32 bitmap[ceil(n/32)]      */
@@ -72,14 +80,14 @@ typedef int32_t ef_status;
 #define EF_ABI_VERSION 1
 
 /* Library ABI version (EF_ABI_VERSION of the build). */
-int32_t ef_abi_version(void);
+EF_API int32_t ef_abi_version(void);
 
 /* Static, NUL-terminated description of a status code. */
-const char* ef_status_string(ef_status s);
+EF_API const char* ef_status_string(ef_status s);
 
 /* cudaError_t of the last failed CUDA call made by this thread inside the
  * library (0 if none). */
-int32_t ef_last_cuda_error(void);
+EF_API int32_t ef_last_cuda_error(void);
 
 /* ------------------------------------------------------------------------
  * Top-k error feedback, sender side.
@@ -113,12 +121,12 @@ int32_t ef_last_cuda_error(void);
  * e must not overlap.  The result is unique (the order above is total), so it
  * does not depend on the launch configuration.
  * ---------------------------------------------------------------------- */
-ef_status ef_topk_workspace_size(int64_t n, int32_t nseg,
+EF_API ef_status ef_topk_workspace_size(int64_t n, int32_t nseg,
                                  const int64_t* h_seg_offsets,
                                  const int64_t* h_seg_k, int32_t idx_format,
                                  size_t* bytes);
 
-ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
+EF_API ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
                            int32_t nseg, const int64_t* h_seg_offsets,
                            const int64_t* h_seg_k, int32_t idx_format,
                            float* out_values, int32_t* out_indices,
@@ -143,7 +151,7 @@ ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
  *          padding bits 0.  Must not overlap g or eps; g and eps must not
  *          overlap.
  * ---------------------------------------------------------------------- */
-ef_status ef_sign_compress(const float* g, float* eps, int64_t n, float beta1,
+EF_API ef_status ef_sign_compress(const float* g, float* eps, int64_t n, float beta1,
                            uint32_t* out_bits, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -173,10 +181,10 @@ ef_status ef_sign_compress(const float* g, float* eps, int64_t n, float beta1,
  * different from k_w) are never read out of bounds; they set EF_ERR_PACKET
  * in the workspace status and the outputs are then unspecified.
  * ---------------------------------------------------------------------- */
-ef_status ef_aggregate_workspace_size(int32_t W, int32_t idx_format, int64_t n,
+EF_API ef_status ef_aggregate_workspace_size(int32_t W, int32_t idx_format, int64_t n,
                                       size_t* bytes);
 
-ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
+EF_API ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
                                  const float* const* h_values,
                                  const int32_t* const* h_indices,
                                  const uint32_t* const* h_bitmaps,
@@ -200,7 +208,7 @@ ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
  * G           [n] fp32, written in full; may be NULL.
  * w_or_m      [n] fp32 parameters (SGD) or momentum (MOMENTUM), in place.
  * ---------------------------------------------------------------------- */
-ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bits,
+EF_API ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bits,
                                int64_t n, int32_t mode, float eta, float beta1,
                                float* G, float* w_or_m, void* stream);
 
@@ -210,7 +218,7 @@ ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bits,
  * EF_ERR_PACKET) to *device_status.  Each call that takes a workspace resets
  * the word when it starts.
  * ---------------------------------------------------------------------- */
-ef_status ef_workspace_status(const void* workspace, void* stream,
+EF_API ef_status ef_workspace_status(const void* workspace, void* stream,
                               int32_t* device_status);
 
 /* ------------------------------------------------------------------------
@@ -223,7 +231,7 @@ ef_status ef_workspace_status(const void* workspace, void* stream,
 #define EF_KERNEL_SIGN         2  /* 1-bit compress                           */
 #define EF_KERNEL_SPARSE_APPLY 3  /* dense tile merge + SGD                   */
 #define EF_KERNEL_SIGN_APPLY   4  /* 1-bit aggregate + SGD / momentum         */
-ef_status ef_profile_events(int32_t kernel_id, void* start_event,
+EF_API ef_status ef_profile_events(int32_t kernel_id, void* start_event,
                             void* stop_event);
 
 #ifdef __cplusplus

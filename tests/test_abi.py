@@ -1,0 +1,160 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/efgrad.h declares, and its host-side validation rejects bad
+arguments before touching the device (no compute calls here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import error_feedback_gradient_gb300 as efg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "efgrad.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(efg.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return efg.library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^EF_API\s+[\w\s\*]+?\b(\w+)\(", text, flags=re.M)
+
+
+def _header_defines():
+    text = open(HEADER).read()
+    return {m[0]: int(m[1]) for m in re.findall(r"^#define (EF_\w+)\s+(-?\d+)", text, flags=re.M)}
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_header(lib):
+    from error_feedback_gradient_gb300 import binding
+    assert set(_declared()) == set(binding._SIGNATURES)
+
+
+def test_constants_match_header():
+    d = _header_defines()
+    from error_feedback_gradient_gb300 import binding
+    assert d["EF_IDX_INT32"] == binding.IDX_INT32 and d["EF_IDX_BITMAP"] == binding.IDX_BITMAP
+    assert d["EF_APPLY_SGD"] == binding.APPLY_SGD
+    assert d["EF_APPLY_MOMENTUM"] == binding.APPLY_MOMENTUM
+    assert d["EF_KERNEL_TOPK_FUSED"] == binding.KERNEL_TOPK_FUSED
+
+
+def test_status_strings(lib):
+    d = _header_defines()
+    for name, v in d.items():
+        if name.startswith("EF_ERR_") or name == "EF_OK":
+            s = lib.ef_status_string(v)
+            assert s and b"unknown" not in s, name
+    assert lib.ef_abi_version() == d["EF_ABI_VERSION"]
+
+
+def _i64(xs):
+    return (ctypes.c_int64 * len(xs))(*xs)
+
+
+def _ws_size(lib, n, offs, ks, fmt=0):
+    out = ctypes.c_size_t(0)
+    st = lib.ef_topk_workspace_size(n, len(ks), _i64(offs), _i64(ks), fmt, ctypes.byref(out))
+    return st, out.value
+
+
+def test_topk_workspace_queries(lib):
+    d = _header_defines()
+    st, small = _ws_size(lib, 1000, [0, 1000], [10])
+    assert st == d["EF_OK"] and small >= 256
+    st, big = _ws_size(lib, 1 << 24, [0, 1 << 24], [16777])
+    assert st == d["EF_OK"] and big > 4 * 16777 * 8          # candidate list
+    st, _ = _ws_size(lib, 100, [0, 50, 100], [51, 1])
+    assert st == d["EF_ERR_K"]
+    st, _ = _ws_size(lib, 100, [0, 60, 50, 100], [1, 1, 1])
+    assert st == d["EF_ERR_SEGMENTS"]
+    st, _ = _ws_size(lib, 100, [0, 99], [1])
+    assert st == d["EF_ERR_SEGMENTS"]
+    st, _ = _ws_size(lib, 100, [0, 100], [1], fmt=7)
+    assert st == d["EF_ERR_ARG"]
+    st, _ = _ws_size(lib, (1 << 31) + 1, [0, 1 << 30, (1 << 31) + 1], [1, 1], fmt=0)
+    assert st == d["EF_ERR_SIZE"]                             # int32 indices overflow
+    st, _ = _ws_size(lib, (1 << 31) + 1, [0, 1 << 30, (1 << 31) + 1], [1, 1], fmt=1)
+    assert st == d["EF_OK"]                                   # bitmap has no index limit
+    st, _ = _ws_size(lib, 1 << 31, [0, 1 << 31], [1], fmt=1)
+    assert st == d["EF_ERR_SIZE"]                             # one segment >= 2^31
+
+
+def test_topk_rejects_before_device(lib):
+    d = _header_defines()
+    ws = ctypes.c_void_p(256 * 1000)           # never dereferenced: validation fails first
+    fake = ctypes.c_void_p(4096)
+    st = lib.ef_topk_compress(fake, ctypes.c_void_p(8192), 100, 1, _i64([0, 100]), _i64([101]),
+                              0, fake, fake, None, ws, 1 << 20, None)
+    assert st == d["EF_ERR_K"]
+    st = lib.ef_topk_compress(fake, ctypes.c_void_p(8192), 100, 1, _i64([0, 100]), _i64([5]),
+                              0, fake, fake, None, None, 0, None)
+    assert st == d["EF_ERR_WORKSPACE"]
+    st = lib.ef_topk_compress(fake, ctypes.c_void_p(8192), 100, 1, _i64([0, 100]), _i64([5]),
+                              0, fake, fake, None, ctypes.c_void_p(255), 1 << 20, None)
+    assert st == d["EF_ERR_WORKSPACE"]                        # misaligned
+    st = lib.ef_topk_compress(fake, fake, 100, 1, _i64([0, 100]), _i64([5]),
+                              0, ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), None, ws,
+                              1 << 20, None)
+    assert st == d["EF_ERR_ALIAS"]                            # g_raw == e
+    st = lib.ef_topk_compress(ctypes.c_void_p(4098), ctypes.c_void_p(1 << 20), 100, 1,
+                              _i64([0, 100]), _i64([5]), 0, ctypes.c_void_p(2 << 20),
+                              ctypes.c_void_p(3 << 20), None, ws, 1 << 20, None)
+    assert st == d["EF_ERR_ALIGN"]
+    st = lib.ef_topk_compress(fake, ctypes.c_void_p(1 << 20), 100, 1, _i64([0, 100]),
+                              _i64([5]), 0, None, ctypes.c_void_p(3 << 20), None, ws, 1 << 20,
+                              None)
+    assert st == d["EF_ERR_NULL"]
+
+
+def test_sign_rejects_before_device(lib):
+    d = _header_defines()
+    a, b, c = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    assert lib.ef_sign_compress(a, b, -1, 0.9, c, None) == d["EF_ERR_SIZE"]
+    assert lib.ef_sign_compress(a, b, 10, float("nan"), c, None) == d["EF_ERR_ARG"]
+    assert lib.ef_sign_compress(a, a, 10, 0.9, c, None) == d["EF_ERR_ALIAS"]
+    assert lib.ef_sign_compress(None, b, 10, 0.9, c, None) == d["EF_ERR_NULL"]
+    assert lib.ef_sign_compress(a, b, 0, 0.9, c, None) == d["EF_OK"]      # empty: no work
+    bits = (ctypes.c_void_p * 1)(c)
+    assert lib.sign_aggregate_apply(0, bits, 10, 0, 0.1, 0.9, None, a, None) == d["EF_ERR_WORKERS"]
+    assert lib.sign_aggregate_apply(1, bits, 10, 5, 0.1, 0.9, None, a, None) == d["EF_ERR_ARG"]
+    assert lib.sign_aggregate_apply(1, bits, 10, 0, float("inf"), 0.9, None, a,
+                                    None) == d["EF_ERR_ARG"]
+
+
+def test_aggregate_rejects_before_device(lib):
+    d = _header_defines()
+    out = ctypes.c_size_t(0)
+    assert lib.ef_aggregate_workspace_size(0, 0, 10, ctypes.byref(out)) == d["EF_ERR_WORKERS"]
+    assert lib.ef_aggregate_workspace_size(65, 0, 10, ctypes.byref(out)) == d["EF_ERR_WORKERS"]
+    assert lib.ef_aggregate_workspace_size(8, 1, 1 << 20, ctypes.byref(out)) == d["EF_OK"]
+    vals = (ctypes.c_void_p * 1)(ctypes.c_void_p(1 << 20))
+    inds = (ctypes.c_void_p * 1)(ctypes.c_void_p(2 << 20))
+    ws = ctypes.c_void_p(256 * 4096)
+    w = ctypes.c_void_p(3 << 20)
+    st = lib.sparse_aggregate_apply(1, 0, vals, inds, None, _i64([11]), 10, 0.1, None, w, ws,
+                                    1 << 20, None)
+    assert st == d["EF_ERR_K"]
+    st = lib.sparse_aggregate_apply(1, 0, vals, None, None, _i64([1]), 10, 0.1, None, w, ws,
+                                    1 << 20, None)
+    assert st == d["EF_ERR_NULL"]
+    st = lib.sparse_aggregate_apply(1, 0, vals, inds, None, _i64([1]), 10, 0.1, None, w, ws,
+                                    8, None)
+    assert st == d["EF_ERR_WORKSPACE"]
+    st = lib.sparse_aggregate_apply(1, 0, vals, inds, None, _i64([1]), 10, 0.1, w, w, ws,
+                                    1 << 20, None)
+    assert st == d["EF_ERR_ALIAS"]

@@ -1,0 +1,117 @@
+"""GPU parity of ef_topk_compress against the oracle (bit-exact)."""
+
+import numpy as np
+import pytest
+import torch
+
+import error_feedback_gradient_gb300 as efg
+from error_feedback_gradient_gb300 import workloads as wl
+from efcheck import check_topk_step, gpu_topk, host, assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FMTS = [efg.IDX_INT32, efg.IDX_BITMAP]
+
+
+def _t(n, seed, scale=1e-3):
+    return wl.student_t3(n, scale, seed, DEV)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_small_segments(fmt):
+    sizes = [1, 2, 3, 31, 32, 33, 100, 1000, 4096, 20000, 32767, 32768]
+    ks = [1, 0, 3, 5, 32, 1, 10, 17, 41, 200, 327, 1]
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    check_topk_step(_t(n, 1), _t(n, 2, 1e-4), offs, ks, fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(32769, 328), (100_003, 1000), (1 << 20, 10486),
+                                 (3_000_017, 3000), (200_000, 1), (40_000, 40_000),
+                                 (50_000, 0)])
+def test_single_streaming_segment(n, k, fmt):
+    check_topk_step(_t(n, 10 + n % 97), _t(n, 20 + n % 89, 1e-4), [0, n], [k], fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mixed_segments_and_empty(fmt):
+    sizes = [0, 64, 40000, 0, 1, 250_000, 7, 65_537, 32768, 32769]
+    ks = [0, 1, 400, 0, 1, 250, 7, 0, 16, 33]
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    check_topk_step(_t(n, 3), _t(n, 4, 1e-4), offs, ks, fmt)
+
+
+def test_ties_everywhere():
+    # one value everywhere: every candidate list overflows, the whole-segment
+    # select runs, and the lowest indices win
+    n = 300_000
+    g = torch.full((n,), 0.5, device=DEV)
+    check_topk_step(g, torch.zeros(n, device=DEV), [0, 100_000, n], [777, 5000])
+    # a few levels with +-0 and sign flips, many equal keys at the threshold
+    rng = np.random.default_rng(5)
+    lv = np.array([0.0, -0.0, 1e-3, -1e-3, 2e-3, -2e-3, 4e-3], np.float32)
+    g = torch.from_numpy(lv[rng.integers(0, lv.size, n)]).to(DEV)
+    check_topk_step(g, torch.zeros(n, device=DEV), [0, n], [60_000])
+    check_topk_step(g, torch.zeros(n, device=DEV), [0, 20_000, n], [3000, 200_000])
+
+
+def test_special_values():
+    n = 150_001
+    g = _t(n, 7)
+    g[::1000] = float("inf")
+    g[5::1003] = float("-inf")
+    g[7::2000] = float("nan")
+    g[9::97] = 1e-40          # denormal
+    g[11::89] = -0.0
+    # NaNs with different payloads and signs: all tie above +Inf
+    raw = g.view(torch.int32)
+    raw[13::3001] = 0x7FC00001
+    raw[17::3007] = -4194304          # 0xFFC00000
+    e = torch.zeros(n, device=DEV)
+    check_topk_step(g, e, [0, 1000, n], [3, 500])
+
+
+def test_unaligned_addresses():
+    n = 120_001
+    base_g = _t(n + 8, 8)
+    base_e = _t(n + 8, 9, 1e-4)
+    # same misalignment (16-byte path with a phase) ...
+    check_topk_step(base_g[1:n + 1], base_e[1:n + 1], [0, 5, 50_007, n], [1, 400, 700])
+    # ... and different misalignments (scalar path)
+    check_topk_step(base_g[2:n + 2], base_e[3:n + 3], [0, 5, 50_007, n], [1, 400, 700])
+
+
+def test_sampled_threshold_too_high_falls_back():
+    """Large values exactly at the sampled positions push the sampled
+    threshold above the true k-th key; the whole-segment select must take
+    over and still give the oracle's answer."""
+    n, k, S = 1 << 20, 10486, 32768
+    g = torch.full((n,), 1e-4, device=DEV) * torch.linspace(1, 2, n, device=DEV)
+    j = torch.arange(S, device=DEV, dtype=torch.int64)
+    pos = ((2 * j + 1) * n) // (2 * S)
+    g[pos] = 1.0 + j.float() * 1e-6
+    check_topk_step(g, torch.zeros(n, device=DEV), [0, n], [k])
+
+
+def test_multistep_carries_residual():
+    n, k = 500_000, 500
+    e = torch.zeros(n, device=DEV)
+    for step in range(4):
+        g = _t(n, 100 + step)
+        want, _ = check_topk_step(g, e, [0, n], [k])
+        e.copy_(torch.from_numpy(want["e"]))       # lockstep: continue from the oracle
+
+
+def test_deterministic_repeat():
+    n = 700_001
+    g = _t(n, 31)
+    e0 = _t(n, 32, 1e-4)
+    outs = []
+    for _ in range(2):
+        e = e0.clone()
+        o = gpu_topk(g, e, [0, n], [7000])
+        outs.append((host(o["indices"]), host(o["values"]), host(e)))
+    for a, b in zip(outs[0], outs[1]):
+        assert_bits_equal(a, b, "repeat")
