@@ -354,8 +354,8 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
   }
 }
 
-// Entry j of a segment's select list: (local index, float bits), taken from
-// the candidate list (mode 0) or straight from the segment (mode 1).
+// A segment's select list: the candidate list (mode 0: entries are
+// (local index, float bits)) or the whole segment itself (mode 1).
 struct ListRef {
   uint32_t mode;
   int64_t cand_base, off, len;
@@ -368,17 +368,6 @@ __device__ __forceinline__ ListRef list_ref(const SegState* st, int seg) {
   r.off = st[seg].d.off;
   r.len = st[seg].list_len;
   return r;
-}
-
-__device__ __forceinline__ uint32_t list_bits(const ListRef& l, const IO& io, const uint2* cand,
-                                              int64_t j, uint32_t* local) {
-  if (l.mode == 0) {
-    const uint2 v = cand[l.cand_base + j];
-    *local = v.x;
-    return v.y;
-  }
-  *local = (uint32_t)j;
-  return __float_as_uint(io.e[l.off + j]);
 }
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -402,9 +391,11 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
     const uint32_t prefix = st[seg].prefix;
     const int64_t j0 = (c - s_cb[seg]) * kChunk;
     const int64_t j1 = min(j0 + (int64_t)kChunk, l.len);
+    const uint2* cl = cand + l.cand_base;
+    const float* el = io.e + l.off;
     for (int64_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-      uint32_t local;
-      const uint32_t key = list_bits(l, io, cand, j, &local) & 0x7FFFFFFFu;
+      const uint32_t bits = l.mode == 0 ? cl[j].y : __float_as_uint(el[j]);
+      const uint32_t key = bits & 0x7FFFFFFFu;
       if (hi >= 31 || (key >> hi) == (prefix >> hi))
         atomicAdd(&sh[(key >> shift) & (nb - 1)], 1u);
     }
@@ -468,17 +459,34 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
     const int64_t jw = (c - s_cb[seg]) * kChunk + warp * 512;
     uint32_t vb[16], loc[16];
     uint32_t gtm = 0, eqm = 0;
+    // The list kind is uniform per segment, so the branch sits outside the
+    // unrolled loads.  (A per-entry branch inside this unrolled, predicated
+    // loop produced wrong flags with this toolchain; this form does not.)
+    if (l.mode == 0) {
+      const uint2* cl = cand + l.cand_base;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int64_t j = jw + r * 32 + lane;
-      if (j < l.len) {
-        vb[r] = list_bits(l, io, cand, j, &loc[r]);
-        const uint32_t key = vb[r] & 0x7FFFFFFFu;
-        gtm |= (uint32_t)(key > T) << r;
-        eqm |= (uint32_t)(key == T) << r;
-      } else {
-        vb[r] = 0;
-        loc[r] = 0;
+      for (int r = 0; r < 16; ++r) {
+        const int64_t j = jw + r * 32 + lane;
+        uint2 v = make_uint2(0u, 0u);
+        if (j < l.len) v = cl[j];
+        vb[r] = v.y;
+        loc[r] = v.x;
+        const uint32_t key = v.y & 0x7FFFFFFFu;
+        gtm |= (uint32_t)(j < l.len && key > T) << r;
+        eqm |= (uint32_t)(j < l.len && key == T) << r;
+      }
+    } else {
+      const float* el = io.e + l.off;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int64_t j = jw + r * 32 + lane;
+        uint32_t v = 0u;
+        if (j < l.len) v = __float_as_uint(el[j]);
+        vb[r] = v;
+        loc[r] = (uint32_t)j;
+        const uint32_t key = v & 0x7FFFFFFFu;
+        gtm |= (uint32_t)(j < l.len && key > T) << r;
+        eqm |= (uint32_t)(j < l.len && key == T) << r;
       }
     }
     uint32_t cg = __popc(gtm), ce = __popc(eqm);
