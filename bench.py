@@ -1,0 +1,605 @@
+#!/usr/bin/env python
+"""Throughput benchmark of one full error-feedback step on GB300.
+
+Workload (default ``slab_2p31``): a flat fp32 slab of n = 2**31 gradient
+elements per worker, W = 4 simulated workers on one GPU, Student-t(3) x 1e-3
+gradients.  One step runs the whole hot path three times over the same
+gradients, as the configuration asks:
+  1. top-0.1 % error feedback with int32 indices for each worker, then the
+     receive side (sum of the 4 packets into a dense G, SGD eta = 0.1);
+  2. the same with bitmap-indexed packets (own residuals, own weights);
+  3. 1-bit error feedback (beta1 = 0.9) for each worker, then the sign sum
+     and SGD.
+Units per step: 3 variants x W x n gradient elements.  ``value`` is in
+G elements / s over all ranks.  Inputs (134 GB of state) are far larger than
+the 129 MB L2, so no flush is needed between steps.
+
+``--impl reference`` times the CPU oracle (numpy, one host core) on a bounded
+sample of the same workload and prints the same line with
+``"impl": "reference"``.  Under torchrun each rank runs its own replica
+(the path needs no cross-GPU exchange); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "G grad elements/s per EF compress+apply step; HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "G grad elements/s"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; barrier + max over ranks)
+# ---------------------------------------------------------------------------
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+
+
+class SlabStep:
+    """State and launches of one full step of the slab workload."""
+
+    def __init__(self, n: int, workers: int, dev):
+        import torch
+        from error_feedback_gradient_gb300 import workloads as wl
+        import error_feedback_gradient_gb300 as efg
+        self.efg, self.torch = efg, torch
+        self.wl = wl.workload("slab_2p31", n)
+        self.n, self.W, self.dev = n, workers, dev
+        self.k = self.wl.total_k
+        self.offs, self.ks = list(self.wl.seg_offsets), list(self.wl.seg_k)
+        f32 = torch.float32
+        nw = (n + 31) // 32
+        self.g = [self.wl.gradient(w, 1, dev) for w in range(workers)]
+        z = lambda: torch.zeros(n, dtype=f32, device=dev)   # noqa: E731
+        self.e_int = [z() for _ in range(workers)]
+        self.e_bm = [z() for _ in range(workers)]
+        self.eps = [z() for _ in range(workers)]
+        w0 = self.wl.weights(dev)
+        self.w_int, self.w_bm, self.w_sign = w0, w0.clone(), w0.clone()
+        self.G = torch.empty(n, dtype=f32, device=dev)
+        self.vals_int = [torch.empty(self.k, dtype=f32, device=dev) for _ in range(workers)]
+        self.idx_int = [torch.empty(self.k, dtype=torch.int32, device=dev) for _ in range(workers)]
+        self.vals_bm = [torch.empty(self.k, dtype=f32, device=dev) for _ in range(workers)]
+        self.bm = [torch.empty(nw, dtype=torch.int32, device=dev) for _ in range(workers)]
+        self.bits = [torch.empty(nw, dtype=torch.int32, device=dev) for _ in range(workers)]
+        u8 = torch.uint8
+        self.ws_int = torch.empty(efg.topk_workspace_size(n, self.offs, self.ks, efg.IDX_INT32),
+                                  dtype=u8, device=dev)
+        self.ws_bm = torch.empty(efg.topk_workspace_size(n, self.offs, self.ks, efg.IDX_BITMAP),
+                                 dtype=u8, device=dev)
+        self.ws_ai = torch.empty(efg.aggregate_workspace_size(workers, efg.IDX_INT32, n),
+                                 dtype=u8, device=dev)
+        self.ws_ab = torch.empty(efg.aggregate_workspace_size(workers, efg.IDX_BITMAP, n),
+                                 dtype=u8, device=dev)
+        self.prof = None   # list of (kernel_id, start_event, stop_event) filled per launch
+
+    # units and algorithmic bytes --------------------------------------------
+    @property
+    def units(self) -> int:
+        return 3 * self.W * self.n
+
+    def algorithmic_bytes(self) -> dict:
+        n, W, k = self.n, self.W, self.k
+        return {
+            # read g_raw + e, write e (the fused pass) + packet write by the emit
+            "topk_int32": W * (12 * n + 8 * k),
+            "topk_bitmap": W * (12 * n + n / 8 + 4 * k),
+            "sign": W * (12 * n + n / 8),
+            # dense G write + packet reads + w read-modify-write where touched
+            "aggregate_int32": 4 * n + 8 * W * k + 8 * W * k,
+            "aggregate_bitmap": 4 * n + W * n / 8 + 4 * W * k + 8 * W * k,
+            # w read + write, G write, W bit vectors
+            "sign_apply": 12 * n + W * n / 8,
+        }
+
+    def _hook(self, kernel_id):
+        if self.prof is None:
+            return
+        torch = self.torch
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        b.record()     # creates the events; the library re-records them
+        self.efg.binding.profile_events(kernel_id, a, b)
+        self.prof.append((kernel_id, a, b))
+
+    def step(self):
+        efg = self.efg
+        for w in range(self.W):
+            self._hook(efg.binding.KERNEL_TOPK_FUSED)
+            efg.topk_compress(self.g[w], self.e_int[w], self.offs, self.ks, self.vals_int[w],
+                              self.idx_int[w], None, self.ws_int, efg.IDX_INT32)
+        self._hook(efg.binding.KERNEL_SPARSE_APPLY)
+        efg.sparse_aggregate_apply(self.vals_int, self.idx_int, None, [self.k] * self.W, self.n,
+                                   self.wl.eta, self.G, self.w_int, self.ws_ai, efg.IDX_INT32)
+        for w in range(self.W):
+            self._hook(efg.binding.KERNEL_TOPK_FUSED)
+            efg.topk_compress(self.g[w], self.e_bm[w], self.offs, self.ks, self.vals_bm[w],
+                              None, self.bm[w], self.ws_bm, efg.IDX_BITMAP)
+        self._hook(efg.binding.KERNEL_SPARSE_APPLY)
+        efg.sparse_aggregate_apply(self.vals_bm, None, self.bm, [self.k] * self.W, self.n,
+                                   self.wl.eta, self.G, self.w_bm, self.ws_ab, efg.IDX_BITMAP)
+        for w in range(self.W):
+            self._hook(efg.binding.KERNEL_SIGN)
+            efg.sign_compress(self.g[w], self.eps[w], self.wl.beta1, self.bits[w])
+        self._hook(efg.binding.KERNEL_SIGN_APPLY)
+        efg.sign_aggregate_apply(self.bits, self.n, efg.APPLY_SGD, self.wl.eta, self.wl.beta1,
+                                 self.G, self.w_sign)
+
+    def clear_hooks(self):
+        for kid in (1, 2, 3, 4):
+            self.efg.binding.profile_events(kid, None, None)
+
+    def check_status(self):
+        for ws in (self.ws_int, self.ws_bm, self.ws_ai, self.ws_ab):
+            st = self.efg.workspace_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {st}")
+
+
+def oracle_step(g_list, n, k, eta, beta1, w0):
+    """One full step of the slab workload by the CPU oracle (numpy) on
+    host arrays; same three variants as SlabStep.step."""
+    import numpy as np
+    import oracle
+    W = len(g_list)
+    offs, ks = [0, n], [k]
+    z = np.zeros(n, np.float32)
+    pk = [oracle.topk_ef_step(g, z, offs, ks, "int32") for g in g_list]
+    G = oracle.sparse_aggregate(pk, n)
+    oracle.sgd_apply(w0, G, eta)
+    pb = [oracle.topk_ef_step(g, z, offs, ks, "bitmap") for g in g_list]
+    G = oracle.sparse_aggregate(pb, n)
+    oracle.sgd_apply(w0, G, eta)
+    bits = [oracle.sign_ef_step(g, z, beta1)[0] for g in g_list]
+    G = oracle.sign_aggregate(bits, n)
+    oracle.sgd_apply(w0, G, eta)
+    return 3 * W * n
+
+
+def oracle_sample_inputs(sample_n: int, workers: int, device="cpu"):
+    from error_feedback_gradient_gb300 import workloads as wl
+    w = wl.workload("slab_2p31", sample_n)
+    g = [w.gradient(i, 1, device).cpu().numpy() for i in range(workers)]
+    return g, w.total_k, w.eta, w.beta1, w.weights(device).cpu().numpy()
+
+
+def time_oracle(sample_n: int, workers: int, repeats: int = 1):
+    g, k, eta, beta1, w0 = oracle_sample_inputs(sample_n, workers)
+    units = 0
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        units += oracle_step(g, sample_n, k, eta, beta1, w0)
+    dt = time.perf_counter() - t0
+    return units, dt, k
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args, rank, world):
+    """CPU oracle as the reference arm: each step is one oracle step on a
+    bounded sample of the workload (sample_n elements per worker)."""
+    if rank != 0:
+        return
+    sample_n = args.ref_sample
+    g, k, eta, beta1, w0 = oracle_sample_inputs(sample_n, args.workers)
+    for _ in range(args.warmup):
+        oracle_step(g, sample_n, k, eta, beta1, w0)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(g, sample_n, k, eta, beta1, w0)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    units = 3 * args.workers * sample_n * args.steps
+    value = units / total / 1e9
+    sample = (f"{args.workers} workers x {sample_n} elements (k = {k}, 0.1 %) per step, "
+              "all three variants, numpy on one host core")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload_desc, "n": args.n, "workers": args.workers,
+                   "reference_sample_elements_per_worker": sample_n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample, "host_cpus": os.cpu_count()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import error_feedback_gradient_gb300 as efg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    efg.library()
+    # CPU baseline first (rank 0, N = 1 only), before any large allocation
+    cpu = None
+    if rank == 0 and world == 1 and args.baseline_sample > 0:
+        units, dt, k = time_oracle(args.baseline_sample, args.workers)
+        cpu = {"value": units / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": (f"one oracle step on {args.workers} workers x {args.baseline_sample} "
+                          f"elements (k = {k}), all three variants, {dt:.1f} s"),
+               "host_cpus": os.cpu_count()}
+
+    s = SlabStep(args.n, args.workers, dev)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        s.step()
+    torch.cuda.synchronize()
+    s.check_status()
+
+    # timed region: K steps between barriers + synchronize, CUDA events
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    launches0 = efg.kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        s.step()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier()
+    launches = efg.kernel_launches() - launches0
+    clk = clocks.stop() if clocks else None
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms)
+    value = world * s.units / (ms_max * 1e-3) / 1e9
+
+    # per-kernel times from the profiling hook (same stream, same work)
+    s.prof = []
+    for _ in range(args.prof_steps):
+        s.step()
+    torch.cuda.synchronize()
+    per = {}
+    for kid, a, b in s.prof:
+        per.setdefault(kid, []).append(a.elapsed_time(b))
+    s.prof = None
+    s.clear_hooks()
+    s.check_status()
+    ab = s.algorithmic_bytes()
+    peak, peak_kind = load_peaks()
+    n = s.n
+    kernels = {}
+    names = {1: "topk_fused", 2: "sign_compress", 3: "sparse_aggregate_apply",
+             4: "sign_aggregate_apply"}
+    kb = {1: 12 * n, 2: 12.125 * n, 3: None, 4: ab["sign_apply"]}
+    for kid, ts in per.items():
+        avg = statistics.mean(ts)
+        d = {"launches_per_step": len(ts) // max(1, args.prof_steps), "avg_ms": avg}
+        if kb.get(kid):
+            d["algorithmic_bytes"] = kb[kid]
+            d["achieved_gbs"] = kb[kid] / (avg * 1e-3) / 1e9
+        kernels[names[kid]] = d
+    top = kernels["topk_fused"]
+    roofline = {"bound": "hbm", "kernel": "topk_fused",
+                "achieved": top["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": top["achieved_gbs"] / peak, "peak_source": peak_kind,
+                "traffic": args.traffic_per_launch,
+                "algorithmic_bytes_per_launch": 12 * n}
+    step_bytes = sum(ab.values())
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, s) if args.e2e_steps > 0 else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload_desc, "n": args.n, "workers": args.workers,
+                   "k": s.k, "variants": ["topk_int32", "topk_bitmap", "sign_1bit"],
+                   "units_per_step": s.units, "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "step_hbm": {"algorithmic_bytes": step_bytes,
+                     "gbs": step_bytes / (ms_max * 1e-3) / 1e9,
+                     "frac_of_peak": step_bytes / (ms_max * 1e-3) / 1e9 / peak},
+        "roofline": roofline, "kernels": kernels,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": launches,
+    }
+    del s
+    torch.cuda.empty_cache()
+    if args.extras and rank == 0:
+        line["per_config"] = run_extras(args, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, s):
+    """Same metric through the public API with host buffers: every step copies
+    each worker's gradient from pinned host memory, runs the step, and reads
+    back the step's compressed packets (int32 packets, bitmap packets, sign
+    bits).  Timed with CUDA events on the stream."""
+    import torch
+    host_g = []
+    for t in s.g:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host_g.append(h)
+    outs = s.vals_int + s.idx_int + s.vals_bm + s.bm + s.bits
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_g)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for dst, src in zip(s.g, host_g):
+            dst.copy_(src, non_blocking=True)
+        s.step()
+        for dst, src in zip(host_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.e2e_steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * s.units / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_extras(args, dev):
+    """The other configurations, timed briefly with CUDA events (context for
+    the main line; each is also a parity test case)."""
+    import torch
+    import error_feedback_gradient_gb300 as efg
+    from error_feedback_gradient_gb300 import workloads as wl
+    out = {}
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    # top-k single tensor 2^20 (W = 1, + aggregate + SGD)
+    w = wl.workload("topk_2p20")
+    g = w.gradient(0, 1, dev)
+    e = torch.zeros_like(g)
+    v = torch.empty(w.total_k, device=dev)
+    i = torch.empty(w.total_k, dtype=torch.int32, device=dev)
+    ws = torch.empty(efg.topk_workspace_size(w.n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                     device=dev)
+    wa = torch.empty(efg.aggregate_workspace_size(1, 0, w.n), dtype=torch.uint8, device=dev)
+    G = torch.empty_like(g)
+    wt = w.weights(dev)
+
+    def c1():
+        efg.topk_compress(g, e, w.seg_offsets, w.seg_k, v, i, None, ws)
+        efg.sparse_aggregate_apply([v], [i], None, [w.total_k], w.n, w.eta, G, wt, wa)
+    ms = timed(c1, 50)
+    out["topk_2p20"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
+                        "note": "L2-resident, launch-bound; no CUDA graph"}
+    del g, e, v, i, ws, wa, G, wt
+
+    # 1-bit on 2^24 with the momentum
+    w = wl.workload("sign_2p24")
+    g = w.gradient(0, 1, dev)
+    eps = torch.zeros_like(g)
+    m = torch.zeros_like(g)
+    bits = torch.empty((w.n + 31) // 32, dtype=torch.int32, device=dev)
+
+    def c2():
+        efg.sign_compress(g, eps, w.beta1, bits)
+        efg.sign_aggregate_apply([bits], w.n, efg.APPLY_MOMENTUM, 0.0, w.beta1, None, m)
+    ms = timed(c2, 50)
+    out["sign_2p24"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
+                        "gbs": (12.125 + 8.125) * w.n / ms / 1e6}
+    del g, eps, m, bits
+
+    # layerwise ResNet-50
+    w = wl.workload("resnet50")
+    g = w.gradient(0, 1, dev)
+    e = torch.zeros_like(g)
+    v = torch.empty(w.total_k, device=dev)
+    i = torch.empty(w.total_k, dtype=torch.int32, device=dev)
+    ws = torch.empty(efg.topk_workspace_size(w.n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                     device=dev)
+
+    def c3():
+        efg.topk_compress(g, e, w.seg_offsets, w.seg_k, v, i, None, ws)
+    ms = timed(c3, 30)
+    out["resnet50"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
+                       "gbs": (12 * w.n + 8 * w.total_k) / ms / 1e6}
+    del g, e, v, i, ws
+
+    # BERT-large flat, 8 workers + aggregate
+    w = wl.workload("bert_large")
+    gs = [w.gradient(k, 1, dev) for k in range(w.workers)]
+    es = [torch.zeros_like(gs[0]) for _ in range(w.workers)]
+    vs = [torch.empty(w.total_k, device=dev) for _ in range(w.workers)]
+    idx = [torch.empty(w.total_k, dtype=torch.int32, device=dev) for _ in range(w.workers)]
+    ws = torch.empty(efg.topk_workspace_size(w.n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                     device=dev)
+    wa = torch.empty(efg.aggregate_workspace_size(w.workers, 0, w.n), dtype=torch.uint8,
+                     device=dev)
+    G = torch.empty_like(gs[0])
+    wt = w.weights(dev)
+
+    def c4():
+        for k in range(w.workers):
+            efg.topk_compress(gs[k], es[k], w.seg_offsets, w.seg_k, vs[k], idx[k], None, ws)
+        efg.sparse_aggregate_apply(vs, idx, None, [w.total_k] * w.workers, w.n, w.eta, G, wt, wa)
+    ms = timed(c4, 10)
+    bytes_ = w.workers * (12 * w.n + 8 * w.total_k) + 4 * w.n + 16 * w.workers * w.total_k
+    out["bert_large"] = {"ms_per_step": ms, "g_elems_per_s": w.workers * w.n / ms / 1e6,
+                         "gbs": bytes_ / ms / 1e6}
+    return out
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--n", type=int, default=1 << 31, help="elements per worker")
+    p.add_argument("--workers", type=int, default=4)
+    p.add_argument("--prof-steps", type=int, default=2)
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--baseline-sample", type=int, default=1 << 27,
+                   help="elements per worker in the timed oracle sample (0: skip)")
+    p.add_argument("--ref-sample", type=int, default=1 << 21,
+                   help="elements per worker in one reference-arm step")
+    p.add_argument("--traffic-per-launch", type=float, default=None,
+                   help="DRAM bytes of one topk_fused launch at this size, from ncu")
+    p.add_argument("--no-extras", dest="extras", action="store_false")
+    args = p.parse_args(argv)
+    args.workload_desc = (f"slab_2p31: flat fp32 slab n={args.n} per worker, W={args.workers}, "
+                          "Student-t(3)x1e-3; top-0.1% int32 + bitmap EF and 1-bit EF "
+                          "(beta1=0.9), each aggregated locally with SGD eta=0.1")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     IDX_INT32,
     APPLY_MOMENTUM,
     APPLY_SGD,
+    kernel_launches,
     library,
     library_path,
     sign_aggregate_apply,

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "ef_abi_version": (ctypes.c_int32, []),
     "ef_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "ef_last_cuda_error": (ctypes.c_int32, []),
+    "ef_kernel_launches": (ctypes.c_int64, []),
     "ef_topk_workspace_size": (ctypes.c_int32, [
         ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p, ctypes.c_int32,
         ctypes.POINTER(ctypes.c_size_t)]),
@@ -215,6 +216,11 @@ def sparse_aggregate_apply(values: Sequence[torch.Tensor],
         float(eta), _ptr(G), _ptr(w), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "sparse_aggregate_apply")
+
+
+def kernel_launches() -> int:
+    """Kernels this thread has launched through the library so far."""
+    return int(library().ef_kernel_launches())
 
 
 def workspace_status(workspace: torch.Tensor, stream=None) -> int:

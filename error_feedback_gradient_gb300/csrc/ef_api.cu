@@ -12,6 +12,7 @@ namespace ef {
 namespace {
 
 thread_local int32_t t_last_cuda_error = 0;
+thread_local int64_t t_launches = 0;
 
 struct ProfSlot {
   cudaEvent_t start = nullptr;
@@ -33,6 +34,7 @@ ef_status cuda_fail(cudaError_t err) {
 }
 
 ef_status check_launch() {
+  ++t_launches;
   cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? EF_OK : cuda_fail(err);
 }
@@ -79,6 +81,8 @@ extern "C" {
 int32_t ef_abi_version(void) { return EF_ABI_VERSION; }
 
 int32_t ef_last_cuda_error(void) { return ef::t_last_cuda_error; }
+
+int64_t ef_kernel_launches(void) { return ef::t_launches; }
 
 const char* ef_status_string(ef_status s) {
   switch (s) {

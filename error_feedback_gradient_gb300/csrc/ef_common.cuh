@@ -27,7 +27,7 @@ ef_status current_device(DeviceInfo* out);
 // Record the failing CUDA error for ef_last_cuda_error() and map to a status.
 ef_status cuda_fail(cudaError_t err);
 
-// Check the last launch; returns EF_OK or EF_ERR_CUDA.
+// Count one kernel launch and check it; returns EF_OK or EF_ERR_CUDA.
 ef_status check_launch();
 
 // Profiling hook: record the thread's start/stop event for `kernel_id`

@@ -23,6 +23,9 @@
 //   4. emit     ordered compaction of the list: an entry is taken when
 //      key > T, or key == T and fewer than `need` equal keys precede it;
 //      position = #(key > T before it) + min(#(key == T before it), need).
+//      The look-back carries (#gt, #lt) prefixes: both stay below 2^31 for a
+//      list of up to 2^31 entries (T itself is in the list), and the equal
+//      count follows from the list position j as j - gt - lt.
 //      Writes values, int32 indices or bitmap bits, and e = +0 there.
 #include <cuda_runtime.h>
 
@@ -438,8 +441,9 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
 __global__ void __launch_bounds__(kEmitThreads)
 topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ctl* ctl) {
   __shared__ int64_t s_cb[kMaxLarge + 1];
-  __shared__ uint32_t s_wgt[kEmitThreads / 32], s_weq[kEmitThreads / 32];
-  __shared__ uint32_t s_ogt[kEmitThreads / 32], s_oeq[kEmitThreads / 32];
+  __shared__ uint32_t s_wgt[kEmitThreads / 32], s_wlt[kEmitThreads / 32];
+  __shared__ uint32_t s_ogt[kEmitThreads / 32], s_olt[kEmitThreads / 32];
+  __shared__ uint32_t s_weq[kEmitThreads / 32];
   __shared__ int64_t s_c;
   __shared__ uint64_t s_excl;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
@@ -458,7 +462,7 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
     const int64_t out_end = out_off + st[seg].d.k;
     const int64_t jw = (c - s_cb[seg]) * kChunk + warp * 512;
     uint32_t vb[16], loc[16];
-    uint32_t gtm = 0, eqm = 0;
+    uint32_t gtm = 0, eqm = 0, ltm = 0;
     // The list kind is uniform per segment, so the branch sits outside the
     // unrolled loads.  (A per-entry branch inside this unrolled, predicated
     // loop produced wrong flags with this toolchain; this form does not.)
@@ -474,6 +478,7 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
         const uint32_t key = v.y & 0x7FFFFFFFu;
         gtm |= (uint32_t)(j < l.len && key > T) << r;
         eqm |= (uint32_t)(j < l.len && key == T) << r;
+        ltm |= (uint32_t)(j < l.len && key < T) << r;
       }
     } else {
       const float* el = io.e + l.off;
@@ -487,26 +492,29 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
         const uint32_t key = v & 0x7FFFFFFFu;
         gtm |= (uint32_t)(j < l.len && key > T) << r;
         eqm |= (uint32_t)(j < l.len && key == T) << r;
+        ltm |= (uint32_t)(j < l.len && key < T) << r;
       }
     }
-    uint32_t cg = __popc(gtm), ce = __popc(eqm);
+    uint32_t cg = __popc(gtm), ce = __popc(eqm), cl = __popc(ltm);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       cg += __shfl_xor_sync(kFull, cg, o);
       ce += __shfl_xor_sync(kFull, ce, o);
+      cl += __shfl_xor_sync(kFull, cl, o);
     }
     if (lane == 0) {
       s_wgt[warp] = cg;
+      s_wlt[warp] = cl;
       s_weq[warp] = ce;
     }
     __syncthreads();
     if (warp == 0) {
       const uint32_t a = lane < kEmitThreads / 32 ? s_wgt[lane] : 0u;
-      const uint32_t b = lane < kEmitThreads / 32 ? s_weq[lane] : 0u;
+      const uint32_t b = lane < kEmitThreads / 32 ? s_wlt[lane] : 0u;
       const uint32_t ia = warp_incl_scan(a), ib = warp_incl_scan(b);
       if (lane < kEmitThreads / 32) {
         s_ogt[lane] = ia - a;
-        s_oeq[lane] = ib - b;
+        s_olt[lane] = ib - b;
       }
       const uint64_t agg = ((uint64_t)__shfl_sync(kFull, ia, 31) << 31) |
                            (uint64_t)__shfl_sync(kFull, ib, 31);
@@ -515,21 +523,22 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
     }
     __syncthreads();
     if (cg | ce) {  // warp-uniform
-      uint32_t run_gt = (uint32_t)(s_excl >> 31) + s_ogt[warp];
-      uint32_t run_eq = (uint32_t)(s_excl & 0x7FFFFFFFu) + s_oeq[warp];
-      const unsigned lt = lanemask_lt();
+      int64_t run_gt = (int64_t)(s_excl >> 31) + s_ogt[warp];
+      int64_t run_lt = (int64_t)(s_excl & 0x7FFFFFFFu) + s_olt[warp];
+      const unsigned lm = lanemask_lt();
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        const bool g = (gtm >> r) & 1u, q = (eqm >> r) & 1u;
-        const unsigned bg = __ballot_sync(kFull, g), bq = __ballot_sync(kFull, q);
-        const uint32_t gt_before = run_gt + __popc(bg & lt);
-        const uint32_t eq_before = run_eq + __popc(bq & lt);
-        if (g || (q && eq_before < need)) {
-          const int64_t pos = out_off + gt_before + min(eq_before, need);
+        const bool g = (gtm >> r) & 1u, q = (eqm >> r) & 1u, b = (ltm >> r) & 1u;
+        const unsigned bg = __ballot_sync(kFull, g), bl = __ballot_sync(kFull, b);
+        const int64_t j = jw + r * 32 + lane;
+        const int64_t gt_before = run_gt + __popc(bg & lm);
+        const int64_t eq_before = j - gt_before - (run_lt + __popc(bl & lm));
+        if (g || (q && eq_before < (int64_t)need)) {
+          const int64_t pos = out_off + gt_before + min(eq_before, (int64_t)need);
           emit_one(io, seg_off + loc[r], pos, out_end, __uint_as_float(vb[r]));
         }
         run_gt += __popc(bg);
-        run_eq += __popc(bq);
+        run_lt += __popc(bl);
       }
     }
     __syncthreads();
@@ -579,7 +588,7 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     const int64_t a = offs[s], b = offs[s + 1];
     if (b < a) return EF_ERR_SEGMENTS;
     const int64_t len = b - a;
-    if (len > (int64_t(1) << 31) - 1) return EF_ERR_SIZE;
+    if (len > (int64_t(1) << 31)) return EF_ERR_SIZE;
     const int64_t k = ks[s];
     if (k < 0 || k > len) return EF_ERR_K;
     if (len == 0) continue;

@@ -89,6 +89,10 @@ EF_API const char* ef_status_string(ef_status s);
  * library (0 if none). */
 EF_API int32_t ef_last_cuda_error(void);
 
+/* Number of kernels this thread has launched through the library since the
+ * library was loaded (memsets and event records are not counted). */
+EF_API int64_t ef_kernel_launches(void);
+
 /* ------------------------------------------------------------------------
  * Top-k error feedback, sender side.
  *
@@ -108,7 +112,7 @@ EF_API int32_t ef_last_cuda_error(void);
  *              n <= 2^31 so that every global index fits an int32.
  * nseg         number of segments, >= 1.
  * h_seg_offsets[nseg+1] host, 0 = off[0] <= off[1] <= ... <= off[nseg] = n;
- *              segment s is [off[s], off[s+1]), at most 2^31 - 1 elements.
+ *              segment s is [off[s], off[s+1]), at most 2^31 elements.
  * h_seg_k[nseg] host, 0 <= k_s <= segment length.
  * idx_format   EF_IDX_INT32 or EF_IDX_BITMAP ([SPARSE] §索引编码压缩).
  * out_values   [sum k] fp32: segment 0's entries first; within a segment in

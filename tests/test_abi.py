@@ -90,8 +90,10 @@ def test_topk_workspace_queries(lib):
     assert st == d["EF_ERR_SIZE"]                             # int32 indices overflow
     st, _ = _ws_size(lib, (1 << 31) + 1, [0, 1 << 30, (1 << 31) + 1], [1, 1], fmt=1)
     assert st == d["EF_OK"]                                   # bitmap has no index limit
-    st, _ = _ws_size(lib, 1 << 31, [0, 1 << 31], [1], fmt=1)
-    assert st == d["EF_ERR_SIZE"]                             # one segment >= 2^31
+    st, _ = _ws_size(lib, 1 << 31, [0, 1 << 31], [1], fmt=0)
+    assert st == d["EF_OK"]                                   # one segment of 2^31
+    st, _ = _ws_size(lib, (1 << 31) + 1, [0, (1 << 31) + 1], [1], fmt=1)
+    assert st == d["EF_ERR_SIZE"]                             # one segment > 2^31
 
 
 def test_topk_rejects_before_device(lib):
