@@ -58,6 +58,9 @@ _SIGNATURES = {
     "ef_topk_compress": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p,
         ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "ef_topk_compress_noalloc": (ctypes.c_int32, [
+        _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p,
+        ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp]),
     "ef_sign_compress": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_float, _c_vp, _c_vp]),
     "ef_aggregate_workspace_size": (ctypes.c_int32, [
@@ -163,6 +166,19 @@ def topk_compress(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Sequence[in
         int(idx_format), _ptr(out_values), _ptr(out_indices), _ptr(out_bitmap),
         _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)), "ef_topk_compress")
+
+
+def topk_compress_noalloc(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Sequence[int],
+                          seg_k: Sequence[int], out_values: torch.Tensor,
+                          out_indices: Optional[torch.Tensor] = None,
+                          out_bitmap: Optional[torch.Tensor] = None,
+                          idx_format: int = IDX_INT32, stream=None) -> None:
+    """ef_topk_compress_noalloc: the same step with the library's own scratch
+    array (no allocation by the library or here)."""
+    _check(library().ef_topk_compress_noalloc(
+        _ptr(g_raw), _ptr(e), g_raw.numel(), len(seg_k), _i64(seg_offsets), _i64(seg_k),
+        int(idx_format), _ptr(out_values), _ptr(out_indices), _ptr(out_bitmap),
+        _stream(stream)), "ef_topk_compress_noalloc")
 
 
 # ---------------------------------------------------------------------------

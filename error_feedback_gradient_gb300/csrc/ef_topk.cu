@@ -788,3 +788,57 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
   }
   return EF_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the same computation as ef_topk_compress with
+// a library-owned scratch array in place of the caller's workspace.
+// ---------------------------------------------------------------------------
+
+namespace ef {
+namespace {
+
+// Scratch for ef_topk_compress_noalloc; holds EF_NOALLOC_SCRATCH_BYTES on
+// every device that loads the library.  In host code this name is only a
+// stand-in for the device array; its device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EF_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).
+ef_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= 64) return EF_ERR_ARCH;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return cuda_fail(err);
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return EF_OK;
+}
+
+}  // namespace
+}  // namespace ef
+
+extern "C" ef_status ef_topk_compress_noalloc(const float* g_raw, float* e, int64_t n,
+                                              int32_t nseg, const int64_t* h_seg_offsets,
+                                              const int64_t* h_seg_k, int32_t idx_format,
+                                              float* out_values, int32_t* out_indices,
+                                              uint32_t* out_bitmap, void* stream) {
+  size_t need = 0;
+  ef_status st = ef_topk_workspace_size(n, nseg, h_seg_offsets, h_seg_k, idx_format, &need);
+  if (st != EF_OK) return st;
+  if (need > (size_t)EF_NOALLOC_SCRATCH_BYTES) return EF_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((st = ef::noalloc_scratch(&scratch)) != EF_OK) return st;
+  return ef_topk_compress(g_raw, e, n, nseg, h_seg_offsets, h_seg_k, idx_format, out_values,
+                          out_indices, out_bitmap, scratch, (size_t)EF_NOALLOC_SCRATCH_BYTES,
+                          stream);
+}

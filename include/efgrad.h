@@ -138,6 +138,41 @@ EF_API ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
                            size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Top-k error feedback for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it is a library
+ * convenience.  Some callers cannot call cudaMalloc when they compress: a
+ * gradient hook that runs while a framework's caching allocator already
+ * holds all free device memory (a raw cudaMalloc would fail or force the
+ * pool to give memory back mid-step), or a host program in a latency-critical
+ * section where an allocation, which may synchronise the device, is not
+ * acceptable.  This call computes exactly what ef_topk_compress computes,
+ * with the same arguments minus the workspace: its scratch is one
+ * library-owned device array of EF_NOALLOC_SCRATCH_BYTES, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * - Requests whose ef_topk_workspace_size() exceeds EF_NOALLOC_SCRATCH_BYTES
+ *   are rejected with EF_ERR_WORKSPACE before anything is enqueued (use
+ *   ef_topk_compress with your own workspace for those).
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ * - All calls share the one array and it keeps the last call's contents (the
+ *   call clears what must start at zero itself).  Calls whose GPU work can
+ *   overlap -- on different streams, or from different threads without
+ *   ordering -- race on it; issue them on one stream.
+ * - Device-side conditions (EF_ERR_DEVICE_TIMEOUT, EF_ERR_INTERNAL) land in
+ *   the library's array and are not reported by this entry point.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ * ---------------------------------------------------------------------- */
+#define EF_NOALLOC_SCRATCH_BYTES 33554432
+EF_API ef_status ef_topk_compress_noalloc(const float* g_raw, float* e, int64_t n,
+                                          int32_t nseg, const int64_t* h_seg_offsets,
+                                          const int64_t* h_seg_k, int32_t idx_format,
+                                          float* out_values, int32_t* out_indices,
+                                          uint32_t* out_bitmap, void* stream);
+
+/* ------------------------------------------------------------------------
  * 1-bit sign error feedback, sender side.
  *
  * [ONEBIT] §2.1 量化与误差补偿机制:
