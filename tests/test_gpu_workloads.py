@@ -1,0 +1,220 @@
+"""GPU parity at the five workloads' full sizes, in the launch configuration
+bench.py times (same entry points, same segment tables, W workers as
+separate buffers on one GPU).
+
+Steps run in lockstep: each GPU step and the oracle step get the same inputs;
+after a step both continue from the oracle's state, so a difference cannot
+cascade.  The 2^31 slab is checked on one worker in full (top-k, both index
+formats) and elsewhere on sampled positions (1-bit path) and with packets
+drawn by the input generator (receive side).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import error_feedback_gradient_gb300 as efg
+from error_feedback_gradient_gb300 import workloads as wl
+from efcheck import assert_bits_equal, assert_close, check_topk_step, gpu_topk, host
+import oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _apply(packets_gpu, ks, n, eta, w_gpu, fmt=efg.IDX_INT32):
+    G = torch.empty(n, device=DEV)
+    vals = [p["values"] for p in packets_gpu]
+    if fmt == efg.IDX_INT32:
+        efg.sparse_aggregate_apply(vals, [p["indices"] for p in packets_gpu], None, ks, n, eta,
+                                   G, w_gpu, idx_format=fmt)
+    else:
+        efg.sparse_aggregate_apply(vals, None, [p["bitmap"] for p in packets_gpu], ks, n, eta,
+                                   G, w_gpu, idx_format=fmt)
+    return G
+
+
+def test_topk_2p20_three_steps_with_apply():
+    w = wl.workload("topk_2p20")
+    e = torch.zeros(w.n, device=DEV)
+    wt = w.weights(DEV)
+    for step in range(1, w.steps + 1):
+        g = w.gradient(0, step, DEV)
+        w_before = host(wt)
+        want, out = check_topk_step(g, e, w.seg_offsets, w.seg_k)
+        G = _apply([out], [w.total_k], w.n, w.eta, wt)
+        G_want = oracle.sparse_aggregate([want], w.n)
+        w_want = oracle.sgd_apply(w_before, G_want, w.eta)
+        torch.cuda.synchronize()
+        assert_close(G, G_want, "G")
+        assert_close(wt, w_want, "w")
+        assert_bits_equal(wt, w_want, "w (bitwise)")
+        e.copy_(torch.from_numpy(want["e"]))
+        wt.copy_(torch.from_numpy(w_want))
+
+
+def test_sign_2p24_ten_steps_with_momentum():
+    w = wl.workload("sign_2p24")
+    eps = torch.zeros(w.n, device=DEV)
+    m = torch.zeros(w.n, device=DEV)
+    eps_ref = np.zeros(w.n, np.float32)
+    m_ref = np.zeros(w.n, np.float32)
+    bits = torch.empty((w.n + 31) // 32, dtype=torch.int32, device=DEV)
+    for step in range(1, w.steps + 1):
+        g = w.gradient(0, step, DEV)
+        efg.sign_compress(g, eps, w.beta1, bits)
+        efg.sign_aggregate_apply([bits], w.n, efg.APPLY_MOMENTUM, 0.0, w.beta1, None, m)
+        bits_want, eps_ref = oracle.sign_ef_step(host(g), eps_ref, w.beta1)
+        m_ref = oracle.onebit_momentum(m_ref, oracle.decode_signs(bits_want, w.n), w.beta1)
+        torch.cuda.synchronize()
+        assert_bits_equal(bits, bits_want, f"bits step {step}")
+        assert_close(eps, eps_ref, f"eps step {step}")
+        assert_close(m, m_ref, f"m step {step}")
+        eps.copy_(torch.from_numpy(eps_ref))
+        m.copy_(torch.from_numpy(m_ref))
+
+
+@pytest.mark.parametrize("fmt", [efg.IDX_INT32, efg.IDX_BITMAP])
+def test_resnet50_layerwise_three_steps(fmt):
+    w = wl.workload("resnet50")
+    e = torch.zeros(w.n, device=DEV)
+    steps = w.steps if fmt == efg.IDX_INT32 else 1
+    for step in range(1, steps + 1):
+        g = w.gradient(0, step, DEV)
+        want, _ = check_topk_step(g, e, w.seg_offsets, w.seg_k, fmt)
+        e.copy_(torch.from_numpy(want["e"]))
+
+
+def test_bert_large_eight_workers_one_step():
+    w = wl.workload("bert_large")
+    wt = w.weights(DEV)
+    w_before = host(wt)
+    packets, wants = [], []
+    for k in range(w.workers):
+        g = w.gradient(k, 1, DEV)
+        e = wl.laplace(w.n, 1e-4, wl.seed(4, k, 0), DEV)        # a carried residual
+        want, out = check_topk_step(g, e, w.seg_offsets, w.seg_k)
+        packets.append(out)
+        wants.append({"indices": want["indices"], "values": want["values"]})
+        del g, e, want
+    G = _apply(packets, [w.total_k] * w.workers, w.n, w.eta, wt)
+    G_want = oracle.sparse_aggregate(wants, w.n)
+    w_want = oracle.sgd_apply(w_before, G_want, w.eta)
+    torch.cuda.synchronize()
+    assert_close(G, G_want, "G")
+    assert_bits_equal(G, G_want, "G (bitwise)")
+    assert_close(wt, w_want, "w")
+    assert_bits_equal(wt, w_want, "w (bitwise)")
+
+
+def test_slab_2p31_topk_one_worker_in_full():
+    w = wl.workload("slab_2p31")
+    n, k = w.n, w.total_k
+    g = w.gradient(0, 1, DEV)
+    e0 = wl.student_t3(n, 1e-4, wl.seed(5, 0, 0), DEV)           # a carried residual
+    g_np, e_np = host(g), host(e0)
+    want = oracle.topk_ef_step(g_np, e_np, w.seg_offsets, w.seg_k, "int32")
+    del e_np
+    e = e0.clone()
+    out = gpu_topk(g, e, w.seg_offsets, w.seg_k, efg.IDX_INT32)
+    torch.cuda.synchronize()
+    assert efg.workspace_status(out["ws"]) == 0
+    assert_bits_equal(out["indices"], want["indices"], "indices")
+    assert_bits_equal(out["values"], want["values"], "values")
+    assert_bits_equal(e, want["e"], "residual")
+    del out
+    # the bitmap format of the same step
+    e.copy_(e0)
+    out = gpu_topk(g, e, w.seg_offsets, w.seg_k, efg.IDX_BITMAP)
+    flags = np.zeros(n, bool)
+    flags[want["indices"]] = True
+    torch.cuda.synchronize()
+    assert_bits_equal(out["bitmap"], oracle.pack_bits(flags), "bitmap")
+    assert_bits_equal(out["values"], want["values"], "values (bitmap)")
+    assert_bits_equal(e, want["e"], "residual (bitmap)")
+
+
+def test_slab_2p31_sign_sampled():
+    w = wl.workload("slab_2p31")
+    n = w.n
+    g = w.gradient(1, 1, DEV)
+    eps = wl.normal(n, 0.05, wl.seed(5, 1, 0), DEV)
+    rng = np.random.default_rng(3)
+    pos = np.unique(rng.integers(0, n, 1 << 20))
+    pos = np.concatenate([pos, [0, 1, 31, 32, n - 33, n - 1]])
+    pos = np.unique(pos)
+    pt = torch.from_numpy(pos).to(DEV)
+    g_s, e_s = host(g[pt]), host(eps[pt])
+    bits = torch.empty((n + 31) // 32, dtype=torch.int32, device=DEV)
+    efg.sign_compress(g, eps, w.beta1, bits)
+    bits_want, eps_want = oracle.sign_ef_step(g_s, e_s, w.beta1)
+    torch.cuda.synchronize()
+    words = host(bits[torch.from_numpy(pos // 32).to(DEV)]).view(np.uint32)
+    got_bit = ((words >> (pos % 32).astype(np.uint32)) & 1).astype(bool)
+    assert np.array_equal(got_bit, oracle.unpack_bits(bits_want, pos.size))
+    assert_bits_equal(eps[pt], eps_want, "eps (sampled)")
+    del g, eps, bits
+
+
+def test_slab_2p31_sign_receive_sampled():
+    """Four workers' 1-bit packets over 2^31 elements (drawn by the input
+    generator as random words), summed and applied with SGD; checked at
+    sampled positions, including both ends of the slab."""
+    w = wl.workload("slab_2p31")
+    n = w.n
+    nw = (n + 31) // 32
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(wl.seed(5, 9, 9))
+    bit_list = [torch.randint(-2**31, 2**31 - 1, (nw,), dtype=torch.int32, device=DEV,
+                              generator=gen) for _ in range(w.workers)]
+    rng = np.random.default_rng(4)
+    pos = np.unique(np.concatenate([rng.integers(0, n, 1 << 20), [0, 1, 31, 32, n - 1]]))
+    pt = torch.from_numpy(pos).to(DEV)
+    wsel = torch.from_numpy(pos // 32).to(DEV)
+    # the sampled bits of every packet, as the oracle's packet of the samples
+    sub_bits = []
+    for b in bit_list:
+        wd = host(b[wsel]).view(np.uint32)
+        sub_bits.append(oracle.pack_bits(((wd >> (pos % 32).astype(np.uint32)) & 1).astype(bool)))
+    wt = w.weights(DEV)
+    w_s = host(wt[pt])
+    G = torch.empty(n, device=DEV)
+    efg.sign_aggregate_apply(bit_list, n, efg.APPLY_SGD, w.eta, w.beta1, G, wt)
+    G_want = oracle.sign_aggregate(sub_bits, pos.size)
+    torch.cuda.synchronize()
+    assert_bits_equal(G[pt], G_want, "G (sampled)")
+    assert_bits_equal(wt[pt], oracle.sgd_apply(w_s, G_want, w.eta), "w (sampled)")
+
+
+def test_slab_2p31_receive_side_four_workers():
+    """W = 4 packets of 2,147,484 entries each (drawn by the input generator:
+    sorted random positions, Student-t values, overlapping between workers),
+    summed into a dense G over 2^31 elements and applied with SGD; G and w
+    are compared at every touched position and at random untouched ones."""
+    w = wl.workload("slab_2p31")
+    n, k = w.n, w.total_k
+    rng = np.random.default_rng(11)
+    common = rng.choice(n, k // 4, replace=False)
+    packets = []
+    for i in range(w.workers):
+        idx = np.unique(np.concatenate([rng.choice(n, k - k // 4, replace=False), common]))
+        vals = (rng.standard_t(3, idx.size) * 1e-3).astype(np.float32)
+        packets.append({"indices": idx.astype(np.int32), "values": vals})
+    wt = w.weights(DEV)
+    touched = np.unique(np.concatenate([p["indices"] for p in packets])).astype(np.int64)
+    untouched = rng.integers(0, n, 1 << 18)
+    probe = np.unique(np.concatenate([touched, untouched, [0, n - 1]]))
+    pt = torch.from_numpy(probe).to(DEV)
+    w_probe = host(wt[pt])
+    gpu_pk = [{"indices": torch.from_numpy(p["indices"]).to(DEV),
+               "values": torch.from_numpy(p["values"]).to(DEV)} for p in packets]
+    G = _apply(gpu_pk, [p["values"].size for p in packets], n, w.eta, wt)
+    # oracle on the probed positions only: restrict every packet to them
+    pos_in_probe = [np.searchsorted(probe, p["indices"]) for p in packets]
+    sub = [{"indices": pi.astype(np.int32), "values": p["values"]}
+           for pi, p in zip(pos_in_probe, packets)]
+    G_want = oracle.sparse_aggregate(sub, probe.size)
+    w_want = oracle.sgd_apply(w_probe, G_want, w.eta)
+    torch.cuda.synchronize()
+    assert_bits_equal(G[pt], G_want, "G (touched + sampled)")
+    assert_bits_equal(wt[pt], w_want, "w (touched + sampled)")
