@@ -41,8 +41,14 @@ namespace {
 
 constexpr int kSmallMax = 32768;
 constexpr int kSmallThreads = 1024;
-constexpr int kTile = 8192;  // elements per fused-pass tile (8 warps x 1024)
-constexpr int kFusedThreads = 256;
+constexpr int kStreamWarps = 8;                 // fused pass: warps that stream the tile
+constexpr int kWarpSpan = 2048;                 // elements per streaming warp per tile
+constexpr int kTile = kStreamWarps * kWarpSpan;  // 16384 elements per fused-pass tile
+constexpr int kStreamThreads = kStreamWarps * 32;
+constexpr int kFusedThreads = kStreamThreads + 32;  // + one scan warp
+constexpr int kStageCap = 256;                  // staged candidates per warp per buffer
+constexpr int kBatch = 4;                       // 128-element rounds loaded at once
+constexpr int kFusedCtasPerSm = 4;
 constexpr int kSample = 32768;
 constexpr int kPrepThreads = 1024;
 constexpr int kChunk = 4096;  // list entries per select / emit chunk
@@ -52,7 +58,7 @@ constexpr int kMaxLarge = 128;     // segments per streaming batch
 constexpr int kMaxSmall = 512;     // segments per small-path launch
 constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
 
-static_assert(kFusedThreads / 32 * 1024 == kTile, "tile layout");
+static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
 static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
 
 struct SmallSeg {
@@ -87,7 +93,7 @@ struct SegState {
   uint32_t prefix;  // radix-select digits fixed so far (= T after pass 3)
   uint32_t krem;    // rank still to find inside the prefix (= need)
   uint32_t gt;
-  uint32_t pad;
+  uint32_t overflow;  // a warp's staging area overflowed: the list is incomplete
 };
 
 struct alignas(256) Ctl {
@@ -199,7 +205,7 @@ topk_prepare(LargeBatch b, int nseg, IO io, SegState* st) {
     v.prefix = 0;
     v.krem = (uint32_t)d.k;
     v.gt = 0;
-    v.pad = 0;
+    v.overflow = 0;
     st[s] = v;
   }
 }
@@ -220,111 +226,182 @@ __device__ __forceinline__ float get4(const float4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
-__global__ void __launch_bounds__(kFusedThreads, 2)
+// Named barriers of the fused pass (0 is __syncthreads).
+constexpr int kBarFull0 = 1;    // + buffer: staging buffer filled (streaming -> scan)
+constexpr int kBarEmpty0 = 3;   // + buffer: staging buffer drained (scan -> streaming)
+constexpr int kBarStream = 5;   // streaming warps only
+
+template <int kId>
+__device__ __forceinline__ void bar_sync(int count) {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "r"(count) : "memory");
+}
+template <int kId>
+__device__ __forceinline__ void bar_arrive(int count) {
+  asm volatile("bar.arrive %0, %1;" ::"n"(kId), "r"(count) : "memory");
+}
+// Barrier of buffer b with compile-time ids (so only the ids in use are
+// reserved, which keeps more CTAs resident per SM).
+__device__ __forceinline__ void full_arrive(int b) {
+  if (b == 0) bar_arrive<kBarFull0>(kFusedThreads); else bar_arrive<kBarFull0 + 1>(kFusedThreads);
+}
+__device__ __forceinline__ void full_sync(int b) {
+  if (b == 0) bar_sync<kBarFull0>(kFusedThreads); else bar_sync<kBarFull0 + 1>(kFusedThreads);
+}
+__device__ __forceinline__ void empty_arrive(int b) {
+  if (b == 0) bar_arrive<kBarEmpty0>(kFusedThreads); else bar_arrive<kBarEmpty0 + 1>(kFusedThreads);
+}
+__device__ __forceinline__ void empty_sync(int b) {
+  if (b == 0) bar_sync<kBarEmpty0>(kFusedThreads); else bar_sync<kBarEmpty0 + 1>(kFusedThreads);
+}
+
+struct FusedStage {
+  uint2 cand[2][kStreamWarps][kStageCap];  // (local index, float bits), index order
+  uint32_t cnt[2][kStreamWarps];           // true candidate count per warp
+  int64_t tile[2];                         // tile of the buffer; -1 ends the pass
+  int32_t seg[2];
+  int64_t next[2];                         // ticket broadcast to the streaming warps
+};
+
+// The HBM pass.  Warps 0..7 stream tiles (ticket order): g = g_raw + e is
+// written over e, and every element with key >= T_lo of its segment is
+// staged in shared memory in index order.  Warp 8 takes each filled staging
+// buffer, resolves the tile's offset in its segment's candidate list with the
+// bounded decoupled look-back, and writes the candidates out; two buffers let
+// the streaming warps run one tile ahead of it.
+__global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
            uint2* cand, Ctl* ctl, int phase, int vec) {
   __shared__ int64_t s_base[kMaxLarge + 1];
-  __shared__ uint32_t s_wcnt[kFusedThreads / 32];
-  __shared__ uint32_t s_woff[kFusedThreads / 32];
-  __shared__ int64_t s_tile;
-  __shared__ uint64_t s_excl;
+  __shared__ FusedStage sg;
   __shared__ int s_last;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_base[i] = st[i].d.tile_base;
   if (threadIdx.x == 0) s_base[nseg] = total_tiles;
+  __syncthreads();
 
-  for (;;) {
-    if (threadIdx.x == 0) s_tile = atomicAdd(&ctl->fused_ticket, 1u);
-    __syncthreads();
-    const int64_t tile = s_tile;
-    if (tile >= total_tiles) break;
-    const int seg = find_seg(s_base, nseg, tile);
-    const int64_t a = st[seg].d.off, bnd = a + st[seg].d.len;
-    const int64_t tbase = s_base[seg];
-    const uint32_t t_lo = st[seg].t_lo;
-    const int64_t q0 = (st[seg].d.q_first + (tile - tbase)) * kTile + warp * 1024;
-
-    float4 gr[8], ee[8];
-    bool full[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int64_t i = q0 + r * 128 + lane * 4 - phase;
-      full[r] = vec && i >= a && i + 4 <= bnd;
-      if (full[r]) {
-        gr[r] = __ldcs(reinterpret_cast<const float4*>(io.g_raw + i));
-        ee[r] = __ldcs(reinterpret_cast<const float4*>(io.e + i));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const bool in = i + c >= a && i + c < bnd;
-          set4(gr[r], c, in ? io.g_raw[i + c] : 0.0f);
-          set4(ee[r], c, in ? io.e[i + c] : 0.0f);
-        }
+  if (warp < kStreamWarps) {
+    // The next tile's ticket is requested while the current tile's last
+    // loads are in flight, so its round trip stays off the critical path.
+    uint32_t ticket = 0;
+    if (threadIdx.x == 0) ticket = atomicAdd(&ctl->fused_ticket, 1u);
+    for (int it = 0;; ++it) {
+      const int b = it & 1;
+      if (threadIdx.x == 0) sg.next[b] = ticket;
+      bar_sync<kBarStream>(kStreamThreads);
+      const int64_t tile = sg.next[b];
+      if (it >= 2) empty_sync(b);  // buffer b drained
+      if (tile >= total_tiles) {
+        if (threadIdx.x == 0) sg.tile[b] = -1;
+        full_arrive(b);
+        // consume the scan warp's last "drained" arrival so every barrier
+        // completes (the scan warp then meets the end marker and stops)
+        if (it >= 1) empty_sync(b ^ 1);
+        break;
       }
-    }
-    uint32_t mask = 0;
+      const int seg = find_seg(s_base, nseg, tile);
+      const int64_t a = st[seg].d.off;
+      const uint32_t t_lo = st[seg].t_lo;
+      // this warp's 2048-element window, as pointers and 32-bit offsets
+      const int64_t w0 = (st[seg].d.q_first + (tile - s_base[seg])) * kTile +
+                         (int64_t)warp * kWarpSpan - phase;
+      const float* gp = io.g_raw + w0;
+      float* ep = io.e + w0;
+      const int lo = (int)max((int64_t)-4, min(a - w0, (int64_t)kWarpSpan));
+      const int hi = (int)max((int64_t)-4, min(a + st[seg].d.len - w0, (int64_t)kWarpSpan + 4));
+      const uint32_t loc0 = (uint32_t)(w0 - a);  // local index of window offset 0 (mod 2^32)
+      uint2* stage = sg.cand[b][warp];
+      uint32_t count = 0;
+#pragma unroll 1
+      for (int r0 = 0; r0 < kWarpSpan / 128; r0 += kBatch) {
+        float4 gr[kBatch], ee[kBatch];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int64_t i = q0 + r * 128 + lane * 4 - phase;
-      float4 g;
-      g.x = __fadd_rn(gr[r].x, ee[r].x);
-      g.y = __fadd_rn(gr[r].y, ee[r].y);
-      g.z = __fadd_rn(gr[r].z, ee[r].z);
-      g.w = __fadd_rn(gr[r].w, ee[r].w);
-      gr[r] = g;
-      if (full[r]) {
-        __stcs(reinterpret_cast<float4*>(io.e + i), g);
+        for (int u = 0; u < kBatch; ++u) {
+          const int o = (r0 + u) * 128 + (int)lane * 4;
+          if (vec && o >= lo && o + 4 <= hi) {
+            gr[u] = __ldcs(reinterpret_cast<const float4*>(gp + o));
+            ee[u] = __ldcs(reinterpret_cast<const float4*>(ep + o));
+          } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          mask |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << (r * 4 + c);
-      } else {
+            for (int c = 0; c < 4; ++c) {
+              const bool in = o + c >= lo && o + c < hi;
+              set4(gr[u], c, in ? gp[o + c] : 0.0f);
+              set4(ee[u], c, in ? ep[o + c] : 0.0f);
+            }
+          }
+        }
+        if (r0 + kBatch == kWarpSpan / 128 && threadIdx.x == 0)
+          ticket = atomicAdd(&ctl->fused_ticket, 1u);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const bool in = i + c >= a && i + c < bnd;
-          if (in) {
-            io.e[i + c] = get4(g, c);
-            mask |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << (r * 4 + c);
+        for (int u = 0; u < kBatch; ++u) {
+          const int o = (r0 + u) * 128 + (int)lane * 4;
+          float4 g;
+          g.x = __fadd_rn(gr[u].x, ee[u].x);
+          g.y = __fadd_rn(gr[u].y, ee[u].y);
+          g.z = __fadd_rn(gr[u].z, ee[u].z);
+          g.w = __fadd_rn(gr[u].w, ee[u].w);
+          uint32_t nib = 0;
+          if (vec && o >= lo && o + 4 <= hi) {
+            __stcs(reinterpret_cast<float4*>(ep + o), g);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) nib |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << c;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (o + c >= lo && o + c < hi) {
+                ep[o + c] = get4(g, c);
+                nib |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << c;
+              }
+            }
+          }
+          if (__any_sync(kFull, nib != 0)) {
+            const uint32_t n4 = __popc(nib);
+            const uint32_t inc = warp_incl_scan(n4);
+            uint32_t pos = count + inc - n4;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if ((nib >> c) & 1u) {
+                if (pos < kStageCap)
+                  stage[pos] = make_uint2(loc0 + (uint32_t)(o + c), __float_as_uint(get4(g, c)));
+                ++pos;
+              }
+            }
+            count += __shfl_sync(kFull, inc, 31);
           }
         }
       }
+      if (lane == 0) sg.cnt[b][warp] = count;
+      if (threadIdx.x == 0) {
+        sg.tile[b] = tile;
+        sg.seg[b] = seg;
+      }
+      full_arrive(b);
     }
-    uint32_t wcnt = __popc(mask);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wcnt += __shfl_xor_sync(kFull, wcnt, o);
-    if (lane == 0) s_wcnt[warp] = wcnt;
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t c = lane < kFusedThreads / 32 ? s_wcnt[lane] : 0u;
+  } else {
+    // scan warp
+    for (int it = 0;; ++it) {
+      const int b = it & 1;
+      full_sync(b);
+      const int64_t tile = sg.tile[b];
+      if (tile < 0) break;
+      const int seg = sg.seg[b];
+      const uint32_t c = lane < kStreamWarps ? sg.cnt[b][lane] : 0u;
       const uint32_t inc = warp_incl_scan(c);
-      if (lane < kFusedThreads / 32) s_woff[lane] = inc - c;
       const uint32_t agg = __shfl_sync(kFull, inc, 31);
-      const uint64_t excl = lookback_warp(tstate, tile, tbase, agg, io.status);
-      if (lane == 0) s_excl = excl;
-    }
-    __syncthreads();
-    if (wcnt) {  // warp-uniform
-      const int64_t cap = st[seg].d.cap;
-      uint2* out = cand + st[seg].d.cand_base;
-      int64_t run = (int64_t)s_excl + s_woff[warp];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t nib = (mask >> (r * 4)) & 0xFu;
-        const uint32_t cnt = __popc(nib);
-        const uint32_t inc = warp_incl_scan(cnt);
-        int64_t pos = run + inc - cnt;
-        const int64_t i = q0 + r * 128 + lane * 4 - phase;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if ((nib >> c) & 1u) {
-            if (pos < cap)
-              out[pos] = make_uint2((uint32_t)(i + c - a), __float_as_uint(get4(gr[r], c)));
-            ++pos;
-          }
+      if (__any_sync(kFull, c > kStageCap) && lane == 0) atomicOr(&st[seg].overflow, 1u);
+      const uint64_t excl = lookback_warp(tstate, tile, s_base[seg], agg, io.status);
+      if (agg) {
+        const int64_t cap = st[seg].d.cap;
+        uint2* out = cand + st[seg].d.cand_base;
+        for (int w = 0; w < kStreamWarps; ++w) {
+          const uint32_t cw = min(__shfl_sync(kFull, c, w), (uint32_t)kStageCap);
+          const int64_t base = (int64_t)excl + __shfl_sync(kFull, inc - c, w);
+          for (uint32_t j = lane; j < cw; j += 32)
+            if (base + j < cap) out[base + j] = sg.cand[b][w][j];
         }
-        run += __shfl_sync(kFull, inc, 31);
       }
+      __syncwarp();
+      empty_arrive(b);
     }
-    __syncthreads();
   }
 
   // The last CTA to finish decides, per segment, which list the select runs on.
@@ -340,7 +417,8 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
     const LargeSeg& d = st[s].d;
     const uint64_t w = ld_acquire(&tstate[s_base[s + 1] - 1]);
     const int64_t c = (w >> 62) == 2 ? (int64_t)(w & kPayloadMask) : -1;
-    uint32_t mode = (c >= d.k && c <= d.cap) ? 0u : 1u;
+    const uint32_t ovf = *reinterpret_cast<volatile uint32_t*>(&st[s].overflow);
+    uint32_t mode = (c >= d.k && c <= d.cap && !ovf) ? 0u : 1u;
     int64_t len = mode == 0 ? c : d.len;
     if (d.k == 0) { mode = 0; len = 0; }
     st[s].mode = mode;
@@ -772,7 +850,7 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     const size_t prep_smem = (size_t)(kSample + 2048 + 64) * 4;
     topk_prepare<<<nsg, kPrepThreads, prep_smem, s>>>(lb, nsg, io, sst);
     if ((st = check_launch()) != EF_OK) return st;
-    const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * 2);
+    const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
     topk_fused<<<fgrid, kFusedThreads, 0, s>>>(io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
