@@ -3,18 +3,20 @@
 //   G[i] = (((+0 + p_0[i]) + p_1[i]) + ...) in worker order over the packets
 //          that contain i;  w[i] -= eta * G[i] where some packet contains i.
 //
-// The dense index space is cut into tiles of kATile elements.  Because every
-// packet is sorted, the entries of worker w that fall in tile t form one run
-// [start[w][t], start[w][t+1]):
+// The dense index space is cut into tiles of kWT = 1024 elements, one per
+// warp.  Because every packet is sorted, the entries of worker w that fall in
+// tile t form one run [start[w][t], start[w][t+1]):
 //   * int32 packets: one pass over the packet entries writes the run
 //     boundaries (each entry fills the starts of the tiles between its
 //     predecessor's tile and its own);
 //   * bitmap packets: per-tile population counts, then one exclusive scan
 //     per worker.
-// The apply kernel then gives each tile to one CTA: it accumulates the runs
-// worker by worker in a shared-memory copy of the tile (no atomics on
-// values; indices inside one packet are distinct), writes the dense tile of G
-// with 16-byte stores, and updates w only at the touched positions.
+// The apply kernel gives each tile to one warp (48 tiles in flight per SM,
+// enough to cover the dependent loads of a tile): the warp loads the run
+// bounds of all workers at once, then the runs' entries of up to 8 workers
+// at once, adds them worker by worker into a shared-memory copy of the tile
+// (no atomics on values; indices inside one packet are distinct), writes the
+// dense tile of G with 16-byte stores, and updates w only where touched.
 // Algorithmic traffic: 4 B per element for G, 8 B per packet entry (values +
 // indices, or values + n/8 bitmap bytes per worker), 8 B per touched w.
 #include <cuda_runtime.h>
@@ -27,10 +29,10 @@
 namespace ef {
 namespace {
 
-constexpr int kATile = 8192;
+constexpr int kWT = 1024;            // elements per warp tile
 constexpr int kAThreads = 256;
-constexpr int kAWords = kATile / 32;
-static_assert(kAWords == kAThreads, "one bitmap word per thread");
+constexpr int kAWarps = kAThreads / 32;
+constexpr int kPre = 8;              // workers whose run entries are loaded at once
 
 struct AggArgs {
   const float* values[EF_MAX_WORKERS];
@@ -44,19 +46,19 @@ struct AggArgs {
   float eta;
 };
 
-__device__ __forceinline__ int64_t* starts_of(int64_t* start, const AggArgs& a, int w) {
+__device__ __forceinline__ uint32_t* starts_of(uint32_t* start, const AggArgs& a, int w) {
   return start + (int64_t)w * (a.ntiles + 1);
 }
 
 __device__ __forceinline__ int64_t clamp_tile(int64_t idx, const AggArgs& a) {
   if (idx < 0) return -1;
-  const int64_t t = idx / kATile;
+  const int64_t t = idx / kWT;
   return t >= a.ntiles ? a.ntiles - 1 : t;
 }
 
 // Run boundaries for int32 packets; validates order and range.
 __global__ void __launch_bounds__(kAThreads)
-agg_starts_int32(AggArgs a, int64_t* start, int32_t* status) {
+agg_starts_int32(AggArgs a, uint32_t* start, int32_t* status) {
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = a.kbase[a.W];
@@ -65,16 +67,16 @@ agg_starts_int32(AggArgs a, int64_t* start, int32_t* status) {
     while (w + 1 < a.W && a.kbase[w + 1] <= x) ++w;
     const int64_t j = x - a.kbase[w];
     const int32_t* ind = a.indices[w];
-    int64_t* st = starts_of(start, a, w);
+    uint32_t* st = starts_of(start, a, w);
     const int64_t idx = ind[j];
     const int64_t prev = j > 0 ? (int64_t)ind[j - 1] : -1;
     const bool ok = idx >= 0 && idx < a.n && (j == 0 || idx > prev);
     if (!ok) set_status(status, EF_ERR_PACKET);
     const int64_t t = clamp_tile(idx, a);
     const int64_t tp = j > 0 ? clamp_tile(prev, a) : -1;
-    for (int64_t tt = tp + 1; tt <= t; ++tt) st[tt] = j;
+    for (int64_t tt = tp + 1; tt <= t; ++tt) st[tt] = (uint32_t)j;
     if (j == a.k[w] - 1)
-      for (int64_t tt = (t < 0 ? 0 : t + 1); tt <= a.ntiles; ++tt) st[tt] = a.k[w];
+      for (int64_t tt = (t < 0 ? 0 : t + 1); tt <= a.ntiles; ++tt) st[tt] = (uint32_t)a.k[w];
   }
   const int64_t span = a.ntiles + 1;
   for (int64_t x = tid; x < (int64_t)a.W * span; x += nthr) {
@@ -83,149 +85,226 @@ agg_starts_int32(AggArgs a, int64_t* start, int32_t* status) {
   }
 }
 
-// Per-(worker, tile) population counts of bitmap packets.
+constexpr int kScanTiles = 2048;  // tiles per chunk of the bitmap run-boundary pass
+
+// Run boundaries for bitmap packets in one pass: CTAs take chunks of
+// kScanTiles tiles in ticket order (worker-major), count each tile's set bits
+// with one warp per tile, scan the chunk in shared memory and get the
+// chunk's offset from the bounded decoupled look-back.  The last chunk of a
+// worker checks the total against k_w.
 __global__ void __launch_bounds__(kAThreads)
-agg_count_bitmap(AggArgs a, uint32_t* counts) {
-  __shared__ uint32_t red[kAThreads / 32];
+agg_bitmap_starts(AggArgs a, uint32_t* start, uint64_t* cstate, uint32_t* ticket,
+                  int32_t* status) {
+  __shared__ uint32_t cnt[kScanTiles];
+  __shared__ uint32_t scratch[64];
+  __shared__ uint32_t s_t;
+  __shared__ uint64_t s_excl;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int64_t nchunks = (a.ntiles + kScanTiles - 1) / kScanTiles;
   const int64_t nwords = (a.n + 31) / 32;
-  for (int64_t x = blockIdx.x; x < (int64_t)a.W * a.ntiles; x += gridDim.x) {
-    const int w = (int)(x / a.ntiles);
-    const int64_t t = x % a.ntiles;
-    const int64_t wi = t * kAWords + threadIdx.x;
-    uint32_t c = wi < nwords ? __popc(__ldg(a.bitmaps[w] + wi)) : 0u;
+  for (;;) {
+    if (threadIdx.x == 0) s_t = atomicAdd(ticket, 1u);
+    __syncthreads();
+    const int64_t tk = s_t;
+    if (tk >= (int64_t)a.W * nchunks) break;
+    const int w = (int)(tk / nchunks);
+    const int64_t c = tk % nchunks;
+    const int64_t t0 = c * kScanTiles;
+    const int ntl = (int)min((int64_t)kScanTiles, a.ntiles - t0);
+    const uint32_t* bm = a.bitmaps[w];
+    for (int i = warp; i < ntl; i += kAWarps) {
+      const int64_t wi = (t0 + i) * (kWT / 32) + lane;
+      uint32_t v = wi < nwords ? __popc(__ldg(bm + wi)) : 0u;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-    if (lane_id() == 0) red[threadIdx.x >> 5] = c;
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+      if (lane == 0) cnt[i] = v;
+    }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t s = 0;
-      for (int i = 0; i < kAThreads / 32; ++i) s += red[i];
-      counts[x] = s;
+    // thread t scans tiles [t * per, (t + 1) * per) of the chunk
+    constexpr int per = kScanTiles / kAThreads;
+    uint32_t local = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      const int i = threadIdx.x * per + q;
+      local += i < ntl ? cnt[i] : 0u;
+    }
+    uint32_t total;
+    const uint32_t ex = block_excl_scan(local, scratch, &total);
+    if (warp == 0) {
+      const uint64_t e = lookback_warp(cstate, tk, (int64_t)w * nchunks, total, status);
+      if (lane == 0) s_excl = e;
+    }
+    __syncthreads();
+    uint32_t* st = starts_of(start, a, w);
+    uint64_t run = s_excl + ex;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      const int i = threadIdx.x * per + q;
+      if (i < ntl) {
+        st[t0 + i] = (uint32_t)run;
+        run += cnt[i];
+      }
+    }
+    if (c == nchunks - 1 && threadIdx.x == 0) {
+      const uint64_t all = s_excl + total;
+      st[a.ntiles] = (uint32_t)all;
+      if ((int64_t)all != a.k[w]) set_status(status, EF_ERR_PACKET);
     }
     __syncthreads();
   }
 }
 
-// Exclusive scan of one worker's tile counts (one CTA per worker).  A
-// thread's partial sum can exceed 32 bits when n >= 2^32, so the low 16 bits
-// and the rest of each partial sum are scanned separately.
-__global__ void __launch_bounds__(1024)
-agg_scan_bitmap(AggArgs a, const uint32_t* counts, int64_t* start, int32_t* status) {
-  __shared__ uint32_t scratch[64];
-  const int w = blockIdx.x;
-  const uint32_t* c = counts + (int64_t)w * a.ntiles;
-  int64_t* st = starts_of(start, a, w);
-  const int64_t per = (a.ntiles + blockDim.x - 1) / blockDim.x;
-  const int64_t t0 = (int64_t)threadIdx.x * per;
-  const int64_t t1 = min(t0 + per, a.ntiles);
-  uint64_t local = 0;
-  for (int64_t t = t0; t < t1; ++t) local += c[t];
-  uint32_t tot_lo, tot_hi;
-  const uint32_t ex_lo = block_excl_scan((uint32_t)(local & 0xFFFFu), scratch, &tot_lo);
-  const uint32_t ex_hi = block_excl_scan((uint32_t)(local >> 16), scratch, &tot_hi);
-  uint64_t run = ((uint64_t)ex_hi << 16) + ex_lo;
-  for (int64_t t = t0; t < t1; ++t) {
-    st[t] = (int64_t)run;
-    run += c[t];
-  }
-  if (threadIdx.x == 0) {
-    const uint64_t total = ((uint64_t)tot_hi << 16) + tot_lo;
-    st[a.ntiles] = (int64_t)total;
-    if ((int64_t)total != a.k[w]) set_status(status, EF_ERR_PACKET);
-  }
+// Run of worker w in tile t, clamped into [0, k_w] (k_w < 2^32).
+__device__ __forceinline__ void run_of(const AggArgs& a, const uint32_t* start, int w, int64_t t,
+                                       uint32_t* lo, uint32_t* hi) {
+  const uint32_t* st = start + (int64_t)w * (a.ntiles + 1);
+  const uint32_t kw = (uint32_t)a.k[w];
+  uint32_t l = st[t], h = st[t + 1];
+  l = l > kw ? kw : l;
+  h = h < l ? l : (h > kw ? kw : h);
+  *lo = l;
+  *hi = h;
 }
 
+template <bool kBitmap>
 __global__ void __launch_bounds__(kAThreads)
-agg_apply(AggArgs a, const int64_t* start, float* __restrict__ G, float* __restrict__ wts) {
-  __shared__ __align__(16) float acc[kATile];
-  __shared__ uint32_t touched[kAWords];
-  __shared__ uint32_t scratch[64];
-  const int tid = threadIdx.x;
+agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
+  __shared__ __align__(16) float acc_all[kAWarps][kWT];
+  __shared__ uint32_t touched_all[kAWarps][kWT / 32];
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  float* acc = acc_all[warp];
+  uint32_t* touched = touched_all[warp];
   const bool g_vec = (reinterpret_cast<uintptr_t>(G) & 15u) == 0;
-  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    const int64_t t0 = tile * kATile;
-    const int tlen = (int)min((int64_t)kATile, a.n - t0);
-    int any = 0;
-    if (tid < a.W) {
-      const int64_t* st = start + (int64_t)tid * (a.ntiles + 1);
-      any = st[tile + 1] > st[tile];
-    }
-    any = __syncthreads_or(any);
+  const int64_t nw = (int64_t)gridDim.x * kAWarps;
+  for (int64_t t = (int64_t)blockIdx.x * kAWarps + warp; t < a.ntiles; t += nw) {
+    const int64_t t0 = t * kWT;
+    const int tlen = (int)min((int64_t)kWT, a.n - t0);
+    // run bounds of workers `lane` and `lane + 32`
+    uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+    if ((int)lane < a.W) run_of(a, start, lane, t, &lo0, &hi0);
+    if ((int)lane + 32 < a.W) run_of(a, start, lane + 32, t, &lo1, &hi1);
+    const bool any = __any_sync(kFull, hi0 > lo0 || hi1 > lo1);
     if (!any && !G) continue;
     float4* acc4 = reinterpret_cast<float4*>(acc);
 #pragma unroll
-    for (int r = 0; r < kATile / 4 / kAThreads; ++r)
-      acc4[r * kAThreads + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
-    touched[tid] = 0;
-    __syncthreads();
+    for (int r = 0; r < kWT / 128; ++r) acc4[r * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    touched[lane] = 0;
+    __syncwarp();
     if (any) {
-      for (int w = 0; w < a.W; ++w) {
-        const int64_t* st = start + (int64_t)w * (a.ntiles + 1);
-        const int64_t kw = a.k[w];
-        int64_t lo = st[tile], hi = st[tile + 1];
-        lo = lo < 0 ? 0 : (lo > kw ? kw : lo);
-        hi = hi < lo ? lo : (hi > kw ? kw : hi);
-        const float* vals = a.values[w];
-        if (!a.bitmap) {
-          const int32_t* ind = a.indices[w];
-          for (int64_t j = lo + tid; j < hi; j += kAThreads) {
-            const int64_t slot = (int64_t)ind[j] - t0;
-            if (slot >= 0 && slot < tlen) {
-              acc[slot] = __fadd_rn(acc[slot], vals[j]);
+      for (int wb = 0; wb < a.W; wb += kPre) {
+        if (!kBitmap) {
+          // the first 32 entries of every worker's run, loaded at once
+          int32_t ix[kPre];
+          float vx[kPre];
+          bool ok[kPre];
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) {
+            const int w = wb + u;
+            const int src = w & 31;
+            const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+            const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+            // int32 packets have k <= 2^31, so these sums cannot wrap
+            const uint32_t j = l + lane;
+            ok[u] = w < a.W && j < h;
+            ix[u] = ok[u] ? a.indices[w][j] : 0;
+            vx[u] = ok[u] ? a.values[w][j] : 0.0f;
+          }
+          // added strictly in worker order; a run longer than 32 entries is
+          // finished before the next worker starts
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) {
+            const int w = wb + u;
+            if (w >= a.W) break;  // warp-uniform
+            const int64_t slot = (int64_t)ix[u] - t0;
+            if (ok[u] && slot >= 0 && slot < tlen) {
+              acc[slot] = __fadd_rn(acc[slot], vx[u]);
               atomicOr(&touched[slot >> 5], 1u << (slot & 31));
+            }
+            __syncwarp();
+            const int src = w & 31;
+            const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+            const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+            for (uint32_t off = 32; l + off < h; off += 32) {
+              const uint32_t j = l + off + lane;
+              if (j < h) {
+                const int64_t sl = (int64_t)a.indices[w][j] - t0;
+                if (sl >= 0 && sl < tlen) {
+                  acc[sl] = __fadd_rn(acc[sl], a.values[w][j]);
+                  atomicOr(&touched[sl >> 5], 1u << (sl & 31));
+                }
+              }
+              __syncwarp();
             }
           }
         } else {
-          const int64_t wi = t0 / 32 + tid;
-          uint32_t word = 0;
-          if (tid * 32 < tlen) {
-            word = __ldg(a.bitmaps[w] + wi);
-            const int rem = tlen - tid * 32;
-            if (rem < 32) word &= (1u << rem) - 1u;
+          uint32_t word[kPre];
+          const int64_t wi = t0 / 32 + lane;
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) {
+            const int w = wb + u;
+            word[u] = 0;
+            if (w < a.W && (int)lane * 32 < tlen) {
+              word[u] = __ldg(a.bitmaps[w] + wi);
+              const int rem = tlen - (int)lane * 32;
+              if (rem < 32) word[u] &= (1u << rem) - 1u;
+            }
           }
-          uint32_t tot;
-          const uint32_t ex = block_excl_scan(__popc(word), scratch, &tot);
-          int64_t j = lo + ex;
-          touched[tid] |= word;
-          while (word) {
-            const int b = __ffs(word) - 1;
-            word &= word - 1;
-            if (j < hi) acc[tid * 32 + b] = __fadd_rn(acc[tid * 32 + b], vals[j]);
-            ++j;
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) {
+            const int w = wb + u;
+            if (w >= a.W) break;  // warp-uniform
+            const int src = w & 31;
+            const int64_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+            const int64_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+            const uint32_t c = __popc(word[u]);
+            int64_t j = l + (int64_t)(warp_incl_scan(c) - c);
+            uint32_t wd = word[u];
+            touched[lane] |= wd;
+            while (wd) {
+              const int bpos = __ffs(wd) - 1;
+              wd &= wd - 1;
+              if (j < h)
+                acc[lane * 32 + bpos] = __fadd_rn(acc[lane * 32 + bpos], a.values[w][j]);
+              ++j;
+            }
+            __syncwarp();
           }
         }
-        __syncthreads();
       }
     }
     if (G) {
       float* gt = G + t0;
-      if (g_vec && tlen == kATile) {
+      if (g_vec && tlen == kWT) {
 #pragma unroll
-        for (int r = 0; r < kATile / 4 / kAThreads; ++r)
-          __stcs(reinterpret_cast<float4*>(gt) + r * kAThreads + tid, acc4[r * kAThreads + tid]);
+        for (int r = 0; r < kWT / 128; ++r)
+          __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, acc4[r * 32 + lane]);
       } else {
-        for (int i = tid; i < tlen; i += kAThreads) gt[i] = acc[i];
+        for (int i = lane; i < tlen; i += 32) gt[i] = acc[i];
       }
     }
-    uint32_t word = touched[tid];
-    while (word) {
-      const int b = __ffs(word) - 1;
-      word &= word - 1;
-      const int slot = tid * 32 + b;
+    uint32_t tw = touched[lane];
+    while (tw) {
+      const int bpos = __ffs(tw) - 1;
+      tw &= tw - 1;
+      const int slot = lane * 32 + bpos;
       const int64_t i = t0 + slot;
       wts[i] = __fsub_rn(wts[i], __fmul_rn(a.eta, acc[slot]));
     }
-    __syncthreads();
+    __syncwarp();
   }
 }
 
-int64_t agg_tiles(int64_t n) { return (n + kATile - 1) / kATile; }
+int64_t agg_tiles(int64_t n) { return (n + kWT - 1) / kWT; }
 
+int64_t agg_chunks(int64_t n) { return (agg_tiles(n) + kScanTiles - 1) / kScanTiles; }
+
+// Workspace: status header | run boundaries uint32[W][tiles + 1] | (bitmap
+// packets) ticket word, 256 bytes | look-back states uint64[W][chunks].
 size_t agg_bytes(int32_t W, int32_t idx_format, int64_t n) {
   const int64_t nt = agg_tiles(n);
   size_t off = sizeof(WsHeader);
-  off = round_up(off + (size_t)W * (nt + 1) * 8, 256);
-  if (idx_format == EF_IDX_BITMAP) off = round_up(off + (size_t)W * nt * 4, 256);
+  off = round_up(off + (size_t)W * (nt + 1) * 4, 256);
+  if (idx_format == EF_IDX_BITMAP) off = round_up(off + 256 + (size_t)W * agg_chunks(n) * 8, 256);
   return off;
 }
 
@@ -277,7 +356,7 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
   a.kbase[0] = 0;
   for (int i = 0; i < W; ++i) {
     const int64_t k = h_k[i];
-    if (k < 0 || k > n) return EF_ERR_K;
+    if (k < 0 || k > n || k > (int64_t)0xFFFFFFFF) return EF_ERR_K;
     if (k > 0 && !h_values[i]) return EF_ERR_NULL;
     if (h_values[i] && !aligned4(h_values[i])) return EF_ERR_ALIGN;
     const size_t kb = (size_t)k * 4;
@@ -309,7 +388,7 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
   if (err != cudaSuccess) return cuda_fail(err);
   if (n == 0) return EF_OK;
   int32_t* status = reinterpret_cast<int32_t*>(ws);
-  int64_t* start = reinterpret_cast<int64_t*>(ws + sizeof(WsHeader));
+  uint32_t* start = reinterpret_cast<uint32_t*>(ws + sizeof(WsHeader));
   const int64_t nt = a.ntiles;
   if (!bitmap) {
     const int64_t work = std::max<int64_t>(a.kbase[W], (int64_t)W * (nt + 1));
@@ -318,18 +397,23 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
     agg_starts_int32<<<grid, kAThreads, 0, s>>>(a, start, status);
     if ((st = check_launch()) != EF_OK) return st;
   } else {
-    uint32_t* counts = reinterpret_cast<uint32_t*>(
-        ws + round_up(sizeof(WsHeader) + (size_t)W * (nt + 1) * 8, 256));
+    char* ctl = ws + round_up(sizeof(WsHeader) + (size_t)W * (nt + 1) * 4, 256);
+    const size_t ctl_bytes = 256 + (size_t)W * agg_chunks(n) * 8;
+    err = cudaMemsetAsync(ctl, 0, ctl_bytes, s);
+    if (err != cudaSuccess) return cuda_fail(err);
     const int grid = (int)std::max<int64_t>(
-        1, std::min<int64_t>((int64_t)W * nt, (int64_t)dev.sms * 8));
-    agg_count_bitmap<<<grid, kAThreads, 0, s>>>(a, counts);
-    if ((st = check_launch()) != EF_OK) return st;
-    agg_scan_bitmap<<<W, 1024, 0, s>>>(a, counts, start, status);
+        1, std::min<int64_t>((int64_t)W * agg_chunks(n), (int64_t)dev.sms * 4));
+    agg_bitmap_starts<<<grid, kAThreads, 0, s>>>(a, start, reinterpret_cast<uint64_t*>(ctl + 256),
+                                                 reinterpret_cast<uint32_t*>(ctl), status);
     if ((st = check_launch()) != EF_OK) return st;
   }
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nt, (int64_t)dev.sms * 6));
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>((nt + kAWarps - 1) / kAWarps, (int64_t)dev.sms * 6));
   prof_begin(EF_KERNEL_SPARSE_APPLY, s);
-  agg_apply<<<grid, kAThreads, 0, s>>>(a, start, G, w);
+  if (bitmap)
+    agg_apply<true><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+  else
+    agg_apply<false><<<grid, kAThreads, 0, s>>>(a, start, G, w);
   if ((st = check_launch()) != EF_OK) return st;
   prof_end(EF_KERNEL_SPARSE_APPLY, s);
   return EF_OK;
