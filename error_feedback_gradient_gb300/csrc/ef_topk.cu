@@ -57,6 +57,7 @@ constexpr int kEmitThreads = 256;  // 8 warps x 16 rounds x 32 lanes = kChunk
 constexpr int kMaxLarge = 128;     // segments per streaming batch
 constexpr int kMaxSmall = 512;     // segments per small-path launch
 constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
+constexpr int kSelSmall = 32768;  // lists up to this length are selected by one CTA
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
 static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
@@ -94,12 +95,13 @@ struct SegState {
   uint32_t krem;    // rank still to find inside the prefix (= need)
   uint32_t gt;
   uint32_t overflow;  // a warp's staging area overflowed: the list is incomplete
+  uint32_t resolved;  // T and need already found (list fitted in one CTA)
+  uint32_t chunks_done[3];  // chunks of the list histogrammed per digit pass
 };
 
 struct alignas(256) Ctl {
   uint32_t fused_ticket, fused_done;
   uint32_t emit_ticket;
-  uint32_t sel_done[3];
   int64_t total_chunks;
 };
 
@@ -148,24 +150,58 @@ topk_small(SmallBatch b, IO io, int keys_words) {
   __syncthreads();
   if (sg.k == 0) return;
   const SelectResult r = block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch);
-  uint32_t run_gt = 0, run_eq = 0;
-  for (int r0 = 0; r0 < len; r0 += blockDim.x) {
-    const int i = r0 + threadIdx.x;
-    const bool in = i < len;
-    const uint32_t bits = in ? gbits[i] : 0u;
+  // Ordered emit: warp w owns the contiguous range [w * span, (w + 1) * span);
+  // one pass counts (greater, equal) per warp, one scan of the 32 warp counts
+  // gives each warp its offsets, and a second pass emits with ballots.
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int span = ((len + nwarps - 1) / nwarps + 31) & ~31;
+  const int w0 = warp * span, w1 = min(w0 + span, len);
+  uint32_t cg = 0, ce = 0;
+  for (int i = w0 + (int)lane; i < w1; i += 32) {
+    const uint32_t key = gbits[i] & 0x7FFFFFFFu;
+    cg += key > r.T;
+    ce += key == r.T;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(kFull, cg, o);
+    ce += __shfl_xor_sync(kFull, ce, o);
+  }
+  uint32_t* wgt = hist;            // the histogram is free again: reuse it
+  uint32_t* weq = hist + 32;
+  if (lane == 0) {
+    wgt[warp] = cg;
+    weq[warp] = ce;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t g = lane < (unsigned)nwarps ? wgt[lane] : 0u;
+    const uint32_t q = lane < (unsigned)nwarps ? weq[lane] : 0u;
+    const uint32_t ig = warp_incl_scan(g), iq = warp_incl_scan(q);
+    if (lane < (unsigned)nwarps) {
+      wgt[lane] = ig - g;
+      weq[lane] = iq - q;
+    }
+  }
+  __syncthreads();
+  uint32_t run_gt = wgt[warp], run_eq = weq[warp];
+  const unsigned lm = lanemask_lt();
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + (int)lane;
+    const uint32_t bits = i < w1 ? gbits[i] : 0u;
     const uint32_t key = bits & 0x7FFFFFFFu;
-    const bool gt = in && key > r.T;
-    const bool eq = in && key == r.T;
-    uint32_t tot;
-    const uint32_t ex = block_excl_scan(((uint32_t)gt << 16) | (uint32_t)eq, scratch, &tot);
-    const uint32_t gt_before = run_gt + (ex >> 16);
-    const uint32_t eq_before = run_eq + (ex & 0xFFFFu);
+    const bool gt = i < w1 && key > r.T;
+    const bool eq = i < w1 && key == r.T;
+    const unsigned bg = __ballot_sync(kFull, gt), bq = __ballot_sync(kFull, eq);
+    const uint32_t gt_before = run_gt + __popc(bg & lm);
+    const uint32_t eq_before = run_eq + __popc(bq & lm);
     if (gt || (eq && eq_before < r.need)) {
       const int64_t pos = sg.out_off + gt_before + min(eq_before, r.need);
       emit_one(io, sg.off + i, pos, sg.out_off + sg.k, __uint_as_float(bits));
     }
-    run_gt += tot >> 16;
-    run_eq += tot & 0xFFFFu;
+    run_gt += __popc(bg);
+    run_eq += __popc(bq);
   }
 }
 
@@ -173,8 +209,43 @@ topk_small(SmallBatch b, IO io, int keys_words) {
 // streaming path
 // ---------------------------------------------------------------------------
 
+constexpr int kSampleCtas = 32;      // CTAs gathering one segment's samples
+constexpr int kSampleThreads = 256;  // kSample / kSampleCtas / kSampleThreads per thread
+
+// Gathers the compensated keys at the sample positions of every streaming
+// segment: sample j of a segment sits at off + floor((2j + 1) * len /
+// (2 * kSample)).  Spread over kSampleCtas CTAs per segment so that the
+// scattered reads use many SMs; eight samples' loads per thread are issued
+// before any is used.
+__global__ void __launch_bounds__(kSampleThreads)
+topk_sample(LargeBatch b, IO io, uint32_t* samples) {
+  static_assert((kSample & (kSample - 1)) == 0, "sample count must be a power of two");
+  constexpr int kShift = __builtin_ctz(2 * kSample);
+  constexpr int kPer = kSample / (kSampleCtas * kSampleThreads);
+  static_assert(kPer == 4, "sampling layout");
+  const int s = blockIdx.x / kSampleCtas;
+  const LargeSeg& d = b.seg[s];
+  if (d.rank <= 0 || d.rank > kSample) return;
+  const int64_t j0 = (int64_t)(blockIdx.x % kSampleCtas) * kSampleThreads * kPer + threadIdx.x;
+  float gv[kPer], ev[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int64_t j = j0 + (int64_t)u * kSampleThreads;
+    const int64_t p = d.off + (((2 * j + 1) * d.len) >> kShift);
+    gv[u] = io.g_raw[p];
+    ev[u] = io.e[p];
+  }
+  uint32_t* out = samples + (int64_t)s * kSample;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    out[j0 + (int64_t)u * kSampleThreads] = abs_key(__fadd_rn(gv[u], ev[u]));
+}
+
+// One CTA per streaming segment: T_lo = the rank-th largest sampled key, a
+// conservative lower threshold for the candidate list (a speed-up only; the
+// result never depends on it), and the segment's state for the later passes.
 __global__ void __launch_bounds__(kPrepThreads)
-topk_prepare(LargeBatch b, int nseg, IO io, SegState* st) {
+topk_prepare(LargeBatch b, int nseg, const uint32_t* samples, SegState* st) {
   extern __shared__ uint32_t sm[];
   uint32_t* keys = sm;
   uint32_t* hist = sm + kSample;
@@ -188,10 +259,9 @@ topk_prepare(LargeBatch b, int nseg, IO io, SegState* st) {
   } else if (d.rank > kSample) {
     t_lo = 0;
   } else {
-    for (int j = threadIdx.x; j < kSample; j += blockDim.x) {
-      const int64_t p = d.off + ((2 * (int64_t)j + 1) * d.len) / (2 * (int64_t)kSample);
-      keys[j] = abs_key(__fadd_rn(io.g_raw[p], io.e[p]));
-    }
+    const uint4* src = reinterpret_cast<const uint4*>(samples + (int64_t)s * kSample);
+    uint4* dst = reinterpret_cast<uint4*>(keys);
+    for (int j = threadIdx.x; j < kSample / 4; j += blockDim.x) dst[j] = src[j];
     __syncthreads();
     t_lo = block_radix_select(keys, kSample, (uint32_t)d.rank, hist, scratch).T;
   }
@@ -206,6 +276,8 @@ topk_prepare(LargeBatch b, int nseg, IO io, SegState* st) {
     v.krem = (uint32_t)d.k;
     v.gt = 0;
     v.overflow = 0;
+    v.resolved = 0;
+    v.chunks_done[0] = v.chunks_done[1] = v.chunks_done[2] = 0;
     st[s] = v;
   }
 }
@@ -451,6 +523,40 @@ __device__ __forceinline__ ListRef list_ref(const SegState* st, int seg) {
   return r;
 }
 
+// Lists of at most kSelSmall entries: one CTA per segment loads the keys into
+// shared memory and runs the 3-digit radix select there.
+__global__ void __launch_bounds__(kSmallThreads)
+topk_select_small(IO io, SegState* st, const uint2* cand) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* keys = sm;
+  uint32_t* hist = sm + kSelSmall;
+  uint32_t* scratch = hist + 2048;
+  const int seg = blockIdx.x;
+  const ListRef l = list_ref(st, seg);
+  const int64_t k = st[seg].d.k;
+  if (k == 0 || l.len == 0 || l.len > kSelSmall) return;
+  const int len = (int)l.len;
+  if (l.mode == 0) {
+    const uint2* cl = cand + l.cand_base;
+    for (int j = threadIdx.x; j < len; j += blockDim.x) keys[j] = cl[j].y;
+  } else {
+    const float* el = io.e + l.off;
+    for (int j = threadIdx.x; j < len; j += blockDim.x) keys[j] = __float_as_uint(el[j]);
+  }
+  __syncthreads();
+  const SelectResult r = block_radix_select(keys, len, (uint32_t)k, hist, scratch);
+  if (threadIdx.x == 0) {
+    st[seg].prefix = r.T;
+    st[seg].krem = r.need;
+    st[seg].gt = r.gt;
+    st[seg].resolved = 1;
+  }
+}
+
+// Longer lists: one digit pass over the chunks of every unresolved list.
+// Each CTA builds a shared-memory histogram of a chunk and
+// merges it into its segment's global histogram; the CTA that merges a
+// segment's last chunk fixes that digit for the segment.
 __global__ void __launch_bounds__(kSelThreads)
 topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, Ctl* ctl,
             int pass) {
@@ -468,6 +574,7 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
   __syncthreads();
   for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
     const int seg = find_seg(s_cb, nseg, c);
+    if (st[seg].resolved) continue;  // uniform across the CTA
     const ListRef l = list_ref(st, seg);
     const uint32_t prefix = st[seg].prefix;
     const int64_t j0 = (c - s_cb[seg]) * kChunk;
@@ -489,30 +596,30 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
       }
     }
     __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(&ctl->sel_done[pass], 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int seg = 0; seg < nseg; ++seg) {
-    if (st[seg].d.k == 0) continue;
-    uint32_t* gh = ghist + (int64_t)seg * 2048;
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-      sh[b] = *reinterpret_cast<volatile uint32_t*>(&gh[b]);
-      gh[b] = 0;
-    }
-    __syncthreads();
-    uint32_t bin, above;
-    block_find_bin(sh, nb, st[seg].krem, scratch, &bin, &above);
     if (threadIdx.x == 0) {
-      st[seg].prefix |= bin << shift;
-      st[seg].krem -= above;
-      st[seg].gt += above;
+      __threadfence();
+      const int64_t nch = s_cb[seg + 1] - s_cb[seg];
+      s_last = (int64_t)atomicAdd(&st[seg].chunks_done[pass], 1u) == nch - 1;
     }
     __syncthreads();
+    if (s_last) {
+      __threadfence();
+      uint32_t* gh = ghist + (int64_t)seg * 2048;
+      for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        sh[b] = *reinterpret_cast<volatile uint32_t*>(&gh[b]);
+        gh[b] = 0;
+      }
+      __syncthreads();
+      uint32_t bin, above;
+      block_find_bin(sh, nb, st[seg].krem, scratch, &bin, &above);
+      if (threadIdx.x == 0) {
+        st[seg].prefix |= bin << shift;
+        st[seg].krem -= above;
+        st[seg].gt += above;
+      }
+      for (int b = threadIdx.x; b < nb; b += blockDim.x) sh[b] = 0;
+      __syncthreads();
+    }
   }
 }
 
@@ -641,6 +748,7 @@ struct Plan {
   int64_t total_k = 0;
   // workspace regions (byte offsets); batches reuse the same regions
   size_t off_ctl = 0, off_st = 0, off_hist = 0, off_tiles = 0, off_chunks = 0, off_cand = 0;
+  size_t off_samples = 0;
   size_t ctl_clear_bytes = 0;  // bytes cleared from off_ctl before each batch
   size_t bytes = 0;
 };
@@ -696,8 +804,9 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
   if (!cur.segs.empty()) p->batches.push_back(cur);
   p->total_k = out_off;
 
-  int64_t tiles = 0, chunks = 0, cands = 0;
+  int64_t tiles = 0, chunks = 0, cands = 0, segs = 0;
   for (const Batch& b : p->batches) {
+    segs = std::max(segs, (int64_t)b.segs.size());
     tiles = std::max(tiles, b.max_tiles);
     chunks = std::max(chunks, b.max_chunks);
     cands = std::max(cands, b.cand_total);
@@ -717,6 +826,8 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     p->ctl_clear_bytes = off - p->off_ctl;
     p->off_cand = off;
     off = round_up(off + (size_t)cands * 8, 256);
+    p->off_samples = off;
+    off = round_up(off + (size_t)segs * kSample * 4, 256);
   }
   p->bytes = off;
   return EF_OK;
@@ -734,9 +845,11 @@ ef_status set_attributes(int dev) {
                                           small_smem);
     cudaError_t e2 = cudaFuncSetAttribute(topk_prepare,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
-    g_attr_status[dev] = (e1 == cudaSuccess && e2 == cudaSuccess)
-                             ? EF_OK
-                             : cuda_fail(e1 != cudaSuccess ? e1 : e2);
+    const int sel_smem = (kSelSmall + 2048 + 64) * 4;
+    cudaError_t e3 = cudaFuncSetAttribute(topk_select_small,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
+    cudaError_t bad = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    g_attr_status[dev] = bad == cudaSuccess ? EF_OK : cuda_fail(bad);
   });
   return g_attr_status[dev];
 }
@@ -847,14 +960,20 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     }
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
+    uint32_t* samples = reinterpret_cast<uint32_t*>(ws + p.off_samples);
+    topk_sample<<<nsg * kSampleCtas, kSampleThreads, 0, s>>>(lb, io, samples);
+    if ((st = check_launch()) != EF_OK) return st;
     const size_t prep_smem = (size_t)(kSample + 2048 + 64) * 4;
-    topk_prepare<<<nsg, kPrepThreads, prep_smem, s>>>(lb, nsg, io, sst);
+    topk_prepare<<<nsg, kPrepThreads, prep_smem, s>>>(lb, nsg, samples, sst);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
     topk_fused<<<fgrid, kFusedThreads, 0, s>>>(io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
+    topk_select_small<<<nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s>>>(io, sst,
+                                                                                      cand);
+    if ((st = check_launch()) != EF_OK) return st;
     const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 2));
     for (int pass = 0; pass < 3; ++pass) {
       topk_select<<<sgrid, kSelThreads, 0, s>>>(io, sst, nsg, cand, ghist, ctl, pass);
