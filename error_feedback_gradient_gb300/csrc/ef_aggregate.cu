@@ -13,7 +13,7 @@
 //     per worker.
 // The apply kernel gives each tile to one warp (48 tiles in flight per SM,
 // enough to cover the dependent loads of a tile): the warp loads the run
-// bounds of all workers at once, then the runs' entries of up to 8 workers
+// bounds of all workers at once, then the runs' entries of up to 4 workers
 // at once, adds them worker by worker into a shared-memory copy of the tile
 // (no atomics on values; indices inside one packet are distinct), writes the
 // dense tile of G with 16-byte stores, and updates w only where touched.
@@ -32,7 +32,7 @@ namespace {
 constexpr int kWT = 1024;            // elements per warp tile
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
-constexpr int kPre = 8;              // workers whose run entries are loaded at once
+constexpr int kPre = 4;              // workers whose run entries are loaded at once
 
 struct AggArgs {
   const float* values[EF_MAX_WORKERS];
@@ -112,12 +112,36 @@ agg_bitmap_starts(AggArgs a, uint32_t* start, uint64_t* cstate, uint32_t* ticket
     const int64_t t0 = c * kScanTiles;
     const int ntl = (int)min((int64_t)kScanTiles, a.ntiles - t0);
     const uint32_t* bm = a.bitmaps[w];
-    for (int i = warp; i < ntl; i += kAWarps) {
-      const int64_t wi = (t0 + i) * (kWT / 32) + lane;
-      uint32_t v = wi < nwords ? __popc(__ldg(bm + wi)) : 0u;
+    // A tile is 32 words; lane l of a warp reads words 4l..4l+3 of a 4-tile
+    // group (16 bytes, when the bitmap is 16-byte aligned), so 8 lanes share
+    // a tile.  Four groups are loaded before any is counted.
+    const bool v16 = (reinterpret_cast<uintptr_t>(bm) & 15u) == 0;
+    for (int i0 = warp * 16; i0 < ntl; i0 += kAWarps * 16) {
+      uint32_t c[4];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-      if (lane == 0) cnt[i] = v;
+      for (int u = 0; u < 4; ++u) {
+        const int tile = i0 + u * 4 + (int)(lane >> 3);
+        const int64_t wi = (t0 + tile) * (kWT / 32) + (lane & 7) * 4;
+        c[u] = 0;
+        if (tile < ntl) {
+          if (v16 && wi + 4 <= nwords) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(bm + wi));
+            c[u] = __popc(q.x) + __popc(q.y) + __popc(q.z) + __popc(q.w);
+          } else {
+            for (int r = 0; r < 4; ++r)
+              if (wi + r < nwords) c[u] += __popc(__ldg(bm + wi + r));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t v = c[u];
+        v += __shfl_xor_sync(kFull, v, 1);
+        v += __shfl_xor_sync(kFull, v, 2);
+        v += __shfl_xor_sync(kFull, v, 4);
+        const int tile = i0 + u * 4 + (int)(lane >> 3);
+        if ((lane & 7) == 0 && tile < ntl) cnt[tile] = v;
+      }
     }
     __syncthreads();
     // thread t scans tiles [t * per, (t + 1) * per) of the chunk
@@ -167,7 +191,7 @@ __device__ __forceinline__ void run_of(const AggArgs& a, const uint32_t* start, 
 }
 
 template <bool kBitmap>
-__global__ void __launch_bounds__(kAThreads)
+__global__ void __launch_bounds__(kAThreads, 6)
 agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
   __shared__ __align__(16) float acc_all[kAWarps][kWT];
   __shared__ uint32_t touched_all[kAWarps][kWT / 32];
@@ -184,7 +208,21 @@ agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __rest
     if ((int)lane < a.W) run_of(a, start, lane, t, &lo0, &hi0);
     if ((int)lane + 32 < a.W) run_of(a, start, lane + 32, t, &lo1, &hi1);
     const bool any = __any_sync(kFull, hi0 > lo0 || hi1 > lo1);
-    if (!any && !G) continue;
+    // The dense tile of G is written as zeros first: those stores depend on
+    // nothing, so they stream while the tile's entries are fetched.  The
+    // touched slots are overwritten with their sums at the end.
+    const bool g_full = G && g_vec && tlen == kWT;
+    if (G) {
+      float* gt = G + t0;
+      if (g_full) {
+#pragma unroll
+        for (int r = 0; r < kWT / 128; ++r)
+          __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, make_float4(0.f, 0.f, 0.f, 0.f));
+      } else {
+        for (int i = lane; i < tlen; i += 32) gt[i] = 0.0f;
+      }
+    }
+    if (!any) continue;
     float4* acc4 = reinterpret_cast<float4*>(acc);
 #pragma unroll
     for (int r = 0; r < kWT / 128; ++r) acc4[r * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -272,22 +310,14 @@ agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __rest
         }
       }
     }
-    if (G) {
-      float* gt = G + t0;
-      if (g_vec && tlen == kWT) {
-#pragma unroll
-        for (int r = 0; r < kWT / 128; ++r)
-          __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, acc4[r * 32 + lane]);
-      } else {
-        for (int i = lane; i < tlen; i += 32) gt[i] = acc[i];
-      }
-    }
+    __syncwarp();  // orders this warp's zero stores before the sums below
     uint32_t tw = touched[lane];
     while (tw) {
       const int bpos = __ffs(tw) - 1;
       tw &= tw - 1;
       const int slot = lane * 32 + bpos;
       const int64_t i = t0 + slot;
+      if (G) G[i] = acc[slot];
       wts[i] = __fsub_rn(wts[i], __fmul_rn(a.eta, acc[slot]));
     }
     __syncwarp();

@@ -74,9 +74,36 @@ void prof_end(int kernel_id, cudaStream_t s) {
     cudaEventRecord(t_prof[kernel_id].stop, s);
 }
 
+namespace {
+
+// Tile 1 of a fresh state array waits on tile 0, which is never published.
+__global__ void selftest_wait_kernel(uint64_t* states, int32_t* status, uint64_t limit_ns) {
+  lookback_warp(states, 1, 0, 1, status, limit_ns);
+}
+
+}  // namespace
 }  // namespace ef
 
 extern "C" {
+
+ef_status ef_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                   void* stream) {
+  if (!workspace) return EF_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 512)
+    return EF_ERR_WORKSPACE;
+  if (limit_ns < 1000000 || limit_ns > 10000000000ll) return EF_ERR_ARG;
+  ef::DeviceInfo dev;
+  ef_status st = ef::current_device(&dev);
+  if (st != EF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  cudaError_t err = cudaMemsetAsync(ws, 0, 512, s);
+  if (err != cudaSuccess) return ef::cuda_fail(err);
+  ef::selftest_wait_kernel<<<1, 32, 0, s>>>(reinterpret_cast<uint64_t*>(ws + 256),
+                                            reinterpret_cast<int32_t*>(ws),
+                                            (uint64_t)limit_ns);
+  return ef::check_launch();
+}
 
 int32_t ef_abi_version(void) { return EF_ABI_VERSION; }
 

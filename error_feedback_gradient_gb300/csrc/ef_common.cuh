@@ -155,7 +155,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // and returns the exclusive prefix (same value in every lane).
 __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile,
                                                   int64_t first, uint64_t agg,
-                                                  int32_t* status) {
+                                                  int32_t* status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   const unsigned lane = lane_id();
   if (tile == first) {
     if (lane == 0) st_release(&states[tile], kFlagIncl | agg);
@@ -175,7 +176,7 @@ __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile
       if ((++spins & 63u) == 0) {
         int bad = 0;
         if (lane == 0)
-          bad = (global_ns() - t0 > kWaitLimitNs) || (ld_volatile(status) != 0) ||
+          bad = (global_ns() - t0 > limit_ns) || (ld_volatile(status) != 0) ||
                 spins > (1u << 26);
         bad = __shfl_sync(kFull, bad, 0);
         if (bad) {

@@ -23,7 +23,8 @@ namespace ef {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;  // 128-element groups in flight per warp
+constexpr int kUnroll = 4;       // 128-element groups in flight per warp (sender)
+constexpr int kApplyUnroll = 2;  // float4 chunks in flight per thread (receiver)
 
 __device__ __forceinline__ float sign_step(float g, float e, float b1, float c, bool* bit) {
   const float v = __fadd_rn(g, e);
@@ -131,20 +132,20 @@ __device__ __forceinline__ float apply_one(float x, float G, const SignApplyArgs
 
 // Float4 chunks [0, nchunks): G = 2 * (#set bits) - W (the exact sum of W
 // terms +-1), then the update.  w and G must be 16-byte aligned.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
 sign_apply_vec(SignApplyArgs a, float* __restrict__ G, float* __restrict__ x,
                int64_t nchunks) {
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t q0 = tid; q0 < nchunks; q0 += nthr * kUnroll) {
-    float4 xv[kUnroll];
+  for (int64_t q0 = tid; q0 < nchunks; q0 += nthr * kApplyUnroll) {
+    float4 xv[kApplyUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kApplyUnroll; ++u) {
       const int64_t q = q0 + (int64_t)u * nthr;
       if (q < nchunks) xv[u] = __ldcs(reinterpret_cast<const float4*>(x) + q);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kApplyUnroll; ++u) {
       const int64_t q = q0 + (int64_t)u * nthr;
       if (q >= nchunks) break;
       const int64_t i = q * 4;
@@ -272,7 +273,7 @@ extern "C" ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bi
   if (aligned16(w_or_m) && (!G || aligned16(G))) {
     const int64_t nchunks = n / 4;
     if (nchunks > 0) {
-      const int grid = grid_for(nchunks, kThreads * kUnroll, dev.sms, 8);
+      const int grid = grid_for(nchunks, kThreads * kApplyUnroll, dev.sms, 8);
       sign_apply_vec<<<grid, kThreads, 0, s>>>(a, G, w_or_m, nchunks);
       if ((st = check_launch()) != EF_OK) return st;
     }

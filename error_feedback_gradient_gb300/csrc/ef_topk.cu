@@ -42,8 +42,8 @@ namespace {
 constexpr int kSmallMax = 32768;
 constexpr int kSmallThreads = 1024;
 constexpr int kStreamWarps = 8;                 // fused pass: warps that stream the tile
-constexpr int kWarpSpan = 2048;                 // elements per streaming warp per tile
-constexpr int kTile = kStreamWarps * kWarpSpan;  // 16384 elements per fused-pass tile
+constexpr int kWarpSpan = 4096;                 // elements per streaming warp per tile
+constexpr int kTile = kStreamWarps * kWarpSpan;  // 32768 elements per fused-pass tile
 constexpr int kStreamThreads = kStreamWarps * 32;
 constexpr int kFusedThreads = kStreamThreads + 32;  // + one scan warp
 constexpr int kStageCap = 256;                  // staged candidates per warp per buffer
