@@ -39,6 +39,32 @@ if ROOT not in sys.path:
 METRIC = "G grad elements/s per EF compress+apply step; HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "G grad elements/s"
 
+# DRAM traffic of one topk_fused launch from one ncu capture (--set full,
+# slab workload at n = 2^26 per worker, see profiles/): 536.97 MB read +
+# 220.88 MB written = 11.293 bytes per element.  Reported, scaled by n, only
+# while the kernel sources still hash to what was captured; otherwise null.
+# (Reads scale with n exactly; the writes fall short of 12 B by the dirty
+# lines still in L2 when the captured launch ends.)
+FUSED_TRAFFIC_PER_ELEMENT = 11.293
+FUSED_TRAFFIC_SOURCES = {
+    "error_feedback_gradient_gb300/csrc/ef_topk.cu":
+        "fed6dec6edd10a05e06608d206fe30fbfab01b74f1e199147a4ebd52a5686a01",
+    "error_feedback_gradient_gb300/csrc/ef_common.cuh":
+        "8c82518cf4425bdd6f8024b355289fa0e638002f3e8476314350ba0271a997c1",
+}
+
+
+def fused_traffic(n: int):
+    import hashlib
+    for rel, digest in FUSED_TRAFFIC_SOURCES.items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return FUSED_TRAFFIC_PER_ELEMENT * n
+
 
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas; barrier + max over ranks)
@@ -336,15 +362,6 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     efg.library()
-    # CPU baseline first (rank 0, N = 1 only), before any large allocation
-    cpu = None
-    if rank == 0 and world == 1 and args.baseline_sample > 0:
-        units, dt, k = time_oracle(args.baseline_sample, args.workers)
-        cpu = {"value": units / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": (f"one oracle step on {args.workers} workers x {args.baseline_sample} "
-                          f"elements (k = {k}), all three variants, {dt:.1f} s"),
-               "host_cpus": os.cpu_count()}
-
     s = SlabStep(args.n, args.workers, dev)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
@@ -403,7 +420,8 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "hbm", "kernel": "topk_fused",
                 "achieved": top["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": top["achieved_gbs"] / peak, "peak_source": peak_kind,
-                "traffic": args.traffic_per_launch,
+                "traffic": (args.traffic_per_launch if args.traffic_per_launch is not None
+                            else fused_traffic(n)),
                 "algorithmic_bytes_per_launch": 12 * n}
     step_bytes = sum(ab.values())
 
@@ -423,13 +441,22 @@ def run_ours(args, rank, world, local):
                      "gbs": step_bytes / (ms_max * 1e-3) / 1e9,
                      "frac_of_peak": step_bytes / (ms_max * 1e-3) / 1e9 / peak},
         "roofline": roofline, "kernels": kernels,
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "cpu_baseline": None, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches,
     }
     del s
     torch.cuda.empty_cache()
     if args.extras and rank == 0:
         line["per_config"] = run_extras(args, dev)
+    # the CPU oracle baseline last (rank 0, N = 1 only), after the GPU legs,
+    # so its host allocations cannot disturb the pinned-memory uploads
+    if rank == 0 and world == 1 and args.baseline_sample > 0:
+        units, dt, k = time_oracle(args.baseline_sample, args.workers)
+        line["cpu_baseline"] = {
+            "value": units / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"one oracle step on {args.workers} workers x {args.baseline_sample} "
+                       f"elements (k = {k}), all three variants, {dt:.1f} s"),
+            "host_cpus": os.cpu_count()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -491,6 +518,17 @@ def run_e2e(args, s):
                 downloaded.record(down)
         main.wait_event(downloaded)
 
+    def run_serial(steps):
+        for t in range(steps):
+            for dst, src in zip(sets[0], host_g):
+                dst.copy_(src, non_blocking=True)
+            s.g = sets[0]
+            s.step()
+            for dst, src in zip(host_out, outs):
+                dst.copy_(src, non_blocking=True)
+
+    if args.e2e_mode == "serial":
+        run = run_serial        # noqa: F811
     run(1)
     torch.cuda.synchronize()
     barrier()
@@ -506,7 +544,7 @@ def run_e2e(args, s):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": world * s.units / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "uploads double-buffered against compute on separate streams"}
+            "mode": args.e2e_mode}
 
 
 def run_extras(args, dev):
@@ -615,6 +653,9 @@ def main(argv=None):
     p.add_argument("--workers", type=int, default=4)
     p.add_argument("--prof-steps", type=int, default=2)
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-mode", choices=["pipelined", "serial"], default="pipelined",
+                   help="pipelined: uploads double-buffered against compute on their own "
+                        "streams; serial: upload, step, download in turn")
     p.add_argument("--baseline-sample", type=int, default=1 << 27,
                    help="elements per worker in the timed oracle sample (0: skip)")
     p.add_argument("--ref-sample", type=int, default=1 << 21,
