@@ -218,3 +218,58 @@ def test_slab_2p31_receive_side_four_workers():
     torch.cuda.synchronize()
     assert_bits_equal(G[pt], G_want, "G (touched + sampled)")
     assert_bits_equal(wt[pt], w_want, "w (touched + sampled)")
+
+
+def test_bitmap_format_beyond_int32_range():
+    """Bitmap packets have no index limit: a step over n = 2^31 + 69,995
+    elements whose second tensor lies entirely beyond index 2^31 (the first,
+    just under 2^31 elements, keeps k = 0 and is only compensated); then the
+    receive side of that packet and a 1-bit step with a ragged tail."""
+    big = (1 << 31) - 5
+    small = 70_000
+    n = big + small
+    offs, ks = [0, big, n], [0, 700]
+    g = wl.student_t3(n, 1e-3, wl.seed(5, 7, 1), DEV)
+    e = wl.normal(n, 1e-4, wl.seed(5, 7, 2), DEV)
+    g_np, e_np = host(g), host(e)
+    want = oracle.topk_ef_step(g_np, e_np, offs, ks, "bitmap")
+    out = gpu_topk(g, e, offs, ks, efg.IDX_BITMAP)
+    torch.cuda.synchronize()
+    assert efg.workspace_status(out["ws"]) == 0
+    assert_bits_equal(out["values"], want["values"], "values")
+    nz = np.flatnonzero(want["bitmap"])
+    assert nz.min() >= (1 << 26) - 1                     # every set word lies past 2^31
+    assert_bits_equal(out["bitmap"], want["bitmap"], "bitmap")
+    assert_bits_equal(e, want["e"], "residual")
+    del e, e_np
+    # receive side of the bitmap packet over the same 2^31+ index space
+    wt = wl.normal(n, 0.02, wl.seed(5, 7, 3), DEV)
+    sel = np.flatnonzero(oracle.unpack_bits(want["bitmap"], n))
+    probe = np.unique(np.concatenate([sel, [0, (1 << 31) - 1, 1 << 31, n - 1]]))
+    pt = torch.from_numpy(probe).to(DEV)
+    w_probe = host(wt[pt])
+    G = torch.empty(n, device=DEV)
+    efg.sparse_aggregate_apply([out["values"]], None, [out["bitmap"]], [sum(ks)], n, 0.1, G, wt,
+                               idx_format=efg.IDX_BITMAP)
+    sub = {"indices": np.searchsorted(probe, sel).astype(np.int32), "values": want["values"]}
+    G_want = oracle.sparse_aggregate([sub], probe.size)
+    torch.cuda.synchronize()
+    assert_bits_equal(G[pt], G_want, "G")
+    assert_bits_equal(wt[pt], oracle.sgd_apply(w_probe, G_want, 0.1), "w")
+    del G, wt
+    # 1-bit step over the same length (ragged tail past 2^31), sampled
+    eps = wl.normal(n, 0.05, wl.seed(5, 7, 4), DEV)
+    rng = np.random.default_rng(8)
+    pos = np.unique(np.concatenate([rng.integers(0, n, 1 << 18), np.arange(n - 70, n)]))
+    pt = torch.from_numpy(pos).to(DEV)
+    g_s, e_s = g_np[pos], host(eps[pt])
+    bits = torch.empty((n + 31) // 32, dtype=torch.int32, device=DEV)
+    efg.sign_compress(g, eps, 0.9, bits)
+    bits_want, eps_want = oracle.sign_ef_step(g_s, e_s, 0.9)
+    torch.cuda.synchronize()
+    words = host(bits[torch.from_numpy(pos // 32).to(DEV)]).view(np.uint32)
+    got = ((words >> (pos % 32).astype(np.uint32)) & 1).astype(bool)
+    assert np.array_equal(got, oracle.unpack_bits(bits_want, pos.size))
+    assert_bits_equal(eps[pt], eps_want, "eps (sampled)")
+    last = host(bits[-1:]).view(np.uint32)[0]
+    assert last >> (n % 32) == 0                         # padding bits are 0
