@@ -115,3 +115,23 @@ def test_deterministic_repeat():
         outs.append((host(o["indices"]), host(o["values"]), host(e)))
     for a, b in zip(outs[0], outs[1]):
         assert_bits_equal(a, b, "repeat")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_many_tensors_use_several_batches(fmt):
+    """300 streaming tensors (more than one batch of 128) interleaved with
+    1100 small ones (more than one launch of 512), in one layerwise call."""
+    rng = np.random.default_rng(21)
+    sizes, ks = [], []
+    for i in range(1400):
+        if i % 14 < 3:                       # 300 streaming tensors
+            n_i = int(rng.integers(32769, 60000))
+            ks.append(int(rng.integers(0, 400)))
+        else:                                # 1100 small tensors
+            n_i = int(rng.integers(1, 300))
+            ks.append(int(rng.integers(0, n_i + 1)))
+        sizes.append(n_i)
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    assert sum(1 for s in sizes if s > 32768) == 300
+    check_topk_step(_t(n, 41), _t(n, 42, 1e-4), offs, ks, fmt)
