@@ -76,6 +76,8 @@ _SIGNATURES = {
     "ef_workspace_status": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.POINTER(ctypes.c_int32)]),
     "ef_profile_events": (ctypes.c_int32, [ctypes.c_int32, _c_vp, _c_vp]),
+    "ef_selftest_wait_timeout": (ctypes.c_int32, [_c_vp, ctypes.c_size_t, ctypes.c_int64,
+                                                  _c_vp]),
 }
 
 
@@ -244,6 +246,13 @@ def workspace_status(workspace: torch.Tensor, stream=None) -> int:
     _check(library().ef_workspace_status(_ptr(workspace), _stream(stream),
                                          ctypes.byref(out)), "ef_workspace_status")
     return int(out.value)
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait self-test (see include/efgrad.h)."""
+    _check(library().ef_selftest_wait_timeout(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_ns),
+        _stream(stream)), "ef_selftest_wait_timeout")
 
 
 def profile_events(kernel_id: int, start, stop) -> None:

@@ -261,6 +261,17 @@ EF_API ef_status ef_workspace_status(const void* workspace, void* stream,
                               int32_t* device_status);
 
 /* ------------------------------------------------------------------------
+ * Self-test of the bounded inter-block wait.  Launches one warp that runs
+ * the library's look-back wait on a predecessor whose state nothing ever
+ * publishes, with a wall-clock limit of limit_ns (1 ms .. 10 s).  The wait
+ * must give up, record EF_ERR_DEVICE_TIMEOUT in the workspace status word and
+ * return, leaving the context usable; read the result with
+ * ef_workspace_status().  workspace: >= 512 bytes, 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+EF_API ef_status ef_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                          int64_t limit_ns, void* stream);
+
+/* ------------------------------------------------------------------------
  * Profiling hook (per calling thread).  While set, every launch of kernel
  * `kernel_id` made by this thread is bracketed by cudaEventRecord(start) and
  * cudaEventRecord(stop) on the call's stream, so the caller can time that
