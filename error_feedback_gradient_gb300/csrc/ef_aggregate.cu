@@ -114,28 +114,29 @@ agg_bitmap_starts(AggArgs a, uint32_t* start, uint64_t* cstate, uint32_t* ticket
     const uint32_t* bm = a.bitmaps[w];
     // A tile is 32 words; lane l of a warp reads words 4l..4l+3 of a 4-tile
     // group (16 bytes, when the bitmap is 16-byte aligned), so 8 lanes share
-    // a tile.  Four groups are loaded before any is counted.
+    // a tile.  Eight groups are loaded before any is counted.
     const bool v16 = (reinterpret_cast<uintptr_t>(bm) & 15u) == 0;
-    for (int i0 = warp * 16; i0 < ntl; i0 += kAWarps * 16) {
-      uint32_t c[4];
+    for (int i0 = warp * 32; i0 < ntl; i0 += kAWarps * 32) {
+      uint4 q[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int tile = i0 + u * 4 + (int)(lane >> 3);
         const int64_t wi = (t0 + tile) * (kWT / 32) + (lane & 7) * 4;
-        c[u] = 0;
+        q[u] = make_uint4(0u, 0u, 0u, 0u);
         if (tile < ntl) {
           if (v16 && wi + 4 <= nwords) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(bm + wi));
-            c[u] = __popc(q.x) + __popc(q.y) + __popc(q.z) + __popc(q.w);
+            q[u] = __ldg(reinterpret_cast<const uint4*>(bm + wi));
           } else {
-            for (int r = 0; r < 4; ++r)
-              if (wi + r < nwords) c[u] += __popc(__ldg(bm + wi + r));
+            if (wi < nwords) q[u].x = __ldg(bm + wi);
+            if (wi + 1 < nwords) q[u].y = __ldg(bm + wi + 1);
+            if (wi + 2 < nwords) q[u].z = __ldg(bm + wi + 2);
+            if (wi + 3 < nwords) q[u].w = __ldg(bm + wi + 3);
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t v = c[u];
+      for (int u = 0; u < 8; ++u) {
+        uint32_t v = __popc(q[u].x) + __popc(q[u].y) + __popc(q[u].z) + __popc(q[u].w);
         v += __shfl_xor_sync(kFull, v, 1);
         v += __shfl_xor_sync(kFull, v, 2);
         v += __shfl_xor_sync(kFull, v, 4);
@@ -190,139 +191,380 @@ __device__ __forceinline__ void run_of(const AggArgs& a, const uint32_t* start, 
   *hi = h;
 }
 
+// One tile by the general method: every worker's run bounds, the tile's
+// zeros, then the runs' entries of up to kPre workers at once, added worker
+// by worker into a shared dense copy of the tile (no atomics on values;
+// indices inside one packet are distinct); touched slots get their sums in G
+// and their SGD update in w.  Its loads wait on one another (bounds, then
+// entries, then w).
+template <bool kBitmap>
+__device__ __forceinline__ void tile_general(const AggArgs& a, const uint32_t* start, int64_t t,
+                                             float* G, float* wts, bool g_vec, float* acc,
+                                             uint32_t* touched, unsigned lane) {
+  const int64_t t0 = t * kWT;
+  const int tlen = (int)min((int64_t)kWT, a.n - t0);
+  // run bounds of workers `lane` and `lane + 32`
+  uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+  if ((int)lane < a.W) run_of(a, start, lane, t, &lo0, &hi0);
+  if ((int)lane + 32 < a.W) run_of(a, start, lane + 32, t, &lo1, &hi1);
+  const bool any = __any_sync(kFull, hi0 > lo0 || hi1 > lo1);
+  // The dense tile of G is written as zeros first: those stores depend on
+  // nothing, so they stream while the tile's entries are fetched.  The
+  // touched slots are overwritten with their sums at the end.
+  const bool g_full = G && g_vec && tlen == kWT;
+  if (G) {
+    float* gt = G + t0;
+    if (g_full) {
+#pragma unroll
+      for (int r = 0; r < kWT / 128; ++r)
+        __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, make_float4(0.f, 0.f, 0.f, 0.f));
+    } else {
+      for (int i = lane; i < tlen; i += 32) gt[i] = 0.0f;
+    }
+  }
+  if (!any) return;
+  float4* acc4 = reinterpret_cast<float4*>(acc);
+#pragma unroll
+  for (int r = 0; r < kWT / 128; ++r) acc4[r * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  touched[lane] = 0;
+  __syncwarp();
+  if (any) {
+    for (int wb = 0; wb < a.W; wb += kPre) {
+      if (!kBitmap) {
+        // the first 32 entries of every worker's run, loaded at once
+        int32_t ix[kPre];
+        float vx[kPre];
+        bool ok[kPre];
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int w = wb + u;
+          const int src = w & 31;
+          const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+          const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+          // int32 packets have k <= 2^31, so these sums cannot wrap
+          const uint32_t j = l + lane;
+          ok[u] = w < a.W && j < h;
+          ix[u] = ok[u] ? a.indices[w][j] : 0;
+          vx[u] = ok[u] ? a.values[w][j] : 0.0f;
+        }
+        // added strictly in worker order; a run longer than 32 entries is
+        // finished before the next worker starts
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int w = wb + u;
+          if (w >= a.W) break;  // warp-uniform
+          const int64_t slot = (int64_t)ix[u] - t0;
+          if (ok[u] && slot >= 0 && slot < tlen) {
+            acc[slot] = __fadd_rn(acc[slot], vx[u]);
+            atomicOr(&touched[slot >> 5], 1u << (slot & 31));
+          }
+          __syncwarp();
+          const int src = w & 31;
+          const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+          const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+          for (uint32_t off = 32; l + off < h; off += 32) {
+            const uint32_t j = l + off + lane;
+            if (j < h) {
+              const int64_t sl = (int64_t)a.indices[w][j] - t0;
+              if (sl >= 0 && sl < tlen) {
+                acc[sl] = __fadd_rn(acc[sl], a.values[w][j]);
+                atomicOr(&touched[sl >> 5], 1u << (sl & 31));
+              }
+            }
+            __syncwarp();
+          }
+        }
+      } else {
+        uint32_t word[kPre];
+        const int64_t wi = t0 / 32 + lane;
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int w = wb + u;
+          word[u] = 0;
+          if (w < a.W && (int)lane * 32 < tlen) {
+            word[u] = __ldg(a.bitmaps[w] + wi);
+            const int rem = tlen - (int)lane * 32;
+            if (rem < 32) word[u] &= (1u << rem) - 1u;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          const int w = wb + u;
+          if (w >= a.W) break;  // warp-uniform
+          const int src = w & 31;
+          const int64_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
+          const int64_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
+          const uint32_t c = __popc(word[u]);
+          int64_t j = l + (int64_t)(warp_incl_scan(c) - c);
+          uint32_t wd = word[u];
+          touched[lane] |= wd;
+          while (wd) {
+            const int bpos = __ffs(wd) - 1;
+            wd &= wd - 1;
+            if (j < h)
+              acc[lane * 32 + bpos] = __fadd_rn(acc[lane * 32 + bpos], a.values[w][j]);
+            ++j;
+          }
+          __syncwarp();
+        }
+      }
+    }
+  }
+  __syncwarp();  // orders this warp's zero stores before the sums below
+  uint32_t tw = touched[lane];
+  while (tw) {
+    const int bpos = __ffs(tw) - 1;
+    tw &= tw - 1;
+    const int slot = lane * 32 + bpos;
+    const int64_t i = t0 + slot;
+    if (G) G[i] = acc[slot];
+    wts[i] = __fsub_rn(wts[i], __fmul_rn(a.eta, acc[slot]));
+  }
+  __syncwarp();
+}
+
+// General apply: one tile per warp at a time (48 tiles in flight per SM).
 template <bool kBitmap>
 __global__ void __launch_bounds__(kAThreads, 6)
 agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
   __shared__ __align__(16) float acc_all[kAWarps][kWT];
   __shared__ uint32_t touched_all[kAWarps][kWT / 32];
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
-  float* acc = acc_all[warp];
-  uint32_t* touched = touched_all[warp];
   const bool g_vec = (reinterpret_cast<uintptr_t>(G) & 15u) == 0;
   const int64_t nw = (int64_t)gridDim.x * kAWarps;
-  for (int64_t t = (int64_t)blockIdx.x * kAWarps + warp; t < a.ntiles; t += nw) {
-    const int64_t t0 = t * kWT;
-    const int tlen = (int)min((int64_t)kWT, a.n - t0);
-    // run bounds of workers `lane` and `lane + 32`
-    uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
-    if ((int)lane < a.W) run_of(a, start, lane, t, &lo0, &hi0);
-    if ((int)lane + 32 < a.W) run_of(a, start, lane + 32, t, &lo1, &hi1);
-    const bool any = __any_sync(kFull, hi0 > lo0 || hi1 > lo1);
-    // The dense tile of G is written as zeros first: those stores depend on
-    // nothing, so they stream while the tile's entries are fetched.  The
-    // touched slots are overwritten with their sums at the end.
-    const bool g_full = G && g_vec && tlen == kWT;
-    if (G) {
-      float* gt = G + t0;
-      if (g_full) {
+  for (int64_t t = (int64_t)blockIdx.x * kAWarps + warp; t < a.ntiles; t += nw)
+    tile_general<kBitmap>(a, start, t, G, wts, g_vec, acc_all[warp], touched_all[warp], lane);
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined apply for the common case: few workers and at most 32 packet
+// entries in a tile, so that lane e holds entry e of the tile (entries in
+// worker-major order).  A warp walks its tiles j = 0, 1, ... and in step j
+// issues the loads of later tiles while it finishes tile j:
+//   int32 packets:  run bounds of tile j+3, entries of tile j+2 (from the
+//                   bounds loaded in the previous step), w at the slots of
+//                   tile j+1 (from the entries loaded in the previous step);
+//   bitmap packets: run bounds and bitmap words of tile j+2, values and w of
+//                   tile j+1;
+// so no step waits on a load issued in the same step.  Finishing tile j
+// stores its zeros, groups the lanes holding the same slot
+// (__match_any_sync: at most one lane per worker, in worker order), and the
+// lowest lane of each group adds the group's values in lane order onto +0
+// and writes G and the SGD update of w.  A tile with more than 32 entries is
+// done by tile_general instead.
+// ---------------------------------------------------------------------------
+
+constexpr int kPipeMaxW = 32;       // int32 packets: one lane per worker's run bounds
+constexpr int kPipeMaxWBitmap = 4;  // bitmap packets: bitmap words of 4 workers per lane
+
+struct Bounds {
+  uint32_t lo, hi;  // run of worker `lane` in the tile (zero for lane >= W)
+};
+
+struct Entry {
+  int32_t ix;    // packet index (int32 stages), then slot in the tile or -1
+  float v;
+  bool fast;     // warp-uniform: the tile has at most 32 entries
+};
+
+__device__ __forceinline__ Bounds pipe_bounds(const AggArgs& a, const uint32_t* start, int64_t t,
+                                              bool valid, unsigned lane) {
+  Bounds b{0u, 0u};
+  if (valid && (int)lane < a.W) run_of(a, start, lane, t, &b.lo, &b.hi);
+  return b;
+}
+
+// Entry `lane` of the tile from the run bounds: its worker is the last w
+// whose list offset is <= lane (a worker with an empty run is never last).
+__device__ __forceinline__ Entry pipe_entries_int32(const AggArgs& a, Bounds b, unsigned lane) {
+  Entry e{0, 0.0f, true};
+  const uint32_t len = min(b.hi - b.lo, 33u);
+  const uint32_t incl = warp_incl_scan(len);
+  const uint32_t E = __shfl_sync(kFull, incl, 31);
+  e.fast = E <= 32u;
+  if (!e.fast) return e;
+  const uint32_t roff = incl - len;
+  int myw = 0;
+  for (int w = 1; w < a.W; ++w)
+    if (__shfl_sync(kFull, roff, w) <= lane) myw = w;
+  const uint32_t ro = __shfl_sync(kFull, roff, myw);
+  const uint32_t lo = __shfl_sync(kFull, b.lo, myw);
+  e.ix = -1;
+  if (lane < E) {
+    const uint32_t j = lo + (lane - ro);
+    e.ix = a.indices[myw][j];
+    e.v = a.values[myw][j];
+  }
+  return e;
+}
+
+// Turns the packet index into a slot of tile t (or -1) and loads w there.
+__device__ __forceinline__ float pipe_w_int32(const AggArgs& a, const float* wts, int64_t t,
+                                              Entry* e) {
+  if (!e->fast) return 0.0f;
+  const int64_t t0 = t * kWT;
+  const int tlen = (int)min((int64_t)kWT, a.n - t0);
+  const int64_t sl = (e->ix < 0) ? -1 : (int64_t)e->ix - t0;
+  e->ix = (sl >= 0 && sl < tlen) ? (int32_t)sl : -1;
+  return e->ix >= 0 ? wts[t0 + e->ix] : 0.0f;
+}
+
+struct BitmapStage {
+  Bounds b;
+  uint32_t word[kPipeMaxWBitmap];  // word `lane` of the tile, per worker
+};
+
+__device__ __forceinline__ BitmapStage pipe_bitmap_load(const AggArgs& a, const uint32_t* start,
+                                                        int64_t t, bool valid, unsigned lane) {
+  BitmapStage s;
+  s.b = pipe_bounds(a, start, t, valid, lane);
+  const int tlen = valid ? (int)min((int64_t)kWT, a.n - t * kWT) : 0;
 #pragma unroll
-        for (int r = 0; r < kWT / 128; ++r)
-          __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, make_float4(0.f, 0.f, 0.f, 0.f));
-      } else {
-        for (int i = lane; i < tlen; i += 32) gt[i] = 0.0f;
-      }
+  for (int w = 0; w < kPipeMaxWBitmap; ++w) {
+    s.word[w] = 0u;
+    if (w < a.W && (int)lane * 32 < tlen) {
+      s.word[w] = __ldg(a.bitmaps[w] + t * (kWT / 32) + lane);
+      const int rem = tlen - (int)lane * 32;
+      if (rem < 32) s.word[w] &= (1u << rem) - 1u;
     }
-    if (!any) continue;
-    float4* acc4 = reinterpret_cast<float4*>(acc);
+  }
+  return s;
+}
+
+// Entry `lane` of the tile from the bitmap words: the r-th set bit of worker
+// w is entry r of its run (bits past the run's length, possible only in a
+// malformed packet, are dropped); then its value and w at its slot.
+__device__ __forceinline__ Entry pipe_bitmap_entries(const AggArgs& a, const float* wts,
+                                                     const BitmapStage& s, int64_t t,
+                                                     uint32_t* lst, unsigned lane, float* wv) {
+  Entry e{-1, 0.0f, true};
+  *wv = 0.0f;
+  const uint32_t len = min(s.b.hi - s.b.lo, 33u);
+  const uint32_t incl = warp_incl_scan(len);
+  const uint32_t E = __shfl_sync(kFull, incl, 31);
+  e.fast = E <= 32u;
+  if (!e.fast) return e;
+  const uint32_t roff = incl - len;
+  lst[lane] = 0xFFFFFFFFu;
+  __syncwarp();
 #pragma unroll
-    for (int r = 0; r < kWT / 128; ++r) acc4[r * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-    touched[lane] = 0;
-    __syncwarp();
-    if (any) {
-      for (int wb = 0; wb < a.W; wb += kPre) {
-        if (!kBitmap) {
-          // the first 32 entries of every worker's run, loaded at once
-          int32_t ix[kPre];
-          float vx[kPre];
-          bool ok[kPre];
-#pragma unroll
-          for (int u = 0; u < kPre; ++u) {
-            const int w = wb + u;
-            const int src = w & 31;
-            const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
-            const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
-            // int32 packets have k <= 2^31, so these sums cannot wrap
-            const uint32_t j = l + lane;
-            ok[u] = w < a.W && j < h;
-            ix[u] = ok[u] ? a.indices[w][j] : 0;
-            vx[u] = ok[u] ? a.values[w][j] : 0.0f;
-          }
-          // added strictly in worker order; a run longer than 32 entries is
-          // finished before the next worker starts
-#pragma unroll
-          for (int u = 0; u < kPre; ++u) {
-            const int w = wb + u;
-            if (w >= a.W) break;  // warp-uniform
-            const int64_t slot = (int64_t)ix[u] - t0;
-            if (ok[u] && slot >= 0 && slot < tlen) {
-              acc[slot] = __fadd_rn(acc[slot], vx[u]);
-              atomicOr(&touched[slot >> 5], 1u << (slot & 31));
-            }
-            __syncwarp();
-            const int src = w & 31;
-            const uint32_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
-            const uint32_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
-            for (uint32_t off = 32; l + off < h; off += 32) {
-              const uint32_t j = l + off + lane;
-              if (j < h) {
-                const int64_t sl = (int64_t)a.indices[w][j] - t0;
-                if (sl >= 0 && sl < tlen) {
-                  acc[sl] = __fadd_rn(acc[sl], a.values[w][j]);
-                  atomicOr(&touched[sl >> 5], 1u << (sl & 31));
-                }
-              }
-              __syncwarp();
-            }
-          }
-        } else {
-          uint32_t word[kPre];
-          const int64_t wi = t0 / 32 + lane;
-#pragma unroll
-          for (int u = 0; u < kPre; ++u) {
-            const int w = wb + u;
-            word[u] = 0;
-            if (w < a.W && (int)lane * 32 < tlen) {
-              word[u] = __ldg(a.bitmaps[w] + wi);
-              const int rem = tlen - (int)lane * 32;
-              if (rem < 32) word[u] &= (1u << rem) - 1u;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < kPre; ++u) {
-            const int w = wb + u;
-            if (w >= a.W) break;  // warp-uniform
-            const int src = w & 31;
-            const int64_t l = __shfl_sync(kFull, w < 32 ? lo0 : lo1, src);
-            const int64_t h = __shfl_sync(kFull, w < 32 ? hi0 : hi1, src);
-            const uint32_t c = __popc(word[u]);
-            int64_t j = l + (int64_t)(warp_incl_scan(c) - c);
-            uint32_t wd = word[u];
-            touched[lane] |= wd;
-            while (wd) {
-              const int bpos = __ffs(wd) - 1;
-              wd &= wd - 1;
-              if (j < h)
-                acc[lane * 32 + bpos] = __fadd_rn(acc[lane * 32 + bpos], a.values[w][j]);
-              ++j;
-            }
-            __syncwarp();
-          }
-        }
-      }
+  for (int w = 0; w < kPipeMaxWBitmap; ++w) {
+    if (w >= a.W) break;  // warp-uniform
+    const uint32_t c = __popc(s.word[w]);
+    uint32_t r = warp_incl_scan(c) - c;
+    const uint32_t base = __shfl_sync(kFull, roff, w), ln = __shfl_sync(kFull, len, w);
+    uint32_t x = s.word[w];
+    while (x) {
+      const int bpos = __ffs(x) - 1;
+      x &= x - 1;
+      if (r < ln) lst[base + r] = (lane * 32u + (uint32_t)bpos) | ((uint32_t)w << 16);
+      ++r;
     }
-    __syncwarp();  // orders this warp's zero stores before the sums below
-    uint32_t tw = touched[lane];
-    while (tw) {
-      const int bpos = __ffs(tw) - 1;
-      tw &= tw - 1;
-      const int slot = lane * 32 + bpos;
-      const int64_t i = t0 + slot;
-      if (G) G[i] = acc[slot];
-      wts[i] = __fsub_rn(wts[i], __fmul_rn(a.eta, acc[slot]));
+  }
+  __syncwarp();
+  const uint32_t code = lst[lane];
+  const bool ok = lane < E && code != 0xFFFFFFFFu;
+  const int myw = ok ? (int)(code >> 16) : 0;
+  const uint32_t ro = __shfl_sync(kFull, roff, myw);
+  const uint32_t lo = __shfl_sync(kFull, s.b.lo, myw);
+  if (ok) {
+    e.ix = (int32_t)(code & 0xFFFFu);
+    e.v = a.values[myw][lo + (lane - ro)];
+    *wv = wts[t * kWT + e.ix];
+  }
+  __syncwarp();
+  return e;
+}
+
+// Finishes a tile whose entries, slots and w values are in the lanes.
+__device__ __forceinline__ void pipe_finish(const AggArgs& a, int64_t t, const Entry& e, float wv,
+                                            float* G, float* wts, bool g_vec, float* vbuf,
+                                            unsigned lane) {
+  const int64_t t0 = t * kWT;
+  const int tlen = (int)min((int64_t)kWT, a.n - t0);
+  if (G) {
+    float* gt = G + t0;
+    if (g_vec && tlen == kWT) {
+#pragma unroll
+      for (int r = 0; r < kWT / 128; ++r)
+        __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, make_float4(0.f, 0.f, 0.f, 0.f));
+    } else {
+      for (int i = lane; i < tlen; i += 32) gt[i] = 0.0f;
     }
-    __syncwarp();
+  }
+  const unsigned grp = __match_any_sync(kFull, e.ix >= 0 ? e.ix : kWT + (int)lane);
+  vbuf[lane] = e.v;
+  __syncwarp();  // also orders every lane's zero stores before the sums below
+  if (e.ix >= 0 && (int)lane == __ffs(grp) - 1) {
+    float sum = __fadd_rn(0.0f, e.v);
+    unsigned m = grp & (grp - 1);
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      sum = __fadd_rn(sum, vbuf[i]);
+    }
+    if (G) G[t0 + e.ix] = sum;
+    wts[t0 + e.ix] = __fsub_rn(wv, __fmul_rn(a.eta, sum));
+  }
+  __syncwarp();
+}
+
+template <bool kBitmap>
+__global__ void __launch_bounds__(kAThreads, 5)
+agg_apply_pipe(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
+  __shared__ __align__(16) float acc_all[kAWarps][kWT];
+  __shared__ uint32_t touched_all[kAWarps][kWT / 32];
+  __shared__ float vbuf_all[kAWarps][32];
+  __shared__ uint32_t lst_all[kAWarps][32];
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const bool g_vec = (reinterpret_cast<uintptr_t>(G) & 15u) == 0;
+  const int64_t first = (int64_t)blockIdx.x * kAWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kAWarps;
+  if (first >= a.ntiles) return;
+  const int64_t cnt = (a.ntiles - 1 - first) / nw + 1;  // tiles of this warp
+  float* vbuf = vbuf_all[warp];
+  auto finish = [&](int64_t j, const Entry& e, float wv) {
+    const int64_t t = first + j * nw;
+    if (e.fast)
+      pipe_finish(a, t, e, wv, G, wts, g_vec, vbuf, lane);
+    else
+      tile_general<kBitmap>(a, start, t, G, wts, g_vec, acc_all[warp], touched_all[warp], lane);
+  };
+  if (!kBitmap) {
+    const Bounds b0 = pipe_bounds(a, start, first, true, lane);
+    Bounds b1 = pipe_bounds(a, start, first + nw, 1 < cnt, lane);
+    Entry e0 = pipe_entries_int32(a, b0, lane);
+    Bounds b2 = pipe_bounds(a, start, first + 2 * nw, 2 < cnt, lane);
+    Entry e1 = pipe_entries_int32(a, b1, lane);
+    float w0 = pipe_w_int32(a, wts, first, &e0);
+    for (int64_t j = 0; j < cnt; ++j) {
+      const Bounds b3 = pipe_bounds(a, start, first + (j + 3) * nw, j + 3 < cnt, lane);
+      const Entry e2 = pipe_entries_int32(a, b2, lane);
+      const float w1 = pipe_w_int32(a, wts, first + (j + 1) * nw, &e1);
+      finish(j, e0, w0);
+      e0 = e1;
+      w0 = w1;
+      e1 = e2;
+      b2 = b3;
+    }
+  } else {
+    uint32_t* lst = lst_all[warp];
+    const BitmapStage s0 = pipe_bitmap_load(a, start, first, true, lane);
+    BitmapStage s1 = pipe_bitmap_load(a, start, first + nw, 1 < cnt, lane);
+    float w0;
+    Entry e0 = pipe_bitmap_entries(a, wts, s0, first, lst, lane, &w0);
+    for (int64_t j = 0; j < cnt; ++j) {
+      const BitmapStage s2 = pipe_bitmap_load(a, start, first + (j + 2) * nw, j + 2 < cnt, lane);
+      float w1;
+      const Entry e1 = pipe_bitmap_entries(a, wts, s1, first + (j + 1) * nw, lst, lane, &w1);
+      finish(j, e0, w0);
+      e0 = e1;
+      w0 = w1;
+      s1 = s2;
+    }
   }
 }
+
 
 int64_t agg_tiles(int64_t n) { return (n + kWT - 1) / kWT; }
 
@@ -432,16 +674,21 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
     err = cudaMemsetAsync(ctl, 0, ctl_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
     const int grid = (int)std::max<int64_t>(
-        1, std::min<int64_t>((int64_t)W * agg_chunks(n), (int64_t)dev.sms * 4));
+        1, std::min<int64_t>((int64_t)W * agg_chunks(n), (int64_t)dev.sms * 5));
     agg_bitmap_starts<<<grid, kAThreads, 0, s>>>(a, start, reinterpret_cast<uint64_t*>(ctl + 256),
                                                  reinterpret_cast<uint32_t*>(ctl), status);
     if ((st = check_launch()) != EF_OK) return st;
   }
+  const bool pipe = bitmap ? W <= kPipeMaxWBitmap : W <= kPipeMaxW;
   const int grid = (int)std::max<int64_t>(
-      1, std::min<int64_t>((nt + kAWarps - 1) / kAWarps, (int64_t)dev.sms * 6));
+      1, std::min<int64_t>((nt + kAWarps - 1) / kAWarps, (int64_t)dev.sms * (pipe ? 5 : 6)));
   prof_begin(EF_KERNEL_SPARSE_APPLY, s);
-  if (bitmap)
+  if (bitmap && pipe)
+    agg_apply_pipe<true><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+  else if (bitmap)
     agg_apply<true><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+  else if (pipe)
+    agg_apply_pipe<false><<<grid, kAThreads, 0, s>>>(a, start, G, w);
   else
     agg_apply<false><<<grid, kAThreads, 0, s>>>(a, start, G, w);
   if ((st = check_launch()) != EF_OK) return st;

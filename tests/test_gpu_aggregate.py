@@ -70,6 +70,40 @@ def test_aggregate_random(fmt, W, n):
     assert_bits_equal(w2, w_want, "w with G = NULL")
 
 
+@pytest.mark.parametrize("fmt", [efg.IDX_INT32, efg.IDX_BITMAP])
+def test_aggregate_sparse_and_dense_tiles_mixed(fmt):
+    """Warp tiles of several 1024-element sub-tiles (n > 2^25): most hold a
+    few entries and are summed from a shared list; a region where worker 2
+    sends every index is summed sub-tile by sub-tile; the ragged tail ends
+    mid-tile."""
+    n = (1 << 25) + 12_345
+    pk = _packets(n, 4, 0.001, seed=77)
+    rng = np.random.default_rng(78)
+    idx = np.unique(np.concatenate([pk[2]["indices"], np.arange(5_000_000, 5_100_000)]))
+    pk[2] = {"indices": idx.astype(np.int32),
+             "values": (rng.standard_t(3, idx.size) * 1e-3).astype(np.float32)}
+    G, w, w0, ws = _run(pk, n, 0.05, fmt)
+    G_want = oracle.sparse_aggregate(pk, n)
+    assert efg.workspace_status(ws) == 0
+    assert_bits_equal(G, G_want, "G")
+    assert_bits_equal(w, oracle.sgd_apply(w0, G_want, 0.05), "w")
+
+
+@pytest.mark.parametrize("fmt", [efg.IDX_INT32, efg.IDX_BITMAP])
+@pytest.mark.parametrize("density", [0.0005, 0.01])
+def test_aggregate_sixty_four_workers(fmt, density):
+    """The largest worker count, with overlapping packets: sparse tiles go
+    through the list (owner lane + binary search in 63 other runs), denser
+    ones through the shared dense copy."""
+    n = 300_001
+    pk = _packets(n, 64, density, seed=int(density * 1e5))
+    G, w, w0, ws = _run(pk, n, 0.1, fmt)
+    G_want = oracle.sparse_aggregate(pk, n)
+    assert efg.workspace_status(ws) == 0
+    assert_bits_equal(G, G_want, "G")
+    assert_bits_equal(w, oracle.sgd_apply(w0, G_want, 0.1), "w")
+
+
 def test_aggregate_golden_examples():
     fx = json.load(open(os.path.join(GOLDEN, "aggregate_examples.json")))
     for ex in fx["examples"]:

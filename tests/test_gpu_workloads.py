@@ -186,11 +186,13 @@ def test_slab_2p31_sign_receive_sampled():
     assert_bits_equal(wt[pt], oracle.sgd_apply(w_s, G_want, w.eta), "w (sampled)")
 
 
-def test_slab_2p31_receive_side_four_workers():
+@pytest.mark.parametrize("fmt", [efg.IDX_INT32, efg.IDX_BITMAP])
+def test_slab_2p31_receive_side_four_workers(fmt):
     """W = 4 packets of 2,147,484 entries each (drawn by the input generator:
     sorted random positions, Student-t values, overlapping between workers),
-    summed into a dense G over 2^31 elements and applied with SGD; G and w
-    are compared at every touched position and at random untouched ones."""
+    as indices or as bitmaps, summed into a dense G over 2^31 elements and
+    applied with SGD; G and w are compared at every touched position and at
+    random untouched ones."""
     w = wl.workload("slab_2p31")
     n, k = w.n, w.total_k
     rng = np.random.default_rng(11)
@@ -206,9 +208,18 @@ def test_slab_2p31_receive_side_four_workers():
     probe = np.unique(np.concatenate([touched, untouched, [0, n - 1]]))
     pt = torch.from_numpy(probe).to(DEV)
     w_probe = host(wt[pt])
-    gpu_pk = [{"indices": torch.from_numpy(p["indices"]).to(DEV),
-               "values": torch.from_numpy(p["values"]).to(DEV)} for p in packets]
-    G = _apply(gpu_pk, [p["values"].size for p in packets], n, w.eta, wt)
+    gpu_pk = []
+    for p in packets:
+        q = {"values": torch.from_numpy(p["values"]).to(DEV)}
+        if fmt == efg.IDX_INT32:
+            q["indices"] = torch.from_numpy(p["indices"]).to(DEV)
+        else:   # element i -> bit i % 32 of word i // 32
+            words = np.zeros((n + 31) // 32, np.uint32)
+            ix = p["indices"].astype(np.int64)
+            np.bitwise_or.at(words, ix >> 5, np.left_shift(1, ix & 31).astype(np.uint32))
+            q["bitmap"] = torch.from_numpy(words.view(np.int32)).to(DEV)
+        gpu_pk.append(q)
+    G = _apply(gpu_pk, [p["values"].size for p in packets], n, w.eta, wt, fmt)
     # oracle on the probed positions only: restrict every packet to them
     pos_in_probe = [np.searchsorted(probe, p["indices"]) for p in packets]
     sub = [{"indices": pi.astype(np.int32), "values": p["values"]}
