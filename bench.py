@@ -529,7 +529,7 @@ def run_e2e(args, s):
 
     if args.e2e_mode == "serial":
         run = run_serial        # noqa: F811
-    run(1)
+    run(2)
     torch.cuda.synchronize()
     barrier()
     a = torch.cuda.Event(enable_timing=True)
@@ -663,7 +663,7 @@ def main(argv=None):
     p.add_argument("--n", type=int, default=1 << 31, help="elements per worker")
     p.add_argument("--workers", type=int, default=4)
     p.add_argument("--prof-steps", type=int, default=2)
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--e2e-mode", choices=["pipelined", "serial"], default="pipelined",
                    help="pipelined: uploads double-buffered against compute on their own "
                         "streams; serial: upload, step, download in turn")

@@ -29,6 +29,8 @@
 //      Writes values, int32 indices or bitmap bits, and e = +0 there.
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -61,6 +63,7 @@ constexpr int kSelSmall = 32768;  // lists up to this length are selected by one
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
 static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
+static_assert(kChunk % kSelThreads == 0, "select layout");
 
 struct SmallSeg {
   int64_t off;
@@ -113,6 +116,71 @@ struct IO {
   uint32_t* out_bitmap;
   int32_t* status;
 };
+
+// Shared scratch of lookback_block.
+struct LookbackShared {
+  int first_incl[32];  // per warp: lowest thread index seeing an inclusive state
+  uint64_t part[32];   // per warp: partial sums
+};
+
+// Block-wide form of the bounded decoupled look-back (same flags, payloads,
+// wait limits and error report as lookback_warp): in each round thread i
+// reads the state of predecessor base - i, so one round trip covers
+// blockDim.x predecessors instead of 32.  Called by every thread of the CTA;
+// every thread gets the exclusive prefix.  blockDim.x is a multiple of 32.
+__device__ uint64_t lookback_block(uint64_t* states, int64_t tile, int64_t first, uint64_t agg,
+                                   int32_t* status, LookbackShared& sh) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const unsigned lane = lane_id();
+  const int wid = tid >> 5, nwarps = nthr >> 5;
+  if (tile == first) {
+    if (tid == 0) st_release(&states[tile], kFlagIncl | agg);
+    return 0;
+  }
+  if (tid == 0) st_release(&states[tile], kFlagAgg | agg);
+  uint64_t excl = 0;
+  int64_t base = tile - 1;
+  const uint64_t t0 = global_ns();
+  while (base >= first) {
+    const int64_t t = base - tid;
+    uint64_t s = (t >= first) ? ld_acquire(&states[t]) : kFlagIncl;
+    uint32_t spins = 0;
+    bool gave_up = false;
+    while (__syncthreads_or((s >> 62) == 0)) {
+      if ((s >> 62) == 0) s = ld_acquire(&states[t]);
+      if ((++spins & 63u) == 0) {  // spins is uniform across the CTA
+        int bad = 0;
+        if (tid == 0)
+          bad = (global_ns() - t0 > kWaitLimitNs) || (ld_volatile(status) != 0) ||
+                spins > (1u << 26);
+        if (__syncthreads_or(bad)) {
+          if (tid == 0) set_status(status, EF_ERR_DEVICE_TIMEOUT);
+          gave_up = true;
+          break;
+        }
+      }
+      __nanosleep(32);
+    }
+    if (gave_up) break;
+    // the nearest inclusive predecessor of this round: the lowest thread
+    // index whose state is inclusive (predecessors before `first` count as
+    // inclusive zeros)
+    const unsigned incl = __ballot_sync(kFull, (s >> 62) == 2);
+    if (lane == 0) sh.first_incl[wid] = incl ? wid * 32 + __ffs(incl) - 1 : INT_MAX;
+    __syncthreads();
+    int stop = INT_MAX;
+    for (int w = 0; w < nwarps; ++w) stop = min(stop, sh.first_incl[w]);
+    const uint64_t ws = warp_sum_u64(tid <= stop ? (s & kPayloadMask) : 0ull);
+    if (lane == 0) sh.part[wid] = ws;
+    __syncthreads();
+    for (int w = 0; w < nwarps; ++w) excl += sh.part[w];
+    __syncthreads();  // the scratch is reused by the next round
+    if (stop != INT_MAX) break;
+    base -= nthr;
+  }
+  if (tid == 0) st_release(&states[tile], kFlagIncl | ((excl + agg) & kPayloadMask));
+  return excl;
+}
 
 // Writes packet entry `pos` (must lie below `limit`, the segment's packet end;
 // anything else would be a library defect and is recorded, not written).
@@ -556,35 +624,62 @@ topk_select_small(IO io, SegState* st, const uint2* cand) {
 // Longer lists: one digit pass over the chunks of every unresolved list.
 // Each CTA builds a shared-memory histogram of a chunk and
 // merges it into its segment's global histogram; the CTA that merges a
-// segment's last chunk fixes that digit for the segment.
+// segment's last chunk fixes that digit for the segment.  The segments'
+// list descriptors and digit prefixes are read once per CTA (they do not
+// change during a pass: a segment's prefix is extended only after all of
+// its chunks are counted), and a chunk's keys are loaded all at once.
 __global__ void __launch_bounds__(kSelThreads)
 topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, Ctl* ctl,
             int pass) {
+  constexpr int kPer = kChunk / kSelThreads;  // keys per thread per chunk
   __shared__ uint32_t sh[2048];
   __shared__ int64_t s_cb[kMaxLarge + 1];
+  __shared__ ListRef s_list[kMaxLarge];
+  __shared__ uint32_t s_prefix[kMaxLarge];
+  __shared__ uint32_t s_resolved[kMaxLarge];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
   const int shift = pass == 0 ? 20 : (pass == 1 ? 10 : 0);
   const int nb = pass == 0 ? 2048 : 1024;
   const int hi = shift + (pass == 0 ? 11 : 10);
   const int64_t total = *reinterpret_cast<volatile int64_t*>(&ctl->total_chunks);
-  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_cb[i] = st[i].chunk_base;
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) {
+    s_cb[i] = st[i].chunk_base;
+    s_list[i] = list_ref(st, i);
+    s_prefix[i] = st[i].prefix;
+    s_resolved[i] = st[i].resolved;
+  }
   if (threadIdx.x == 0) s_cb[nseg] = total;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) sh[b] = 0;
   __syncthreads();
   for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
     const int seg = find_seg(s_cb, nseg, c);
-    if (st[seg].resolved) continue;  // uniform across the CTA
-    const ListRef l = list_ref(st, seg);
-    const uint32_t prefix = st[seg].prefix;
+    if (s_resolved[seg]) continue;  // uniform across the CTA
+    const ListRef l = s_list[seg];
+    const uint32_t prefix = s_prefix[seg];
     const int64_t j0 = (c - s_cb[seg]) * kChunk;
     const int64_t j1 = min(j0 + (int64_t)kChunk, l.len);
-    const uint2* cl = cand + l.cand_base;
-    const float* el = io.e + l.off;
-    for (int64_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-      const uint32_t bits = l.mode == 0 ? cl[j].y : __float_as_uint(el[j]);
-      const uint32_t key = bits & 0x7FFFFFFFu;
-      if (hi >= 31 || (key >> hi) == (prefix >> hi))
+    uint32_t bits[kPer];
+    if (l.mode == 0) {
+      const uint2* cl = cand + l.cand_base;
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int64_t j = j0 + r * kSelThreads + threadIdx.x;
+        bits[r] = j < j1 ? cl[j].y : 0u;
+      }
+    } else {
+      const float* el = io.e + l.off;
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int64_t j = j0 + r * kSelThreads + threadIdx.x;
+        bits[r] = j < j1 ? __float_as_uint(el[j]) : 0u;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int64_t j = j0 + r * kSelThreads + threadIdx.x;
+      const uint32_t key = bits[r] & 0x7FFFFFFFu;
+      if (j < j1 && (hi >= 31 || (key >> hi) == (prefix >> hi)))
         atomicAdd(&sh[(key >> shift) & (nb - 1)], 1u);
     }
     __syncthreads();
@@ -628,9 +723,9 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
   __shared__ int64_t s_cb[kMaxLarge + 1];
   __shared__ uint32_t s_wgt[kEmitThreads / 32], s_wlt[kEmitThreads / 32];
   __shared__ uint32_t s_ogt[kEmitThreads / 32], s_olt[kEmitThreads / 32];
-  __shared__ uint32_t s_weq[kEmitThreads / 32];
   __shared__ int64_t s_c;
-  __shared__ uint64_t s_excl;
+  __shared__ uint64_t s_agg;
+  __shared__ LookbackShared s_lb;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   const int64_t total = *reinterpret_cast<volatile int64_t*>(&ctl->total_chunks);
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_cb[i] = st[i].chunk_base;
@@ -690,7 +785,6 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
     if (lane == 0) {
       s_wgt[warp] = cg;
       s_wlt[warp] = cl;
-      s_weq[warp] = ce;
     }
     __syncthreads();
     if (warp == 0) {
@@ -703,13 +797,13 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
       }
       const uint64_t agg = ((uint64_t)__shfl_sync(kFull, ia, 31) << 31) |
                            (uint64_t)__shfl_sync(kFull, ib, 31);
-      const uint64_t excl = lookback_warp(cstate, c, s_cb[seg], agg, io.status);
-      if (lane == 0) s_excl = excl;
+      if (lane == 0) s_agg = agg;
     }
     __syncthreads();
+    const uint64_t excl = lookback_block(cstate, c, s_cb[seg], s_agg, io.status, s_lb);
     if (cg | ce) {  // warp-uniform
-      int64_t run_gt = (int64_t)(s_excl >> 31) + s_ogt[warp];
-      int64_t run_lt = (int64_t)(s_excl & 0x7FFFFFFFu) + s_olt[warp];
+      int64_t run_gt = (int64_t)(excl >> 31) + s_ogt[warp];
+      int64_t run_lt = (int64_t)(excl & 0x7FFFFFFFu) + s_olt[warp];
       const unsigned lm = lanemask_lt();
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
@@ -974,7 +1068,7 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     topk_select_small<<<nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s>>>(io, sst,
                                                                                       cand);
     if ((st = check_launch()) != EF_OK) return st;
-    const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 2));
+    const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 3));
     for (int pass = 0; pass < 3; ++pass) {
       topk_select<<<sgrid, kSelThreads, 0, s>>>(io, sst, nsg, cand, ghist, ctl, pass);
       if ((st = check_launch()) != EF_OK) return st;
