@@ -42,26 +42,36 @@ UNIT = "G grad elements/s"
 # DRAM traffic of one topk_fused launch from one ncu capture (--set full,
 # slab workload at n = 2^26 per worker, see profiles/): 536.97 MB read +
 # 220.88 MB written = 11.293 bytes per element.  Reported, scaled by n, only
-# while the kernel sources still hash to what was captured; otherwise null.
-# (Reads scale with n exactly; the writes fall short of 12 B by the dirty
-# lines still in L2 when the captured launch ends.)
+# while the captured code still hashes to what was captured (the kernel's
+# region of ef_topk.cu, from its staging struct to the end of the kernel, and
+# the shared device header); otherwise null.  (Reads scale with n exactly;
+# the writes fall short of 12 B by the dirty lines still in L2 when the
+# captured launch ends.)
 FUSED_TRAFFIC_PER_ELEMENT = 11.293
 FUSED_TRAFFIC_SOURCES = {
-    "error_feedback_gradient_gb300/csrc/ef_topk.cu":
-        "fed6dec6edd10a05e06608d206fe30fbfab01b74f1e199147a4ebd52a5686a01",
-    "error_feedback_gradient_gb300/csrc/ef_common.cuh":
+    # (file, first marker, end marker or None for the whole file): sha256
+    ("error_feedback_gradient_gb300/csrc/ef_topk.cu", "struct FusedStage {",
+     "// A segment's select list:"):
+        "36c3ecac2bb5855c1ffc576df5b36989327df45ee747a8fb657a12d0dbe33d1f",
+    ("error_feedback_gradient_gb300/csrc/ef_common.cuh", None, None):
         "8c82518cf4425bdd6f8024b355289fa0e638002f3e8476314350ba0271a997c1",
 }
 
 
 def fused_traffic(n: int):
     import hashlib
-    for rel, digest in FUSED_TRAFFIC_SOURCES.items():
+    for (rel, first, end), digest in FUSED_TRAFFIC_SOURCES.items():
         try:
             with open(os.path.join(ROOT, rel), "rb") as f:
-                if hashlib.sha256(f.read()).hexdigest() != digest:
-                    return None
+                src = f.read()
         except OSError:
+            return None
+        if first is not None:
+            a, b = src.find(first.encode()), src.find(end.encode())
+            if a < 0 or b < a:
+                return None
+            src = src[a:b]
+        if hashlib.sha256(src).hexdigest() != digest:
             return None
     return FUSED_TRAFFIC_PER_ELEMENT * n
 
