@@ -24,6 +24,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;       // 128-element groups in flight per warp (sender)
+constexpr int kSpan = 32;        // 128-element groups in a warp's span on large inputs
+static_assert(kSpan % kUnroll == 0, "span layout");
 constexpr int kApplyUnroll = 2;  // float4 chunks in flight per thread (receiver)
 
 __device__ __forceinline__ float sign_step(float g, float e, float b1, float c, bool* bit) {
@@ -38,6 +40,7 @@ __device__ __forceinline__ float sign_step(float g, float e, float b1, float c, 
 // Groups of 128 elements [0, ngroups): lane l of a warp owns elements
 // 4l..4l+3 of a group, so a group's four bit words are built from 8-lane
 // nibble sets.  g and eps must be 16-byte aligned.
+template <int kSpanT>
 __global__ void __launch_bounds__(kThreads)
 sign_compress_vec(const float* __restrict__ g, float* __restrict__ eps,
                   uint32_t* __restrict__ bits, int64_t ngroups, float b1, float c,
@@ -45,7 +48,15 @@ sign_compress_vec(const float* __restrict__ g, float* __restrict__ eps,
   const unsigned lane = lane_id();
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t g0 = warp * kUnroll; g0 < ngroups; g0 += nwarps * kUnroll) {
+  // Each warp streams a contiguous span of kSpanT groups (a multiple of
+  // kUnroll; 16 KB of g and of eps on large inputs), kUnroll groups at a
+  // time; spans are dealt to warps round-robin.  The span length is a
+  // compile-time constant so that the compiler can unroll it and issue the
+  // next groups' loads early.
+  for (int64_t s0 = warp * kSpanT; s0 < ngroups; s0 += nwarps * kSpanT)
+#pragma unroll
+  for (int64_t g0 = s0; g0 < s0 + kSpanT; g0 += kUnroll) {
+    if (g0 >= ngroups) break;  // warp-uniform
     float4 gv[kUnroll], ev[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -219,9 +230,17 @@ extern "C" ef_status ef_sign_compress(const float* g, float* eps, int64_t n, flo
   if (aligned16(g) && aligned16(eps)) {
     const int64_t ngroups = n / 128;
     if (ngroups > 0) {
-      const int grid = grid_for(ngroups, warps_per_block * kUnroll, dev.sms, 8);
-      sign_compress_vec<<<grid, kThreads, 0, s>>>(g, eps, out_bits, ngroups, b1, c,
-                                                  aligned16(out_bits));
+      // long spans only once every resident warp gets at least two of them
+      const int64_t resident_warps = (int64_t)dev.sms * 8 * warps_per_block;
+      if (ngroups >= 2 * resident_warps * kSpan) {
+        const int grid = grid_for(ngroups, warps_per_block * kSpan, dev.sms, 8);
+        sign_compress_vec<kSpan><<<grid, kThreads, 0, s>>>(g, eps, out_bits, ngroups, b1, c,
+                                                           aligned16(out_bits));
+      } else {
+        const int grid = grid_for(ngroups, warps_per_block * kUnroll, dev.sms, 8);
+        sign_compress_vec<kUnroll><<<grid, kThreads, 0, s>>>(g, eps, out_bits, ngroups, b1, c,
+                                                             aligned16(out_bits));
+      }
       if ((st = check_launch()) != EF_OK) return st;
     }
     w_begin = ngroups * 4;

@@ -31,6 +31,14 @@ def test_sign_sizes(n):
     _sign_step(wl.normal(n, 1e-3, n, DEV), wl.normal(n, 1e-3, n + 1, DEV))
 
 
+def test_sign_long_spans_with_ragged_tail():
+    """Above about 80 M elements each warp streams contiguous 4096-element
+    spans; 2^27 + 37 elements end in a partial span, a partial 128-element
+    group and a partial bit word."""
+    n = (1 << 27) + 37
+    _sign_step(wl.normal(n, 1e-3, 71, DEV), wl.normal(n, 1e-3, 72, DEV))
+
+
 def test_sign_unaligned_and_special():
     n = 100_003
     gb = wl.normal(n + 4, 1e-3, 1, DEV)
