@@ -7,15 +7,21 @@
 // the whole segment in shared memory (compensate, 3-digit radix select,
 // ordered emit).  Longer segments take the streaming path, batched over all
 // such segments of a call:
-//   1. prepare  (one CTA per segment): sample 32768 compensated keys and take
-//      a conservative lower threshold T_lo from them (only a speed-up: the
-//      result never depends on it).
-//   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e;
-//      every key >= T_lo is appended, in index order, to a per-segment
-//      candidate list via warp ballots and a bounded decoupled look-back.
-//      The last CTA checks each list: between k and its capacity -> select
-//      on the list; otherwise (T_lo too high or overflow) -> select on the
-//      whole segment, which is always correct, only slower.
+//   1. sample + prepare (32 CTAs per segment each): up to 4096 blocks of 64
+//      contiguous elements (at most 1/16 of the segment) are compensated,
+//      and two histogram passes over their keys (top 11 bits, then the next
+//      10 inside the chosen bin) give a conservative lower threshold T_lo:
+//      the lower edge of the 21-bit bin holding the rank-th largest sampled
+//      key.  Only a speed-up: the result never depends on it.
+//   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e,
+//      except that a key >= T_lo is written as +0 and appended, in index
+//      order, to a per-segment candidate list (warp ballots and a bounded
+//      decoupled look-back).  A candidate that finds no room in a staging
+//      buffer or the list keeps g in e.  The last CTA checks each list:
+//      between k and its capacity -> select on the list; otherwise (T_lo too
+//      high or overflow) -> select on the whole segment, which is always
+//      correct, only slower; `restore` then first puts g back at the listed
+//      candidates.
 //   3. select   (x3): radix select on 11/10/10-bit digits of the keys of
 //      each list, shared-memory histograms merged into one per segment; the
 //      last CTA of each pass fixes that digit.  Result: the k-th key T and
@@ -26,7 +32,10 @@
 //      The look-back carries (#gt, #lt) prefixes: both stay below 2^31 for a
 //      list of up to 2^31 entries (T itself is in the list), and the equal
 //      count follows from the list position j as j - gt - lt.
-//      Writes values, int32 indices or bitmap bits, and e = +0 there.
+//      Writes values, int32 indices or bitmap bits.  On a candidate list e
+//      already holds +0 at every candidate, so emit writes g back at the
+//      candidates not taken (with a tight T_lo far fewer than k scattered
+//      writes); on a whole-segment list it writes e = +0 at the taken ones.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -51,14 +60,15 @@ constexpr int kFusedThreads = kStreamThreads + 32;  // + one scan warp
 constexpr int kStageCap = 256;                  // staged candidates per warp per buffer
 constexpr int kBatch = 4;                       // 128-element rounds loaded at once
 constexpr int kFusedCtasPerSm = 4;
-constexpr int kSample = 32768;
-constexpr int kPrepThreads = 1024;
+constexpr int kSampleBlock = 64;         // contiguous elements per sample block
+constexpr int kSampleBlocksMax = 4096;  // sample blocks per segment (262 144 keys)
 constexpr int kChunk = 4096;  // list entries per select / emit chunk
 constexpr int kSelThreads = 512;
 constexpr int kEmitThreads = 256;  // 8 warps x 16 rounds x 32 lanes = kChunk
 constexpr int kMaxLarge = 128;     // segments per streaming batch
 constexpr int kMaxSmall = 512;     // segments per small-path launch
 constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
+constexpr uint32_t kNoEntry = 0xFFFFFFFFu;      // candidate-list slot of an unstaged candidate
 constexpr int kSelSmall = 32768;  // lists up to this length are selected by one CTA
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
@@ -81,7 +91,7 @@ struct LargeSeg {
   int64_t cand_base, cap;
   int64_t tile_base;  // global id of the segment's first fused tile
   int64_t q_first;    // index of that tile in aligned kTile units
-  int64_t rank;       // sample rank for T_lo (0: no candidates, > kSample: all)
+  int64_t rank;       // sample rank for T_lo (0: no candidates, > samples: all)
 };
 
 struct LargeBatch {
@@ -100,7 +110,31 @@ struct SegState {
   uint32_t overflow;  // a warp's staging area overflowed: the list is incomplete
   uint32_t resolved;  // T and need already found (list fitted in one CTA)
   uint32_t chunks_done[3];  // chunks of the list histogrammed per digit pass
+  int64_t cand_count;       // candidates found by the fused pass (-1: unknown)
 };
+
+// Per-segment state of the two sampling passes (in the cleared control area).
+struct SampleState {
+  uint32_t done[2];  // CTAs finished in the first / second pass
+  uint32_t b0;       // top-11-bit bin holding the rank-th largest sampled key
+  uint32_t r1;       // that key's rank inside the bin
+};
+
+// Sample blocks of a segment of `len` elements (> kSmallMax): at most 1/16
+// of the segment, at most kSampleBlocksMax.
+__host__ __device__ __forceinline__ int64_t sample_blocks(int64_t len) {
+  const int64_t b = len / (16 * kSampleBlock);
+  return b < kSampleBlocksMax ? b : kSampleBlocksMax;
+}
+
+// First element of sample block `b` of `nblk`: the blocks are centred on
+// evenly spaced points and do not overlap (spacing >= 16 blocks).
+__host__ __device__ __forceinline__ int64_t sample_block_start(int64_t len, int64_t nblk,
+                                                             int64_t b) {
+  int64_t p = ((2 * b + 1) * len) / (2 * nblk) - kSampleBlock / 2;
+  p = p < 0 ? 0 : p;
+  return p > len - kSampleBlock ? len - kSampleBlock : p;
+}
 
 struct alignas(256) Ctl {
   uint32_t fused_ticket, fused_done;
@@ -183,9 +217,10 @@ __device__ uint64_t lookback_block(uint64_t* states, int64_t tile, int64_t first
 }
 
 // Writes packet entry `pos` (must lie below `limit`, the segment's packet end;
-// anything else would be a library defect and is recorded, not written).
+// anything else would be a library defect and is recorded, not written), and
+// e = +0 at the element unless it already holds +0 (zero_e false).
 __device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t pos, int64_t limit,
-                                         float v) {
+                                         float v, bool zero_e) {
   if (pos >= limit) {
     set_status(io.status, EF_ERR_INTERNAL);
     return;
@@ -193,7 +228,7 @@ __device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t pos
   io.out_values[pos] = v;
   if (io.out_indices) io.out_indices[pos] = (int32_t)gidx;
   if (io.out_bitmap) atomicOr(io.out_bitmap + (gidx >> 5), 1u << (gidx & 31));
-  io.e[gidx] = 0.0f;
+  if (zero_e) io.e[gidx] = 0.0f;
 }
 
 // ---------------------------------------------------------------------------
@@ -266,7 +301,7 @@ topk_small(SmallBatch b, IO io, int keys_words) {
     const uint32_t eq_before = run_eq + __popc(bq & lm);
     if (gt || (eq && eq_before < r.need)) {
       const int64_t pos = sg.out_off + gt_before + min(eq_before, r.need);
-      emit_one(io, sg.off + i, pos, sg.out_off + sg.k, __uint_as_float(bits));
+      emit_one(io, sg.off + i, pos, sg.out_off + sg.k, __uint_as_float(bits), true);
     }
     run_gt += __popc(bg);
     run_eq += __popc(bq);
@@ -277,77 +312,164 @@ topk_small(SmallBatch b, IO io, int keys_words) {
 // streaming path
 // ---------------------------------------------------------------------------
 
-constexpr int kSampleCtas = 32;      // CTAs gathering one segment's samples
-constexpr int kSampleThreads = 256;  // kSample / kSampleCtas / kSampleThreads per thread
+constexpr int kSampleCtasMax = 128;  // CTAs per segment in each sampling pass, at most
+constexpr int kSampleThreads = 256;
+constexpr int kSampleUnroll = 4;     // sample blocks per warp in flight
 
-// Gathers the compensated keys at the sample positions of every streaming
-// segment: sample j of a segment sits at off + floor((2j + 1) * len /
-// (2 * kSample)).  Spread over kSampleCtas CTAs per segment so that the
-// scattered reads use many SMs; eight samples' loads per thread are issued
-// before any is used.
-__global__ void __launch_bounds__(kSampleThreads)
-topk_sample(LargeBatch b, IO io, uint32_t* samples) {
-  static_assert((kSample & (kSample - 1)) == 0, "sample count must be a power of two");
-  constexpr int kShift = __builtin_ctz(2 * kSample);
-  constexpr int kPer = kSample / (kSampleCtas * kSampleThreads);
-  static_assert(kPer == 4, "sampling layout");
-  const int s = blockIdx.x / kSampleCtas;
-  const LargeSeg& d = b.seg[s];
-  if (d.rank <= 0 || d.rank > kSample) return;
-  const int64_t j0 = (int64_t)(blockIdx.x % kSampleCtas) * kSampleThreads * kPer + threadIdx.x;
-  float gv[kPer], ev[kPer];
+// Compensated keys of sample blocks `bi` .. of this warp: lane l holds
+// elements l and l + 32 of each block.
+__device__ __forceinline__ void sample_keys(const IO& io, const LargeSeg& d, int64_t nblk,
+                                            int64_t b0, int64_t stride, unsigned lane,
+                                            uint32_t (&key)[kSampleUnroll][2],
+                                            bool (&ok)[kSampleUnroll]) {
+  float gv[kSampleUnroll][2], ev[kSampleUnroll][2];
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int64_t j = j0 + (int64_t)u * kSampleThreads;
-    const int64_t p = d.off + (((2 * j + 1) * d.len) >> kShift);
-    gv[u] = io.g_raw[p];
-    ev[u] = io.e[p];
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    const int64_t bi = b0 + u * stride;
+    ok[u] = bi < nblk;
+    if (ok[u]) {
+      const int64_t p = d.off + sample_block_start(d.len, nblk, bi) + lane;
+      gv[u][0] = io.g_raw[p];
+      gv[u][1] = io.g_raw[p + 32];
+      ev[u][0] = io.e[p];
+      ev[u][1] = io.e[p + 32];
+    }
   }
-  uint32_t* out = samples + (int64_t)s * kSample;
 #pragma unroll
-  for (int u = 0; u < kPer; ++u)
-    out[j0 + (int64_t)u * kSampleThreads] = abs_key(__fadd_rn(gv[u], ev[u]));
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    key[u][0] = ok[u] ? abs_key(__fadd_rn(gv[u][0], ev[u][0])) : 0u;
+    key[u][1] = ok[u] ? abs_key(__fadd_rn(gv[u][1], ev[u][1])) : 0u;
+  }
 }
 
-// One CTA per streaming segment: T_lo = the rank-th largest sampled key, a
-// conservative lower threshold for the candidate list (a speed-up only; the
-// result never depends on it), and the segment's state for the later passes.
-__global__ void __launch_bounds__(kPrepThreads)
-topk_prepare(LargeBatch b, int nseg, const uint32_t* samples, SegState* st) {
-  extern __shared__ uint32_t sm[];
-  uint32_t* keys = sm;
-  uint32_t* hist = sm + kSample;
-  uint32_t* scratch = hist + 2048;
-  const int s = blockIdx.x;
-  if (s >= nseg) return;
-  const LargeSeg d = b.seg[s];
-  uint32_t t_lo;
-  if (d.rank <= 0) {
-    t_lo = kNoCandidate;
-  } else if (d.rank > kSample) {
-    t_lo = 0;
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(samples + (int64_t)s * kSample);
-    uint4* dst = reinterpret_cast<uint4*>(keys);
-    for (int j = threadIdx.x; j < kSample / 4; j += blockDim.x) dst[j] = src[j];
-    __syncthreads();
-    t_lo = block_radix_select(keys, kSample, (uint32_t)d.rank, hist, scratch).T;
+// Whether the segment samples at all (rank 0: no candidates; rank above the
+// sample count: every element is a candidate).
+__device__ __forceinline__ bool samples_needed(const LargeSeg& d, int64_t nblk) {
+  return d.rank > 0 && d.rank <= nblk * kSampleBlock;
+}
+
+// Sampling pass 1: histogram of the top 11 key bits over all sample blocks
+// of each streaming segment (`ctas` CTAs per segment, merged in global
+// memory); the CTA that merges last finds the bin b0 holding the rank-th
+// largest sampled key and the rank r1 left inside it.
+__global__ void __launch_bounds__(kSampleThreads)
+topk_sample(LargeBatch b, IO io, uint32_t* hist0, SampleState* ss, int ctas) {
+  __shared__ uint32_t sh[2048];
+  __shared__ uint32_t scratch[64];
+  __shared__ int s_last;
+  const int s = blockIdx.x / ctas, q = blockIdx.x % ctas;
+  const LargeSeg& d = b.seg[s];
+  const int64_t nblk = sample_blocks(d.len);
+  if (!samples_needed(d, nblk)) return;  // uniform across the CTA
+  const unsigned lane = lane_id();
+  const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
+  const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  for (int64_t b0 = gw; b0 < nblk; b0 += kWarps * kSampleUnroll) {
+    uint32_t key[kSampleUnroll][2];
+    bool ok[kSampleUnroll];
+    sample_keys(io, d, nblk, b0, kWarps, lane, key, ok);
+#pragma unroll
+    for (int u = 0; u < kSampleUnroll; ++u) {
+      if (ok[u]) {
+        atomicAdd(&sh[key[u][0] >> 20], 1u);
+        atomicAdd(&sh[key[u][1] >> 20], 1u);
+      }
+    }
   }
+  __syncthreads();
+  uint32_t* gh = hist0 + (int64_t)s * 2048;
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+  __syncthreads();
   if (threadIdx.x == 0) {
-    SegState v;
-    v.d = d;
-    v.t_lo = t_lo;
-    v.mode = 0;
-    v.list_len = 0;
-    v.chunk_base = 0;
-    v.prefix = 0;
-    v.krem = (uint32_t)d.k;
-    v.gt = 0;
-    v.overflow = 0;
-    v.resolved = 0;
-    v.chunks_done[0] = v.chunks_done[1] = v.chunks_done[2] = 0;
-    st[s] = v;
+    __threadfence();
+    s_last = atomicAdd(&ss[s].done[0], 1u) == (uint32_t)ctas - 1;
   }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
+    sh[i] = *reinterpret_cast<volatile uint32_t*>(&gh[i]);
+  __syncthreads();
+  uint32_t bin, above;
+  block_find_bin(sh, 2048, (uint32_t)d.rank, scratch, &bin, &above);
+  if (threadIdx.x == 0) {
+    ss[s].b0 = bin;
+    ss[s].r1 = (uint32_t)d.rank - above;
+  }
+}
+
+__device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& d, uint32_t t_lo) {
+  SegState v;
+  v.d = d;
+  v.t_lo = t_lo;
+  v.mode = 0;
+  v.list_len = 0;
+  v.chunk_base = 0;
+  v.prefix = 0;
+  v.krem = (uint32_t)d.k;
+  v.gt = 0;
+  v.overflow = 0;
+  v.resolved = 0;
+  v.chunks_done[0] = v.chunks_done[1] = v.chunks_done[2] = 0;
+  v.cand_count = -1;
+  st[s] = v;
+}
+
+// Sampling pass 2: histogram of the next 10 key bits of the sampled keys in
+// bin b0; the CTA that merges last sets T_lo = the lower edge of the 21-bit
+// bin holding the rank-th largest sampled key (so at least `rank` sampled
+// keys are >= T_lo) and the segment's state for the later passes.
+__global__ void __launch_bounds__(kSampleThreads)
+topk_prepare(LargeBatch b, IO io, uint32_t* hist1, SampleState* ss, SegState* st, int ctas) {
+  __shared__ uint32_t sh[1024];
+  __shared__ uint32_t scratch[64];
+  __shared__ int s_last;
+  const int s = blockIdx.x / ctas, q = blockIdx.x % ctas;
+  const LargeSeg d = b.seg[s];
+  const int64_t nblk = sample_blocks(d.len);
+  if (!samples_needed(d, nblk)) {
+    if (q == 0 && threadIdx.x == 0) init_state(st, s, d, d.rank <= 0 ? kNoCandidate : 0u);
+    return;
+  }
+  const uint32_t b0 = *reinterpret_cast<volatile uint32_t*>(&ss[s].b0);
+  const unsigned lane = lane_id();
+  const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
+  const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  for (int64_t bb = gw; bb < nblk; bb += kWarps * kSampleUnroll) {
+    uint32_t key[kSampleUnroll][2];
+    bool ok[kSampleUnroll];
+    sample_keys(io, d, nblk, bb, kWarps, lane, key, ok);
+#pragma unroll
+    for (int u = 0; u < kSampleUnroll; ++u) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (ok[u] && (key[u][h] >> 20) == b0) atomicAdd(&sh[(key[u][h] >> 10) & 1023u], 1u);
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = hist1 + (int64_t)s * 1024;
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ss[s].done[1], 1u) == (uint32_t)ctas - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+    sh[i] = *reinterpret_cast<volatile uint32_t*>(&gh[i]);
+  __syncthreads();
+  uint32_t bin, above;
+  block_find_bin(sh, 1024, *reinterpret_cast<volatile uint32_t*>(&ss[s].r1), scratch, &bin,
+                 &above);
+  if (threadIdx.x == 0) init_state(st, s, d, (b0 << 20) | (bin << 10));
 }
 
 __device__ __forceinline__ int find_seg(const int64_t* base, int nseg, int64_t x) {
@@ -479,20 +601,15 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
           g.y = __fadd_rn(gr[u].y, ee[u].y);
           g.z = __fadd_rn(gr[u].z, ee[u].z);
           g.w = __fadd_rn(gr[u].w, ee[u].w);
+          const bool full = vec && o >= lo && o + 4 <= hi;
           uint32_t nib = 0;
-          if (vec && o >= lo && o + 4 <= hi) {
-            __stcs(reinterpret_cast<float4*>(ep + o), g);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) nib |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << c;
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (o + c >= lo && o + c < hi) {
-                ep[o + c] = get4(g, c);
-                nib |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << c;
-              }
-            }
-          }
+          for (int c = 0; c < 4; ++c)
+            if (full || (o + c >= lo && o + c < hi))
+              nib |= (uint32_t)(abs_key(get4(g, c)) >= t_lo) << c;
+          // staged candidates are written to e as +0 (emit puts g back at
+          // the ones not taken); a candidate without a staging slot keeps g
+          uint32_t zero = 0;
           if (__any_sync(kFull, nib != 0)) {
             const uint32_t n4 = __popc(nib);
             const uint32_t inc = warp_incl_scan(n4);
@@ -500,12 +617,25 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               if ((nib >> c) & 1u) {
-                if (pos < kStageCap)
+                if (pos < kStageCap) {
                   stage[pos] = make_uint2(loc0 + (uint32_t)(o + c), __float_as_uint(get4(g, c)));
+                  zero |= 1u << c;
+                }
                 ++pos;
               }
             }
             count += __shfl_sync(kFull, inc, 31);
+          }
+          g.x = (zero & 1u) ? 0.0f : g.x;
+          g.y = (zero & 2u) ? 0.0f : g.y;
+          g.z = (zero & 4u) ? 0.0f : g.z;
+          g.w = (zero & 8u) ? 0.0f : g.w;
+          if (full) {
+            __stcs(reinterpret_cast<float4*>(ep + o), g);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (o + c >= lo && o + c < hi) ep[o + c] = get4(g, c);
           }
         }
       }
@@ -531,12 +661,22 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
       const uint64_t excl = lookback_warp(tstate, tile, s_base[seg], agg, io.status);
       if (agg) {
         const int64_t cap = st[seg].d.cap;
+        float* es = io.e + st[seg].d.off;
         uint2* out = cand + st[seg].d.cand_base;
         for (int w = 0; w < kStreamWarps; ++w) {
-          const uint32_t cw = min(__shfl_sync(kFull, c, w), (uint32_t)kStageCap);
+          const uint32_t ct = __shfl_sync(kFull, c, w);
+          const uint32_t cw = min(ct, (uint32_t)kStageCap);
           const int64_t base = (int64_t)excl + __shfl_sync(kFull, inc - c, w);
-          for (uint32_t j = lane; j < cw; j += 32)
-            if (base + j < cap) out[base + j] = sg.cand[b][w][j];
+          for (uint32_t j = lane; j < cw; j += 32) {
+            const uint2 v = sg.cand[b][w][j];
+            if (base + j < cap)
+              out[base + j] = v;
+            else
+              es[v.x] = __uint_as_float(v.y);  // no room in the list: e keeps g
+          }
+          // list slots of candidates that found no staging slot
+          for (uint32_t j = kStageCap + lane; j < ct && base + j < cap; j += 32)
+            out[base + j] = make_uint2(kNoEntry, 0u);
         }
       }
       __syncwarp();
@@ -563,6 +703,7 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
     if (d.k == 0) { mode = 0; len = 0; }
     st[s].mode = mode;
     st[s].list_len = len;
+    st[s].cand_count = c;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -589,6 +730,31 @@ __device__ __forceinline__ ListRef list_ref(const SegState* st, int seg) {
   r.off = st[seg].d.off;
   r.len = st[seg].list_len;
   return r;
+}
+
+constexpr int kRestoreThreads = 256;
+
+// A segment whose select runs on the whole segment (mode 1) reads its keys
+// from e, which must then hold g everywhere: g is put back at the candidates
+// the fused pass staged and wrote as +0, from the candidate list (its first
+// min(candidates, capacity) slots; slots of never-staged candidates hold
+// kNoEntry).  Segments selecting on their list are left alone.
+__global__ void __launch_bounds__(kRestoreThreads)
+topk_restore(IO io, const SegState* st, int nseg, const uint2* cand) {
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  for (int s = 0; s < nseg; ++s) {
+    if (st[s].mode != 1) continue;  // uniform across the grid
+    const int64_t c = st[s].cand_count;
+    if (c <= 0) continue;  // no candidates, or a pass that already reported an error
+    const int64_t m = min(c, st[s].d.cap);
+    const int64_t len = st[s].d.len;
+    const uint2* l = cand + st[s].d.cand_base;
+    float* es = io.e + st[s].d.off;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < m; j += nthr) {
+      const uint2 v = l[j];
+      if (v.x != kNoEntry && (int64_t)v.x < len) es[v.x] = __uint_as_float(v.y);
+    }
+  }
 }
 
 // Lists of at most kSelSmall entries: one CTA per segment loads the keys into
@@ -801,7 +967,10 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
     }
     __syncthreads();
     const uint64_t excl = lookback_block(cstate, c, s_cb[seg], s_agg, io.status, s_lb);
-    if (cg | ce) {  // warp-uniform
+    // On a candidate list (mode 0) e holds +0 at every entry: entries not
+    // taken get g back.  On the whole segment (mode 1) taken entries get +0.
+    const bool on_list = l.mode == 0;
+    if (cg | ce | (on_list ? cl : 0u)) {  // warp-uniform
       int64_t run_gt = (int64_t)(excl >> 31) + s_ogt[warp];
       int64_t run_lt = (int64_t)(excl & 0x7FFFFFFFu) + s_olt[warp];
       const unsigned lm = lanemask_lt();
@@ -814,7 +983,9 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
         const int64_t eq_before = j - gt_before - (run_lt + __popc(bl & lm));
         if (g || (q && eq_before < (int64_t)need)) {
           const int64_t pos = out_off + gt_before + min(eq_before, (int64_t)need);
-          emit_one(io, seg_off + loc[r], pos, out_end, __uint_as_float(vb[r]));
+          emit_one(io, seg_off + loc[r], pos, out_end, __uint_as_float(vb[r]), !on_list);
+        } else if (on_list && (q || b)) {
+          io.e[seg_off + loc[r]] = __uint_as_float(vb[r]);
         }
         run_gt += __popc(bg);
         run_lt += __popc(bl);
@@ -842,16 +1013,20 @@ struct Plan {
   int64_t total_k = 0;
   // workspace regions (byte offsets); batches reuse the same regions
   size_t off_ctl = 0, off_st = 0, off_hist = 0, off_tiles = 0, off_chunks = 0, off_cand = 0;
-  size_t off_samples = 0;
+  size_t off_hist0 = 0, off_hist1 = 0, off_sstate = 0;
   size_t ctl_clear_bytes = 0;  // bytes cleared from off_ctl before each batch
   size_t bytes = 0;
 };
 
+// Rank of T_lo among a segment's sampled keys: the expected number of
+// sampled keys at or above the k-th largest key, m = k * S / len, plus five
+// standard deviations and 10 (0: no candidates; > S: every element).
 int64_t sample_rank(int64_t k, int64_t len) {
   if (k <= 0) return 0;
-  const double m = (double)k * kSample / (double)len;
+  const int64_t S = sample_blocks(len) * kSampleBlock;
+  const double m = (double)k * (double)S / (double)len;
   const double r = std::ceil(m + 5.0 * std::sqrt(m) + 10.0);
-  return r > (double)kSample ? (int64_t)kSample + 1 : (int64_t)r;
+  return r > (double)S ? S + 1 : (int64_t)r;
 }
 
 ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* ks,
@@ -913,6 +1088,12 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     off = round_up(off + sizeof(SegState) * kMaxLarge, 256);
     p->off_hist = off;
     off = round_up(off + (size_t)kMaxLarge * 2048 * 4, 256);
+    p->off_hist0 = off;
+    off = round_up(off + (size_t)kMaxLarge * 2048 * 4, 256);
+    p->off_hist1 = off;
+    off = round_up(off + (size_t)kMaxLarge * 1024 * 4, 256);
+    p->off_sstate = off;
+    off = round_up(off + sizeof(SampleState) * kMaxLarge, 256);
     p->off_tiles = off;
     off = round_up(off + (size_t)tiles * 8, 256);
     p->off_chunks = off;
@@ -920,8 +1101,6 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     p->ctl_clear_bytes = off - p->off_ctl;
     p->off_cand = off;
     off = round_up(off + (size_t)cands * 8, 256);
-    p->off_samples = off;
-    off = round_up(off + (size_t)segs * kSample * 4, 256);
   }
   p->bytes = off;
   return EF_OK;
@@ -934,15 +1113,12 @@ ef_status set_attributes(int dev) {
   if (dev < 0 || dev >= 64) return EF_ERR_ARCH;
   std::call_once(g_attr_once[dev], [&]() {
     const int small_smem = (kSmallMax + 2048 + 64) * 4;
-    const int prep_smem = (kSample + 2048 + 64) * 4;
     cudaError_t e1 = cudaFuncSetAttribute(topk_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           small_smem);
-    cudaError_t e2 = cudaFuncSetAttribute(topk_prepare,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
     const int sel_smem = (kSelSmall + 2048 + 64) * 4;
-    cudaError_t e3 = cudaFuncSetAttribute(topk_select_small,
+    cudaError_t e2 = cudaFuncSetAttribute(topk_select_small,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
-    cudaError_t bad = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    cudaError_t bad = e1 != cudaSuccess ? e1 : e2;
     g_attr_status[dev] = bad == cudaSuccess ? EF_OK : cuda_fail(bad);
   });
   return g_attr_status[dev];
@@ -1054,17 +1230,23 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     }
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
-    uint32_t* samples = reinterpret_cast<uint32_t*>(ws + p.off_samples);
-    topk_sample<<<nsg * kSampleCtas, kSampleThreads, 0, s>>>(lb, io, samples);
+    uint32_t* hist0 = reinterpret_cast<uint32_t*>(ws + p.off_hist0);
+    uint32_t* hist1 = reinterpret_cast<uint32_t*>(ws + p.off_hist1);
+    SampleState* sstate = reinterpret_cast<SampleState*>(ws + p.off_sstate);
+    // sampling CTAs per segment: about four per SM in all, 8 to 128 each
+    const int sctas = (int)std::max<int64_t>(
+        8, std::min<int64_t>(kSampleCtasMax, (int64_t)dev.sms * 4 / nsg));
+    topk_sample<<<nsg * sctas, kSampleThreads, 0, s>>>(lb, io, hist0, sstate, sctas);
     if ((st = check_launch()) != EF_OK) return st;
-    const size_t prep_smem = (size_t)(kSample + 2048 + 64) * 4;
-    topk_prepare<<<nsg, kPrepThreads, prep_smem, s>>>(lb, nsg, samples, sst);
+    topk_prepare<<<nsg * sctas, kSampleThreads, 0, s>>>(lb, io, hist1, sstate, sst, sctas);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
     topk_fused<<<fgrid, kFusedThreads, 0, s>>>(io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
+    topk_restore<<<dev.sms * 2, kRestoreThreads, 0, s>>>(io, sst, nsg, cand);
+    if ((st = check_launch()) != EF_OK) return st;
     topk_select_small<<<nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s>>>(io, sst,
                                                                                       cand);
     if ((st = check_launch()) != EF_OK) return st;

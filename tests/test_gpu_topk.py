@@ -83,16 +83,41 @@ def test_unaligned_addresses():
     check_topk_step(base_g[2:n + 2], base_e[3:n + 3], [0, 5, 50_007, n], [1, 400, 700])
 
 
+def _sample_block_starts(n):
+    """Starts of the sampled blocks of a streaming segment of n elements:
+    min(4096, n // 1024) blocks of 64 contiguous elements centred on evenly
+    spaced points (the documented sampling rule of the library)."""
+    nblk = min(4096, n // 1024)
+    b = np.arange(nblk, dtype=np.int64)
+    return np.clip((2 * b + 1) * n // (2 * nblk) - 32, 0, n - 64)
+
+
 def test_sampled_threshold_too_high_falls_back():
-    """Large values exactly at the sampled positions push the sampled
-    threshold above the true k-th key; the whole-segment select must take
-    over and still give the oracle's answer."""
-    n, k, S = 1 << 20, 10486, 32768
+    """Large values on exactly the sampled blocks push the sampled threshold
+    above the true k-th key, so fewer than k candidates are found; the
+    whole-segment select must take over (after putting g back at the
+    candidates) and still give the oracle's answer."""
+    n, k = 1 << 20, 10486
     g = torch.full((n,), 1e-4, device=DEV) * torch.linspace(1, 2, n, device=DEV)
-    j = torch.arange(S, device=DEV, dtype=torch.int64)
-    pos = ((2 * j + 1) * n) // (2 * S)
-    g[pos] = 1.0 + j.float() * 1e-6
+    starts = _sample_block_starts(n)
+    pos = (starts[:, None] + np.arange(64)[None, :]).ravel()
+    big = 1.0 + np.arange(pos.size, dtype=np.float32) * 1e-6
+    g[torch.from_numpy(pos).to(DEV)] = torch.from_numpy(big).to(DEV)
     check_topk_step(g, torch.zeros(n, device=DEV), [0, n], [k])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_candidate_list_over_capacity_falls_back(fmt):
+    """5 % of the elements tie at the largest value: every one is a
+    candidate (about 200 per 4096-element warp span, within the staging
+    buffers) but together they exceed the list capacity 4k + 65536; the
+    candidates past the capacity keep g, the fused pass's zeros are undone,
+    and the whole-segment select picks the lowest-index ties."""
+    n, k = 2_000_000, 1000
+    rng = np.random.default_rng(17)
+    g_np = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    g_np[rng.choice(n, n // 20, replace=False)] = 0.5
+    check_topk_step(torch.from_numpy(g_np).to(DEV), torch.zeros(n, device=DEV), [0, n], [k], fmt)
 
 
 def test_multistep_carries_residual():
