@@ -41,18 +41,18 @@ UNIT = "G grad elements/s"
 
 # DRAM traffic of one topk_fused launch from one ncu capture (--set full,
 # slab workload at n = 2^26 per worker, see profiles/): 536.97 MB read +
-# 220.88 MB written = 11.293 bytes per element.  Reported, scaled by n, only
+# 224.77 MB written = 11.351 bytes per element.  Reported, scaled by n, only
 # while the captured code still hashes to what was captured (the kernel's
 # region of ef_topk.cu, from its staging struct to the end of the kernel, and
 # the shared device header); otherwise null.  (Reads scale with n exactly;
 # the writes fall short of 12 B by the dirty lines still in L2 when the
 # captured launch ends.)
-FUSED_TRAFFIC_PER_ELEMENT = 11.293
+FUSED_TRAFFIC_PER_ELEMENT = 11.351
 FUSED_TRAFFIC_SOURCES = {
     # (file, first marker, end marker or None for the whole file): sha256
     ("error_feedback_gradient_gb300/csrc/ef_topk.cu", "struct FusedStage {",
      "// A segment's select list:"):
-        "36c3ecac2bb5855c1ffc576df5b36989327df45ee747a8fb657a12d0dbe33d1f",
+        "5e01040e0c37eedae71aacfa28bdec0b4ef57ae6fdd251f6b196d968344df584",
     ("error_feedback_gradient_gb300/csrc/ef_common.cuh", None, None):
         "8c82518cf4425bdd6f8024b355289fa0e638002f3e8476314350ba0271a997c1",
 }
