@@ -12,11 +12,15 @@ from .ef_oracle import (  # noqa: F401
     onebit_momentum,
     pack_bits,
     packet_indices,
+    q8_dequantize,
+    q8_quantize,
+    q8_scale,
     sgd_apply,
     sign_aggregate,
     sign_ef_step,
     sparse_aggregate,
     topk_ef_step,
+    topk_q8_ef_step,
     topk_indices,
     unpack_bits,
 )

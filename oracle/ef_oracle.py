@@ -16,7 +16,9 @@ Sources (web pages, cited by title and section):
   k largest |g|, send values + indices, the receiver sums by index);
   必不可少的误差补偿 (error compensation); Top-k 稀疏化; 分层阈值与自适应稀疏率
   and 分层自适应Top-k (each tensor selects independently); 详细算法流程
-  (the seven-step algorithm: steps 2-7); 索引编码压缩 (bitmap index).
+  (the seven-step algorithm: steps 2-7); 索引编码压缩 (bitmap index);
+  与其他压缩技术的比较 (top-k followed by 8-bit quantisation of the selected
+  values).
 * [ONEBIT] "1bit Adam梯度压缩技术原理与分布式训练优化" ("1-bit Adam gradient
   compression: principle and distributed-training optimisation"),
   intelliparadigm.com article.  Sections used: 2.1 量化与误差补偿机制 (sign
@@ -43,7 +45,13 @@ Readings taken where the pages are silent (each repeated where it is used):
 * sign(0) = +1 (also for -0 and NaN): a bit is 1 unless v < 0;
 * the receiver adds packets in worker order 0..W-1 starting from +0.0 and
   does not average;
-* (1 - beta1) is formed in float32 before it multiplies.
+* (1 - beta1) is formed in float32 before it multiplies;
+* 8-bit quantisation of a packet's values (the pages give no formula): one
+  float32 scale per segment, s = max |v| / 127 over the segment's finite
+  selected values (0 if none); q = round-half-even(v / s) clamped to
+  [-127, 127], q = 0 for NaN and whenever s = 0; the receiver's value is
+  q * s, and the residual at a selected position is v - q * s, so the error
+  feedback also carries the quantisation error.
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``; no
 function here is parity-unpinned.
@@ -165,8 +173,9 @@ def topk_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
 
     Returns a dict with ``values`` (float32[sum k]), ``indices`` (int32
     global indices, only for ``idx_format == "int32"``), ``bitmap``
-    (uint32[ceil(n/32)], only for ``"bitmap"``) and ``e`` (the new residual,
-    float32[n]).
+    (uint32[ceil(n/32)], only for ``"bitmap"``), ``e`` (the new residual,
+    float32[n]) and ``selected`` (the global indices as int64, for callers
+    inside the oracle).
     """
     g_raw = np.ascontiguousarray(g_raw, dtype=F32)
     e_prev = np.ascontiguousarray(e, dtype=F32)
@@ -189,7 +198,7 @@ def topk_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
     sel = np.concatenate(picked) if picked else np.zeros(0, np.int64)
     values = g[sel].copy()                                # step 5 (values)
     e_new[sel] = F32(0.0)                                 # step 4 on the selection
-    out = {"values": values, "e": e_new}
+    out = {"values": values, "e": e_new, "selected": sel}
     if idx_format == "int32":
         if n > 2**31:
             raise ValueError("int32 indices need n <= 2**31")
@@ -200,6 +209,88 @@ def topk_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
         out["bitmap"] = pack_bits(flags)
     else:
         raise ValueError(idx_format)
+    return out
+
+
+# --------------------------------------------------------------------------
+# 8-bit quantisation of the selected values  ([SPARSE] §与其他压缩技术的比较)
+# --------------------------------------------------------------------------
+
+Q8_LEVELS = 127
+
+
+def q8_scale(values) -> np.float32:
+    """Scale of one segment's packet: s = max |v| / 127 in float32.
+
+    [SPARSE] §与其他压缩技术的比较 quantises the top-k values to 8 bits after
+    the selection and gives no formula; the reading here is symmetric int8
+    with one scale per segment (tensor).  Only finite values count towards
+    the maximum; with none (or an empty segment) s = 0.
+    """
+    v = np.asarray(values, dtype=F32)
+    fin = v[np.isfinite(v)]
+    m = np.max(np.abs(fin)) if fin.size else F32(0.0)
+    return np.divide(F32(m), F32(Q8_LEVELS), dtype=F32)
+
+
+def q8_quantize(values, s) -> np.ndarray:
+    """q = round-half-even(v / s) clamped to [-127, 127], as int8.
+
+    v / s is one float32 division; q = 0 for NaN values and for every value
+    when s = 0; +-Inf clamps to +-127.
+    """
+    v = np.asarray(values, dtype=F32)
+    s = F32(s)
+    q = np.zeros(v.size, dtype=np.int8)
+    if s == F32(0.0):
+        return q
+    ok = ~np.isnan(v)
+    with np.errstate(over="ignore", invalid="ignore"):
+        t = np.divide(v[ok], s, dtype=F32)
+    t = np.minimum(np.maximum(t, F32(-Q8_LEVELS)), F32(Q8_LEVELS))
+    q[ok] = np.rint(t).astype(np.int8)
+    return q
+
+
+def q8_dequantize(q, s) -> np.ndarray:
+    """The receiver's value of each entry: q * s, one float32 multiply."""
+    return np.multiply(np.asarray(q, dtype=np.int8).astype(F32), F32(s), dtype=F32)
+
+
+def topk_q8_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
+    """A top-k error-feedback step whose packet values are 8-bit quantised.
+
+    [SPARSE] §详细算法流程 steps 2-5 (topk_ef_step) followed by the 8-bit
+    quantisation of §与其他压缩技术的比较, per segment: s = q8_scale of the
+    segment's selected values, q = q8_quantize(v, s).  What the packet
+    carries at a selected position is q * s, so step 4's residual
+    e = g - g~ becomes v - q * s there (one float32 subtraction) and stays g
+    elsewhere.
+
+    Returns the topk_ef_step dict with ``q`` (int8[sum k]), ``scales``
+    (float32[nseg]) and ``e`` replaced by this residual; ``values`` keeps the
+    unquantised selected values.
+    """
+    out = topk_ef_step(g_raw, e, seg_offsets, seg_k, idx_format)
+    ks = [int(x) for x in seg_k]
+    v = out["values"]
+    sel = out["selected"]
+    e_new = out["e"]
+    q = np.zeros(v.size, dtype=np.int8)
+    scales = np.zeros(len(ks), dtype=F32)
+    j = 0
+    for s_i, k in enumerate(ks):
+        vs = v[j:j + k]
+        sc = q8_scale(vs)
+        qs = q8_quantize(vs, sc)
+        with np.errstate(invalid="ignore"):
+            e_new[sel[j:j + k]] = np.subtract(vs, q8_dequantize(qs, sc), dtype=F32)
+        q[j:j + k] = qs
+        scales[s_i] = sc
+        j += k
+    out["q"] = q
+    out["scales"] = scales
+    out["e"] = e_new
     return out
 
 

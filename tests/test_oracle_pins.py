@@ -423,6 +423,103 @@ def test_sign_aggregate_counts():
 
 
 # ---------------------------------------------------------------------------
+# 8-bit quantisation of the selected values
+# ---------------------------------------------------------------------------
+
+
+def _fx(x):
+    return float(x)   # json strings "inf" / "nan" parse through float()
+
+
+def check_q8_golden(scale=None, quantize=None, dequantize=None):
+    scale = scale or oracle.q8_scale
+    quantize = quantize or oracle.q8_quantize
+    dequantize = dequantize or oracle.q8_dequantize
+    for ex in _load("q8_examples.json")["quantise"]:
+        v = np.array([_fx(x) for x in ex["values"]], F32)
+        s = scale(v)
+        assert float(s) == ex["scale"], ex["name"]
+        q = quantize(v, s)
+        assert q.dtype == np.int8 and q.tolist() == ex["q"], ex["name"]
+        dq = dequantize(q, s)
+        assert dq.tolist() == ex["dequantised"], ex["name"]
+        with np.errstate(invalid="ignore"):
+            r = np.subtract(v, dq, dtype=F32)
+        want = np.array([_fx(x) for x in ex["residual"]], F32)
+        assert np.array_equal(np.isnan(r), np.isnan(want)), ex["name"]
+        ok = ~np.isnan(want)
+        assert [_bits_of(float(x)) for x in r[ok]] == [_bits_of(float(x)) for x in want[ok]]
+
+
+def check_q8_ef_golden(step=None):
+    step = step or oracle.topk_q8_ef_step
+    fx = _load("q8_examples.json")["ef_step"]
+    out = step(_arr(fx["g_raw"]), np.zeros(6, F32), [0, 6], [fx["k"]])
+    assert out["indices"].tolist() == fx["indices"]
+    assert out["values"].tolist() == fx["values"]
+    assert out["scales"].tolist() == [fx["scale"]]
+    assert out["q"].tolist() == fx["q"]
+    assert out["e"].tolist() == fx["e"]
+
+
+def test_q8_worked_examples():
+    check_q8_golden()
+    check_q8_ef_golden()
+
+
+def test_q8_invariants_random():
+    """On random finite values: |q| <= 127; the largest |v| maps to +-127;
+    sign(q) is 0 or sign(v); q is monotone in v; |v - q s| <= s / 2 (one
+    rounding of slack); and q s + (v - q s) == v bit for bit, because for
+    q != 0 the two terms lie within a factor 2 of each other (Sterbenz), so
+    the residual subtraction is exact: the receiver's value plus the new
+    residual gives back g exactly."""
+    rng = np.random.default_rng(4)
+    for trial in range(50):
+        n = int(rng.integers(1, 2000))
+        v = (rng.standard_t(3, n) * 10.0 ** rng.uniform(-8, 3)).astype(F32)
+        s = oracle.q8_scale(v)
+        assert s == np.float32(np.max(np.abs(v))) / np.float32(127)
+        q = oracle.q8_quantize(v, s)
+        assert np.all(np.abs(q.astype(np.int32)) <= 127)
+        assert abs(int(q[np.argmax(np.abs(v))])) == 127
+        assert np.all((q == 0) | (np.sign(q) == np.sign(v)))
+        order = np.argsort(v, kind="stable")
+        assert np.all(np.diff(q[order].astype(np.int32)) >= 0)
+        dq = oracle.q8_dequantize(q, s)
+        r = np.subtract(v, dq, dtype=F32)
+        assert np.all(np.abs(r.astype(np.float64)) <= 0.5 * float(s) * (1 + 2.0 ** -20))
+        assert np.array_equal(np.add(dq, r, dtype=F32).view(np.uint32), v.view(np.uint32))
+
+
+def test_q8_ef_step_residual_identity():
+    """A quantised top-k EF step against the plain step: same selection and
+    values; off the selection the residuals agree bit for bit; on it the
+    receiver's value plus the residual is g exactly; per-segment scales."""
+    rng = np.random.default_rng(9)
+    n = 5000
+    offs, ks = [0, 100, 1700, 5000], [7, 40, 90]
+    g_raw = (rng.standard_t(3, n) * 1e-3).astype(F32)
+    e = (rng.standard_normal(n) * 1e-4).astype(F32)
+    plain = oracle.topk_ef_step(g_raw, e, offs, ks)
+    q8 = oracle.topk_q8_ef_step(g_raw, e, offs, ks)
+    assert q8["indices"].tolist() == plain["indices"].tolist()
+    assert q8["values"].tolist() == plain["values"].tolist()
+    off = np.ones(n, bool)
+    off[plain["indices"]] = False
+    assert np.array_equal(q8["e"][off].view(np.uint32), plain["e"][off].view(np.uint32))
+    j = 0
+    for si, k in enumerate(ks):
+        v = plain["values"][j:j + k]
+        assert q8["scales"][si] == oracle.q8_scale(v)
+        dq = oracle.q8_dequantize(q8["q"][j:j + k], q8["scales"][si])
+        idx = plain["indices"][j:j + k]
+        g = oracle.compensate(g_raw, e)[idx]
+        assert np.array_equal(np.add(dq, q8["e"][idx], dtype=F32).view(np.uint32), g.view(np.uint32))
+        j += k
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: the pins above must catch them
 # ---------------------------------------------------------------------------
 
@@ -475,6 +572,33 @@ def _sgd_wrong_sign(w, G, eta):
     return (np.asarray(w, F32) + F32(eta) * np.asarray(G, F32)).astype(F32)
 
 
+def _q8_round_half_away(values, s):
+    v = np.asarray(values, F32)
+    q = np.zeros(v.size, np.int8)
+    if F32(s) == F32(0):
+        return q
+    ok = ~np.isnan(v)
+    t = np.clip(np.divide(v[ok], F32(s), dtype=F32), -127, 127)
+    q[ok] = (np.sign(t) * np.floor(np.abs(t) + F32(0.5))).astype(np.int8)
+    return q
+
+
+def _q8_scale_over_128(values):
+    return np.float32(oracle.q8_scale(values) * np.float32(127) / np.float32(128))
+
+
+def _q8_scale_with_inf(values):
+    v = np.asarray(values, F32)
+    m = np.max(np.abs(v[~np.isnan(v)])) if v.size else F32(0)
+    return np.divide(F32(m), F32(127), dtype=F32)
+
+
+def _q8_step_drops_quantisation_error(g_raw, e, offs, ks, idx_format="int32"):
+    out = oracle.topk_q8_ef_step(g_raw, e, offs, ks, idx_format)
+    out["e"][out["selected"]] = F32(0)
+    return out
+
+
 @pytest.mark.parametrize("check,kwargs", [
     (check_topk_bruteforce, {"topk_indices": _topk_ties_to_higher_index}),
     (check_topk_bruteforce, {"topk_indices": _topk_signed_not_abs}),
@@ -483,6 +607,10 @@ def _sgd_wrong_sign(w, G, eta):
     (check_sign_golden, {"sign_step": _sign_zero_is_zero}),
     (check_aggregate_golden, {"aggregate": _aggregate_reverse_order}),
     (check_aggregate_golden, {"sgd": _sgd_wrong_sign}),
+    (check_q8_golden, {"quantize": _q8_round_half_away}),
+    (check_q8_golden, {"scale": _q8_scale_over_128}),
+    (check_q8_golden, {"scale": _q8_scale_with_inf}),
+    (check_q8_ef_golden, {"step": _q8_step_drops_quantisation_error}),
 ])
 def test_pins_catch_planted_mistakes(check, kwargs):
     with pytest.raises(AssertionError):
