@@ -458,6 +458,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     if args.extras and rank == 0:
         line["per_config"] = run_extras(args, dev)
+        line["next_rows"] = run_next(args, dev)
     # the CPU oracle baseline last (rank 0, N = 1 only), after the GPU legs,
     # so its host allocations cannot disturb the pinned-memory uploads
     if rank == 0 and world == 1 and args.baseline_sample > 0:
@@ -661,6 +662,73 @@ def run_extras(args, dev):
     bytes_ = w.workers * (12 * w.n + 8 * w.total_k) + 4 * w.n + 16 * w.workers * w.total_k
     out["bert_large"] = {"ms_per_step": ms, "g_elems_per_s": w.workers * w.n / ms / 1e6,
                          "gbs": bytes_ / ms / 1e6}
+    return out
+
+
+def run_next(args, dev):
+    """The widened rows beyond the step, each timed at the slab size (one
+    worker, 2^31 elements, top-0.1 %) with CUDA events, with the oracle timed
+    beside it on a sample."""
+    import numpy as np
+    import torch
+    import error_feedback_gradient_gb300 as efg
+    from error_feedback_gradient_gb300 import workloads as wl
+    import oracle   # the CPU-baseline leg of each row only
+    out = {}
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    n = args.n
+    k = wl.k_from_ratio(n, 1, 1000)
+    offs, ks = [0, n], [k]
+    g = wl.student_t3(n, 1e-3, wl.seed(5, 0, 1), dev)
+    e = torch.zeros_like(g)
+    v = torch.empty(k, device=dev)
+    idx = torch.empty(k, dtype=torch.int32, device=dev)
+    ws = torch.empty(efg.topk_workspace_size(n, offs, ks), dtype=torch.uint8, device=dev)
+    ms_plain = timed(lambda: efg.topk_compress(g, e, offs, ks, v, idx, None, ws), 5)
+    del ws
+
+    # 8-bit packet values
+    q = torch.empty(k, dtype=torch.int8, device=dev)
+    sc = torch.empty(1, device=dev)
+    wsq = torch.empty(efg.topk_q8_workspace_size(n, offs, ks), dtype=torch.uint8, device=dev)
+    ms_q8 = timed(lambda: efg.topk_compress_q8(g, e, offs, ks, q, sc, idx, None, wsq), 5)
+    ms_dq = timed(lambda: efg.q8_dequantize(q, sc, ks, v), 20)
+    del wsq
+    sample = 1 << 22
+    rng = np.random.default_rng(3)
+    gs = (rng.standard_t(3, sample) * 1e-3).astype(np.float32)
+    es = np.zeros(sample, np.float32)
+    ksm = wl.k_from_ratio(sample, 1, 1000)
+    t0 = time.perf_counter()
+    oracle.topk_q8_ef_step(gs, es, [0, sample], [ksm])
+    dt = time.perf_counter() - t0
+    q_bytes = 17 * k   # max pass 4 B, quantise pass 4 + 4 + 1 + 4 B per entry
+    out["topk_q8"] = {
+        "workload": f"one tensor of {n} elements, k = {k} (top-0.1 %), int32 indices",
+        "ms_topk_compress": ms_plain, "ms_topk_compress_q8": ms_q8,
+        "ms_q8_passes": ms_q8 - ms_plain,
+        "q8_pass_algorithmic_bytes": q_bytes,
+        "q8_pass_gbs": q_bytes / ((ms_q8 - ms_plain) * 1e-3) / 1e9 if ms_q8 > ms_plain else None,
+        "note": "the quantiser's residual write is one scattered 4-byte store per entry",
+        "ms_q8_dequantize": ms_dq, "dequantize_gbs": 5 * k / (ms_dq * 1e-3) / 1e9,
+        "g_elems_per_s": n / ms_q8 / 1e6,
+        "cpu_baseline": {"g_elems_per_s": sample / dt / 1e9, "cores": 1, "kind": "oracle",
+                         "sample": f"one oracle step on {sample} elements, k = {ksm}"}}
+    del g, e, v, idx, q, sc
+    torch.cuda.empty_cache()
     return out
 
 

@@ -19,7 +19,10 @@ from .binding import (  # noqa: F401
     sign_aggregate_apply,
     sign_compress,
     sparse_aggregate_apply,
+    q8_dequantize,
     topk_compress,
+    topk_compress_q8,
+    topk_q8_workspace_size,
     topk_workspace_size,
     aggregate_workspace_size,
     workspace_status,

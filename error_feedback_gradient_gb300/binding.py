@@ -61,6 +61,14 @@ _SIGNATURES = {
     "ef_topk_compress_noalloc": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p,
         ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "ef_topk_q8_workspace_size": (ctypes.c_int32, [
+        ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p, ctypes.c_int32,
+        ctypes.POINTER(ctypes.c_size_t)]),
+    "ef_topk_compress_q8": (ctypes.c_int32, [
+        _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p,
+        ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "ef_q8_dequantize": (ctypes.c_int32, [
+        _c_vp, _c_vp, ctypes.c_int32, _c_i64p, _c_vp, _c_vp]),
     "ef_sign_compress": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_float, _c_vp, _c_vp]),
     "ef_aggregate_workspace_size": (ctypes.c_int32, [
@@ -181,6 +189,42 @@ def topk_compress_noalloc(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Seq
         _ptr(g_raw), _ptr(e), g_raw.numel(), len(seg_k), _i64(seg_offsets), _i64(seg_k),
         int(idx_format), _ptr(out_values), _ptr(out_indices), _ptr(out_bitmap),
         _stream(stream)), "ef_topk_compress_noalloc")
+
+
+def topk_q8_workspace_size(n: int, seg_offsets: Sequence[int], seg_k: Sequence[int],
+                           idx_format: int = IDX_INT32) -> int:
+    out = ctypes.c_size_t(0)
+    _check(library().ef_topk_q8_workspace_size(
+        int(n), len(seg_k), _i64(seg_offsets), _i64(seg_k), int(idx_format),
+        ctypes.byref(out)), "ef_topk_q8_workspace_size")
+    return int(out.value)
+
+
+def topk_compress_q8(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Sequence[int],
+                     seg_k: Sequence[int], out_q: torch.Tensor, out_scale: torch.Tensor,
+                     out_indices: Optional[torch.Tensor] = None,
+                     out_bitmap: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     idx_format: int = IDX_INT32, stream=None) -> None:
+    """ef_topk_compress_q8: top-k EF step with int8 packet values and one
+    fp32 scale per segment (see include/efgrad.h)."""
+    n = g_raw.numel()
+    if workspace is None:
+        nbytes = topk_q8_workspace_size(n, seg_offsets, seg_k, idx_format)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=g_raw.device)
+    _check(library().ef_topk_compress_q8(
+        _ptr(g_raw), _ptr(e), n, len(seg_k), _i64(seg_offsets), _i64(seg_k),
+        int(idx_format), _ptr(out_q), _ptr(out_scale), _ptr(out_indices), _ptr(out_bitmap),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "ef_topk_compress_q8")
+
+
+def q8_dequantize(q: torch.Tensor, scales: torch.Tensor, seg_k: Sequence[int],
+                  out_values: torch.Tensor, stream=None) -> None:
+    """ef_q8_dequantize: out_values = q * scale of each entry's segment."""
+    _check(library().ef_q8_dequantize(
+        _ptr(q), _ptr(scales), len(seg_k), _i64(seg_k), _ptr(out_values),
+        _stream(stream)), "ef_q8_dequantize")
 
 
 # ---------------------------------------------------------------------------

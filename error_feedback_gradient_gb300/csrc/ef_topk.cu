@@ -46,6 +46,7 @@
 #include <vector>
 
 #include "ef_common.cuh"
+#include "ef_topk_internal.h"
 
 namespace ef {
 namespace {
@@ -149,6 +150,7 @@ struct IO {
   int32_t* out_indices;
   uint32_t* out_bitmap;
   int32_t* status;
+  uint32_t* pos_out;  // optional: each packet entry's position inside its segment
 };
 
 // Shared scratch of lookback_block.
@@ -217,16 +219,18 @@ __device__ uint64_t lookback_block(uint64_t* states, int64_t tile, int64_t first
 }
 
 // Writes packet entry `pos` (must lie below `limit`, the segment's packet end;
-// anything else would be a library defect and is recorded, not written), and
-// e = +0 at the element unless it already holds +0 (zero_e false).
-__device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t pos, int64_t limit,
-                                         float v, bool zero_e) {
+// anything else would be a library defect and is recorded, not written) for
+// element gidx (local index lidx in its segment), and e = +0 at the element
+// unless it already holds +0 (zero_e false).
+__device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t lidx, int64_t pos,
+                                         int64_t limit, float v, bool zero_e) {
   if (pos >= limit) {
     set_status(io.status, EF_ERR_INTERNAL);
     return;
   }
   io.out_values[pos] = v;
   if (io.out_indices) io.out_indices[pos] = (int32_t)gidx;
+  if (io.pos_out) io.pos_out[pos] = (uint32_t)lidx;
   if (io.out_bitmap) atomicOr(io.out_bitmap + (gidx >> 5), 1u << (gidx & 31));
   if (zero_e) io.e[gidx] = 0.0f;
 }
@@ -301,7 +305,7 @@ topk_small(SmallBatch b, IO io, int keys_words) {
     const uint32_t eq_before = run_eq + __popc(bq & lm);
     if (gt || (eq && eq_before < r.need)) {
       const int64_t pos = sg.out_off + gt_before + min(eq_before, r.need);
-      emit_one(io, sg.off + i, pos, sg.out_off + sg.k, __uint_as_float(bits), true);
+      emit_one(io, sg.off + i, i, pos, sg.out_off + sg.k, __uint_as_float(bits), true);
     }
     run_gt += __popc(bg);
     run_eq += __popc(bq);
@@ -983,7 +987,7 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
         const int64_t eq_before = j - gt_before - (run_lt + __popc(bl & lm));
         if (g || (q && eq_before < (int64_t)need)) {
           const int64_t pos = out_off + gt_before + min(eq_before, (int64_t)need);
-          emit_one(io, seg_off + loc[r], pos, out_end, __uint_as_float(vb[r]), !on_list);
+          emit_one(io, seg_off + loc[r], loc[r], pos, out_end, __uint_as_float(vb[r]), !on_list);
         } else if (on_list && (q || b)) {
           io.e[seg_off + loc[r]] = __uint_as_float(vb[r]);
         }
@@ -1138,11 +1142,24 @@ extern "C" ef_status ef_topk_workspace_size(int64_t n, int32_t nseg, const int64
   return EF_OK;
 }
 
-extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, int32_t nseg,
-                                      const int64_t* h_seg_offsets, const int64_t* h_seg_k,
-                                      int32_t idx_format, float* out_values,
-                                      int32_t* out_indices, uint32_t* out_bitmap,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
+namespace ef {
+
+ef_status topk_plan_info(int64_t n, int32_t nseg, const int64_t* h_seg_offsets,
+                         const int64_t* h_seg_k, int32_t idx_format, size_t* bytes,
+                         int64_t* total_k) {
+  Plan p;
+  ef_status st = make_plan(n, nseg, h_seg_offsets, h_seg_k, idx_format, &p);
+  if (st != EF_OK) return st;
+  *bytes = p.bytes;
+  *total_k = p.total_k;
+  return EF_OK;
+}
+
+ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t nseg,
+                             const int64_t* h_seg_offsets, const int64_t* h_seg_k,
+                             int32_t idx_format, float* out_values, int32_t* out_indices,
+                             uint32_t* out_bitmap, uint32_t* pos_out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   using namespace ef;
   Plan p;
   ef_status st = make_plan(n, nseg, h_seg_offsets, h_seg_k, idx_format, &p);
@@ -1188,7 +1205,7 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     if (err != cudaSuccess) return cuda_fail(err);
   }
   IO io{g_raw, e, out_values, bitmap ? nullptr : out_indices, bitmap ? out_bitmap : nullptr,
-        reinterpret_cast<int32_t*>(ws)};
+        reinterpret_cast<int32_t*>(ws), pos_out};
 
   // small segments
   for (size_t i0 = 0; i0 < p.small.size(); i0 += kMaxSmall) {
@@ -1260,6 +1277,18 @@ extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, i
     if ((st = check_launch()) != EF_OK) return st;
   }
   return EF_OK;
+}
+
+}  // namespace ef
+
+extern "C" ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n, int32_t nseg,
+                                      const int64_t* h_seg_offsets, const int64_t* h_seg_k,
+                                      int32_t idx_format, float* out_values,
+                                      int32_t* out_indices, uint32_t* out_bitmap,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return ef::topk_compress_impl(g_raw, e, n, nseg, h_seg_offsets, h_seg_k, idx_format,
+                                out_values, out_indices, out_bitmap, nullptr, workspace,
+                                workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

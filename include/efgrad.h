@@ -173,6 +173,50 @@ EF_API ef_status ef_topk_compress_noalloc(const float* g_raw, float* e, int64_t 
                                           uint32_t* out_bitmap, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Top-k error feedback with 8-bit packet values.
+ *
+ * [SPARSE] §与其他压缩技术的比较: after top-k, the selected values are
+ * quantised to 8 bits.  The page gives no formula; the reading here is:
+ *   per segment: s = RN(max|v| / 127) over its finite selected values
+ *                (0 if it has none),
+ *   q = round-half-even(clamp(RN(v / s), -127, 127)), 0 for NaN or s = 0,
+ *   the receiver's value is RN(q * s), and the residual at a selected
+ *   position becomes RN(v - RN(q * s)) (step 4, e = g - g~ with g~ what the
+ *   packet carries); elsewhere it is g as in ef_topk_compress.
+ *
+ * Arguments as ef_topk_compress, except:
+ * out_q       [sum k] int8 codes, in the same order as out_values would be.
+ * out_scale   [nseg] fp32 per-segment scale (0 for a segment with k = 0).
+ * workspace   >= ef_topk_q8_workspace_size() bytes, 256-byte aligned; it
+ *             also holds the unquantised values and each entry's position.
+ * out_q and out_scale must not overlap each other, the inputs, the index
+ * output or the workspace.
+ * ---------------------------------------------------------------------- */
+EF_API ef_status ef_topk_q8_workspace_size(int64_t n, int32_t nseg,
+                                           const int64_t* h_seg_offsets,
+                                           const int64_t* h_seg_k, int32_t idx_format,
+                                           size_t* bytes);
+EF_API ef_status ef_topk_compress_q8(const float* g_raw, float* e, int64_t n, int32_t nseg,
+                                     const int64_t* h_seg_offsets, const int64_t* h_seg_k,
+                                     int32_t idx_format, int8_t* out_q, float* out_scale,
+                                     int32_t* out_indices, uint32_t* out_bitmap,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Receiver of 8-bit packet values: out_values[j] = RN(q[j] * scales[s])
+ * for every entry j of segment s (the reading above).  The result feeds
+ * sparse_aggregate_apply like any fp32 packet.
+ *
+ * q          [sum k] int8 codes (device).
+ * scales     [nseg] fp32 per-segment scales (device, 4-byte aligned).
+ * h_seg_k    [nseg] host array of per-segment entry counts (each 0..2^31).
+ * out_values [sum k] fp32 (device, 4-byte aligned); must not overlap q or
+ *            scales.
+ * ---------------------------------------------------------------------- */
+EF_API ef_status ef_q8_dequantize(const int8_t* q, const float* scales, int32_t nseg,
+                                  const int64_t* h_seg_k, float* out_values, void* stream);
+
+/* ------------------------------------------------------------------------
  * 1-bit sign error feedback, sender side.
  *
  * [ONEBIT] §2.1 量化与误差补偿机制:
