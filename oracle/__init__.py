@@ -8,7 +8,14 @@ library or its binding.  See ``ef_oracle.py`` for sources and readings.
 from .ef_oracle import (  # noqa: F401
     abs_key,
     compensate,
+    decode_block256,
+    decode_local16,
+    decode_runvarint,
     decode_signs,
+    encode_block256,
+    encode_local16,
+    encode_runvarint,
+    leb128,
     onebit_momentum,
     pack_bits,
     packet_indices,

@@ -46,6 +46,16 @@ Readings taken where the pages are silent (each repeated where it is used):
 * the receiver adds packets in worker order 0..W-1 starting from +0.0 and
   does not average;
 * (1 - beta1) is formed in float32 before it multiplies;
+* index codecs (the pages name the ideas, not the formats): a packet's
+  ascending int32 index list becomes one byte stream, little-endian --
+  LOCAL16: uint32 block_start[nblk + 1] (entries before each 65536-element
+  block) then each index's uint16 offset in its block; RUNVARINT: for each
+  index the number of unselected elements since the previous one (the first
+  counts from element 0), as LEB128 (7 bits per byte, low group first, high
+  bit set when more bytes follow); BLOCK256: one bit per 256-element block
+  (bit b % 32 of word b // 32, set when the block holds an index), then for
+  each such block in order its entry count - 1 as uint8, then each index's
+  uint8 offset in its block;
 * 8-bit quantisation of a packet's values (the pages give no formula): one
   float32 scale per segment, s = max |v| / 127 over the segment's finite
   selected values (0 if none); q = round-half-even(v / s) clamped to
@@ -292,6 +302,118 @@ def topk_q8_ef_step(g_raw, e, seg_offsets, seg_k, idx_format: str = "int32"):
     out["scales"] = scales
     out["e"] = e_new
     return out
+
+
+# --------------------------------------------------------------------------
+# index codecs  ([SPARSE] §索引编码压缩, §快速上手指南 step 4)
+# --------------------------------------------------------------------------
+
+LOCAL16_BLOCK = 65536
+BLOCK256 = 256
+
+
+def _check_sorted(idx, n):
+    idx = np.asarray(idx, dtype=np.int64)
+    if idx.size and (idx[0] < 0 or idx[-1] >= n or np.any(np.diff(idx) <= 0)):
+        raise ValueError("indices must be strictly ascending and inside [0, n)")
+    return idx
+
+
+def encode_local16(idx, n: int) -> np.ndarray:
+    """16-bit local indices ([SPARSE] §快速上手指南 step 4: indices first go to
+    16-bit integers).  A 16-bit value only reaches 65536 elements, so the
+    index space is cut into blocks of 65536: the stream holds
+    block_start[b] = number of indices below block b, for b = 0 .. nblk
+    (uint32, nblk = ceil(n / 65536)), then each index's offset inside its
+    block (uint16), in packet order."""
+    idx = _check_sorted(idx, n)
+    nblk = (n + LOCAL16_BLOCK - 1) // LOCAL16_BLOCK
+    starts = np.searchsorted(idx, np.arange(nblk + 1, dtype=np.int64) * LOCAL16_BLOCK)
+    low = (idx % LOCAL16_BLOCK).astype("<u2")
+    return np.concatenate([starts.astype("<u4").view(np.uint8), low.view(np.uint8)])
+
+
+def decode_local16(stream, K: int, n: int) -> np.ndarray:
+    nblk = (n + LOCAL16_BLOCK - 1) // LOCAL16_BLOCK
+    b = np.asarray(stream, np.uint8)
+    starts = b[:4 * (nblk + 1)].view("<u4").astype(np.int64)
+    low = b[4 * (nblk + 1):4 * (nblk + 1) + 2 * K].view("<u2").astype(np.int64)
+    blk = np.repeat(np.arange(nblk, dtype=np.int64), np.diff(starts))
+    return (blk * LOCAL16_BLOCK + low).astype(np.int32)
+
+
+def leb128(x: int) -> list:
+    """Unsigned LEB128: 7-bit groups, least significant first, the high bit
+    set on every byte but the last."""
+    out = []
+    while True:
+        byte = x & 0x7F
+        x >>= 7
+        if x:
+            out.append(byte | 0x80)
+        else:
+            out.append(byte)
+            return out
+
+
+def encode_runvarint(idx, n: int) -> np.ndarray:
+    """Run-length / delta coding ([SPARSE] §索引编码压缩: variable-length codes
+    for runs of zeros or index differences): for each index, the number of
+    unselected elements since the previous index (i_j - i_{j-1} - 1, with
+    i_{-1} = -1), written as LEB128."""
+    idx = _check_sorted(idx, n)
+    prev = -1
+    out = []
+    for i in idx.tolist():
+        out.extend(leb128(i - prev - 1))
+        prev = i
+    return np.array(out, dtype=np.uint8)
+
+
+def decode_runvarint(stream, K: int, n: int) -> np.ndarray:
+    b = np.asarray(stream, np.uint8).tolist()
+    idx, pos, prev = [], 0, -1
+    for _ in range(K):
+        x, shift = 0, 0
+        while True:
+            byte = b[pos]
+            pos += 1
+            x |= (byte & 0x7F) << shift
+            shift += 7
+            if not byte & 0x80:
+                break
+        prev = prev + x + 1
+        idx.append(prev)
+    return np.array(idx, dtype=np.int32)
+
+
+def encode_block256(idx, n: int) -> np.ndarray:
+    """Block-sparse index ([SPARSE] §索引编码压缩 按块稀疏): blocks of 256
+    elements; a block without an index costs one flag bit, a block with
+    indices also sends its entry count and each entry's offset inside it.
+    Stream: uint32 flags[ceil(ceil(n / 256) / 32)] (bit b % 32 of word
+    b // 32 for block b), then uint8 (count - 1) for every flagged block in
+    order, then the uint8 offset of every index in packet order."""
+    idx = _check_sorted(idx, n)
+    nb = (n + BLOCK256 - 1) // BLOCK256
+    blk = idx // BLOCK256
+    flags = np.zeros(nb, dtype=bool)
+    flags[blk] = True
+    used, counts = np.unique(blk, return_counts=True)
+    return np.concatenate([pack_bits(flags).astype("<u4").view(np.uint8),
+                           (counts - 1).astype(np.uint8),
+                           (idx % BLOCK256).astype(np.uint8)])
+
+
+def decode_block256(stream, K: int, n: int) -> np.ndarray:
+    nb = (n + BLOCK256 - 1) // BLOCK256
+    nfw = (nb + 31) // 32
+    b = np.asarray(stream, np.uint8)
+    flags = unpack_bits(b[:4 * nfw].view("<u4"), nb)
+    used = np.flatnonzero(flags)
+    counts = b[4 * nfw:4 * nfw + used.size].astype(np.int64) + 1
+    off = b[4 * nfw + used.size:4 * nfw + used.size + K].astype(np.int64)
+    return (np.repeat(used, counts) * BLOCK256 + off).astype(np.int32)
 
 
 # --------------------------------------------------------------------------

@@ -520,6 +520,75 @@ def test_q8_ef_step_residual_identity():
 
 
 # ---------------------------------------------------------------------------
+# index codecs
+# ---------------------------------------------------------------------------
+
+CODECS = {"local16": ("encode_local16", "decode_local16"),
+          "runvarint": ("encode_runvarint", "decode_runvarint"),
+          "block256": ("encode_block256", "decode_block256")}
+
+
+def check_codec_golden(name, encode=None, decode=None):
+    enc = encode or getattr(oracle, CODECS[name][0])
+    dec = decode or getattr(oracle, CODECS[name][1])
+    ex = _load("index_codec_examples.json")[name]
+    b = enc(np.array(ex["indices"], np.int64), ex["n"])
+    assert b.dtype == np.uint8 and b.tolist() == ex["bytes"], name
+    assert dec(np.array(ex["bytes"], np.uint8), len(ex["indices"]), ex["n"]).tolist() == ex["indices"]
+
+
+def check_leb128(leb=None):
+    leb = leb or oracle.leb128
+    fx = _load("index_codec_examples.json")["leb128"]
+    assert leb(fx["value"]) == fx["bytes"]
+    # closed form: ceil(bits / 7) bytes, at least one; each byte's low 7 bits
+    # are the value's 7-bit groups from the least significant up
+    for x in [0, 1, 127, 128, 16383, 16384, 2**21 - 1, 2**21, 2**28, 2**31 - 1]:
+        bs = leb(x)
+        assert len(bs) == max(1, -(-x.bit_length() // 7))
+        assert all(b & 0x80 for b in bs[:-1]) and not bs[-1] & 0x80
+        assert sum((b & 0x7F) << (7 * i) for i, b in enumerate(bs)) == x
+
+
+def test_codec_worked_examples():
+    for name in CODECS:
+        check_codec_golden(name)
+    check_leb128()
+
+
+def _random_index_sets(rng):
+    yield np.zeros(0, np.int64), 1000
+    yield np.array([999], np.int64), 1000
+    yield np.arange(70000, dtype=np.int64), 70000           # every element
+    for _ in range(20):
+        n = int(rng.integers(1, 400_000))
+        k = int(rng.integers(0, min(n, 5000) + 1))
+        yield np.sort(rng.choice(n, k, replace=False)).astype(np.int64), n
+    # clustered: runs of neighbours and long gaps
+    n = 3_000_000
+    starts = np.sort(rng.choice(n - 300, 40, replace=False))
+    yield np.unique(np.concatenate([s + np.arange(int(rng.integers(1, 300))) for s in starts])), n
+
+
+def test_codec_sizes_and_round_trip():
+    """Every codec's stream length follows from its definition in closed
+    form, and decoding gives the packet back."""
+    rng = np.random.default_rng(12)
+    for idx, n in _random_index_sets(rng):
+        K = idx.size
+        nblk = -(-n // 65536)
+        nb = -(-n // 256)
+        runs = np.diff(np.concatenate([[-1], idx])) - 1
+        sizes = {"local16": 4 * (nblk + 1) + 2 * K,
+                 "runvarint": int(sum(max(1, -(-int(r).bit_length() // 7)) for r in runs)),
+                 "block256": 4 * (-(-nb // 32)) + np.unique(idx // 256).size + K}
+        for name, (e, d) in CODECS.items():
+            b = getattr(oracle, e)(idx, n)
+            assert b.size == sizes[name], (name, n, K)
+            assert getattr(oracle, d)(b, K, n).astype(np.int64).tolist() == idx.tolist(), name
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: the pins above must catch them
 # ---------------------------------------------------------------------------
 
@@ -572,6 +641,34 @@ def _sgd_wrong_sign(w, G, eta):
     return (np.asarray(w, F32) + F32(eta) * np.asarray(G, F32)).astype(F32)
 
 
+def _leb128_high_group_first(x):
+    return list(reversed([b & 0x7F for b in oracle.leb128(x)]))
+
+
+def _runvarint_plain_delta(idx, n):
+    prev, out = 0, []
+    for i in np.asarray(idx, np.int64).tolist():
+        out.extend(oracle.leb128(i - prev))
+        prev = i
+    return np.array(out, np.uint8)
+
+
+def _block256_counts_not_minus_one(idx, n):
+    b = oracle.encode_block256(idx, n)
+    nfw = -(-(-(-n // 256)) // 32)
+    nnzb = b.size - 4 * nfw - len(idx)
+    b[4 * nfw:4 * nfw + nnzb] += 1
+    return b
+
+
+def _local16_starts_after_block(idx, n):
+    b = oracle.encode_local16(idx, n)
+    nblk = -(-n // 65536)
+    starts = b[:4 * (nblk + 1)].view("<u4").copy()
+    return np.concatenate([np.append(starts[1:], starts[-1]).astype("<u4").view(np.uint8),
+                           b[4 * (nblk + 1):]])
+
+
 def _q8_round_half_away(values, s):
     v = np.asarray(values, F32)
     q = np.zeros(v.size, np.int8)
@@ -611,6 +708,10 @@ def _q8_step_drops_quantisation_error(g_raw, e, offs, ks, idx_format="int32"):
     (check_q8_golden, {"scale": _q8_scale_over_128}),
     (check_q8_golden, {"scale": _q8_scale_with_inf}),
     (check_q8_ef_golden, {"step": _q8_step_drops_quantisation_error}),
+    (check_leb128, {"leb": _leb128_high_group_first}),
+    (lambda **kw: check_codec_golden("runvarint", **kw), {"encode": _runvarint_plain_delta}),
+    (lambda **kw: check_codec_golden("block256", **kw), {"encode": _block256_counts_not_minus_one}),
+    (lambda **kw: check_codec_golden("local16", **kw), {"encode": _local16_starts_after_block}),
 ])
 def test_pins_catch_planted_mistakes(check, kwargs):
     with pytest.raises(AssertionError):
