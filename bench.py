@@ -727,7 +727,41 @@ def run_next(args, dev):
         "g_elems_per_s": n / ms_q8 / 1e6,
         "cpu_baseline": {"g_elems_per_s": sample / dt / 1e9, "cores": 1, "kind": "oracle",
                          "sample": f"one oracle step on {sample} elements, k = {ksm}"}}
-    del g, e, v, idx, q, sc
+    del g, e, v, q, sc
+
+    # index codecs on the packet of the last top-k call (k ascending indices)
+    codecs = {"local16": efg.CODEC_LOCAL16, "runvarint": efg.CODEC_RUNVARINT,
+              "block256": efg.CODEC_BLOCK256}
+    enc_o = {"local16": oracle.encode_local16, "runvarint": oracle.encode_runvarint,
+             "block256": oracle.encode_block256}
+    idx_sample = np.sort(rng.choice(sample, ksm, replace=False)).astype(np.int64)
+    rows = {}
+    for name, codec in codecs.items():
+        mb, wb = efg.index_codec_sizes(codec, k, n)
+        buf = torch.empty((mb + 3) // 4, dtype=torch.int32, device=dev)
+        ob = torch.zeros(1, dtype=torch.int64, device=dev)
+        wsc = torch.empty(wb, dtype=torch.uint8, device=dev)
+        back = torch.empty(k, dtype=torch.int32, device=dev)
+        ms_enc = timed(lambda: efg.index_encode(codec, idx, n, buf, ob, wsc), 10)
+        nbytes = int(ob.item())
+        ms_dec = timed(lambda: efg.index_decode(codec, buf, nbytes, k, n, back, wsc), 10)
+        ok = bool(torch.equal(back, idx)) and efg.workspace_status(wsc) == 0
+        t0 = time.perf_counter()
+        enc_o[name](idx_sample, sample)
+        dt = time.perf_counter() - t0
+        rows[name] = {
+            "stream_bytes": nbytes, "bytes_per_index": nbytes / k,
+            "ms_encode": ms_enc, "ms_decode": ms_dec,
+            "encode_gbs": (4 * k + nbytes) / (ms_enc * 1e-3) / 1e9,
+            "decode_gbs": (4 * k + nbytes) / (ms_dec * 1e-3) / 1e9,
+            "round_trip_exact": ok,
+            "cpu_baseline": {"indices_per_s": ksm / dt, "cores": 1, "kind": "oracle",
+                             "sample": f"oracle encode of {ksm} indices from {sample}"}}
+        del buf, ob, wsc, back
+    out["index_codecs"] = {"workload": f"the int32 packet of one tensor of {n} elements, "
+                                       f"k = {k} (4 bytes per index as int32)",
+                           "codecs": rows}
+    del idx
     torch.cuda.empty_cache()
     return out
 

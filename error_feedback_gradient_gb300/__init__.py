@@ -8,11 +8,17 @@ inputs.
 """
 
 from .binding import (  # noqa: F401
+    CODEC_BLOCK256,
+    CODEC_LOCAL16,
+    CODEC_RUNVARINT,
     EFError,
     IDX_BITMAP,
     IDX_INT32,
     APPLY_MOMENTUM,
     APPLY_SGD,
+    index_codec_sizes,
+    index_decode,
+    index_encode,
     kernel_launches,
     library,
     library_path,

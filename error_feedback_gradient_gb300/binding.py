@@ -69,6 +69,15 @@ _SIGNATURES = {
         ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "ef_q8_dequantize": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int32, _c_i64p, _c_vp, _c_vp]),
+    "ef_index_codec_sizes": (ctypes.c_int32, [
+        ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t),
+        ctypes.POINTER(ctypes.c_size_t)]),
+    "ef_index_encode": (ctypes.c_int32, [
+        ctypes.c_int32, _c_vp, ctypes.c_int64, ctypes.c_int64, _c_vp, ctypes.c_size_t, _c_vp,
+        _c_vp, ctypes.c_size_t, _c_vp]),
+    "ef_index_decode": (ctypes.c_int32, [
+        ctypes.c_int32, _c_vp, ctypes.c_size_t, ctypes.c_int64, ctypes.c_int64, _c_vp, _c_vp,
+        ctypes.c_size_t, _c_vp]),
     "ef_sign_compress": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_float, _c_vp, _c_vp]),
     "ef_aggregate_workspace_size": (ctypes.c_int32, [
@@ -225,6 +234,43 @@ def q8_dequantize(q: torch.Tensor, scales: torch.Tensor, seg_k: Sequence[int],
     _check(library().ef_q8_dequantize(
         _ptr(q), _ptr(scales), len(seg_k), _i64(seg_k), _ptr(out_values),
         _stream(stream)), "ef_q8_dequantize")
+
+
+# ---------------------------------------------------------------------------
+# index codecs
+# ---------------------------------------------------------------------------
+
+CODEC_LOCAL16 = 1
+CODEC_RUNVARINT = 2
+CODEC_BLOCK256 = 3
+
+
+def index_codec_sizes(codec: int, K: int, n: int):
+    """(upper bound of the stream's bytes, workspace bytes) for K indices of n."""
+    mb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(library().ef_index_codec_sizes(int(codec), int(K), int(n), ctypes.byref(mb),
+                                          ctypes.byref(wb)), "ef_index_codec_sizes")
+    return int(mb.value), int(wb.value)
+
+
+def index_encode(codec: int, indices: torch.Tensor, n: int, out: torch.Tensor,
+                 out_bytes: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """ef_index_encode: int32 indices -> byte stream in ``out``; its length
+    lands in ``out_bytes`` (one int64 on the device)."""
+    _check(library().ef_index_encode(
+        int(codec), _ptr(indices), indices.numel(), int(n), _ptr(out),
+        out.numel() * out.element_size(), _ptr(out_bytes), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "ef_index_encode")
+
+
+def index_decode(codec: int, stream_bytes: torch.Tensor, nbytes: int, K: int, n: int,
+                 indices: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """ef_index_decode: the first ``nbytes`` bytes of ``stream_bytes`` -> K
+    int32 indices."""
+    _check(library().ef_index_decode(
+        int(codec), _ptr(stream_bytes), int(nbytes), int(K), int(n), _ptr(indices),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "ef_index_decode")
 
 
 # ---------------------------------------------------------------------------

@@ -217,6 +217,60 @@ EF_API ef_status ef_q8_dequantize(const int8_t* q, const float* scales, int32_t 
                                   const int64_t* h_seg_k, float* out_values, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Index codecs for top-k packets.
+ *
+ * [SPARSE] §索引编码压缩 (block-sparse index: a dropped block costs one flag
+ * bit, a kept block sends its inner indices; run-length and delta codes of
+ * variable length) and §快速上手指南 step 4 (indices first as 16-bit
+ * integers).  The page gives no formats; these are the library's readings.
+ * Each codec maps an ascending int32 index list of K entries from [0, n)
+ * (n <= 2^31) to one little-endian byte stream and back:
+ *   EF_CODEC_LOCAL16    uint32 block_start[nblk + 1] (entries before each
+ *                       65536-element block, nblk = ceil(n / 65536)), then
+ *                       each entry's uint16 offset in its block.
+ *                       Size 4 * (nblk + 1) + 2 * K.
+ *   EF_CODEC_RUNVARINT  per entry, the number of unselected elements since
+ *                       the previous entry (i_j - i_{j-1} - 1, i_{-1} = -1)
+ *                       as unsigned LEB128 (7-bit groups, low first, the
+ *                       high bit set on all but the last byte).  At most
+ *                       5 * K bytes.
+ *   EF_CODEC_BLOCK256   uint32 flags[nfw] (bit b % 32 of word b / 32 set when
+ *                       256-element block b holds an entry; nfw =
+ *                       ceil(ceil(n / 256) / 32)), then uint8 (count - 1)
+ *                       of every flagged block in order, then each entry's
+ *                       uint8 offset in its block.  Size 4 * nfw + (flagged
+ *                       blocks) + K, at most 4 * nfw + 2 * K.
+ *
+ * ef_index_codec_sizes   upper bound of a stream's bytes and the workspace
+ *                        bytes (for encode and decode) for K, n.
+ * ef_index_encode        indices [K] int32 (device, 4-byte aligned) ->
+ *                        out [out_capacity >= max bytes] (device, 4-byte
+ *                        aligned); the stream's length is written to
+ *                        *d_out_bytes (device uint64, 8-byte aligned), so
+ *                        no host synchronisation is needed.
+ * ef_index_decode        in [in_bytes] (device, 4-byte aligned; in_bytes is
+ *                        the encoded length) -> indices [K] (device).
+ *                        A length the format cannot have returns
+ *                        EF_ERR_PACKET at once.
+ * workspace: >= workspace_bytes, 256-byte aligned, not overlapping the
+ * buffers.  Unsorted or out-of-range indices, and streams that do not parse
+ * into K valid indices, set EF_ERR_PACKET in the workspace status word
+ * (read it with ef_workspace_status); nothing is ever read or written out
+ * of bounds.
+ * ---------------------------------------------------------------------- */
+#define EF_CODEC_LOCAL16 1
+#define EF_CODEC_RUNVARINT 2
+#define EF_CODEC_BLOCK256 3
+EF_API ef_status ef_index_codec_sizes(int32_t codec, int64_t K, int64_t n,
+                                      size_t* max_stream_bytes, size_t* workspace_bytes);
+EF_API ef_status ef_index_encode(int32_t codec, const int32_t* indices, int64_t K, int64_t n,
+                                 uint8_t* out, size_t out_capacity, uint64_t* d_out_bytes,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+EF_API ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in_bytes, int64_t K,
+                                 int64_t n, int32_t* indices, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * 1-bit sign error feedback, sender side.
  *
  * [ONEBIT] §2.1 量化与误差补偿机制:
