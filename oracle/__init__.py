@@ -19,9 +19,14 @@ from .ef_oracle import (  # noqa: F401
     onebit_momentum,
     pack_bits,
     packet_indices,
+    philox4x32_10,
     q8_dequantize,
     q8_quantize,
     q8_scale,
+    randk_ef_step,
+    randk_keep,
+    randk_scale,
+    randk_words,
     sgd_apply,
     sign_aggregate,
     sign_ef_step,

@@ -56,6 +56,18 @@ Readings taken where the pages are silent (each repeated where it is used):
   (bit b % 32 of word b // 32, set when the block holds an index), then for
   each such block in order its entry count - 1 as uint8, then each index's
   uint8 offset in its block;
+* random magnitude-proportional sparsification ([SPARSE] §随机稀疏化): keep
+  element i with probability p_i = min(1, k |g_i| / S), S = the exact sum
+  of |g| over the segment's finite elements rounded once to float64 (the
+  pages normalise once so that the p_i add up to k; where k |g_i| / S > 1
+  the element is kept surely, so the expected count falls short of k by the
+  clipped excess); non-finite elements are kept surely; S = 0 keeps
+  nothing; the draw for element i is u_i = w / 2^32 with w word i % 4 of
+  Philox4x32-10 (counter (i // 4 low, high word, step low, high word),
+  key (seed low, high word)), kept iff u_i < p_i in float64; kept values
+  are sent as they are (no 1/p scaling: the residual carries the rest), in
+  ascending index order, and a packet stops at its capacity (later kept
+  elements stay in the residual);
 * 8-bit quantisation of a packet's values (the pages give no formula): one
   float32 scale per segment, s = max |v| / 127 over the segment's finite
   selected values (0 if none); q = round-half-even(v / s) clamped to
@@ -414,6 +426,101 @@ def decode_block256(stream, K: int, n: int) -> np.ndarray:
     counts = b[4 * nfw:4 * nfw + used.size].astype(np.int64) + 1
     off = b[4 * nfw + used.size:4 * nfw + used.size + K].astype(np.int64)
     return (np.repeat(used, counts) * BLOCK256 + off).astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# random magnitude-proportional sparsification  ([SPARSE] §随机稀疏化)
+# --------------------------------------------------------------------------
+
+PHILOX_M = (0xD2511F53, 0xCD9E8D57)
+PHILOX_W = (0x9E3779B9, 0xBB67AE85)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel
+    random numbers: as easy as 1, 2, 3", SC 2011): each round multiplies
+    two counter words by the constants M0, M1, mixes the high halves with
+    the other two words and the key, and the key is bumped by the Weyl
+    constants W0, W1 between rounds.  Works elementwise on numpy arrays of
+    32-bit words (held in uint64); returns the four output words."""
+    m = np.uint64(0xFFFFFFFF)
+    c0, c1, c2, c3 = (np.asarray(x, np.uint64) & m for x in (c0, c1, c2, c3))
+    k0, k1 = (np.asarray(x, np.uint64) & m for x in (k0, k1))
+    for _ in range(10):
+        p0 = np.uint64(PHILOX_M[0]) * c0
+        p1 = np.uint64(PHILOX_M[1]) * c2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & m
+        hi1, lo1 = p1 >> np.uint64(32), p1 & m
+        c0, c1, c2, c3 = (hi1 ^ c1 ^ k0) & m, lo1, (hi0 ^ c3 ^ k1) & m, lo0
+        k0 = (k0 + np.uint64(PHILOX_W[0])) & m
+        k1 = (k1 + np.uint64(PHILOX_W[1])) & m
+    return c0, c1, c2, c3
+
+
+def randk_words(first: int, count: int, seed: int, step: int) -> np.ndarray:
+    """The 32-bit random word of elements first .. first + count - 1: word
+    i % 4 of Philox4x32-10 at counter (i // 4 low, i // 4 high, step low,
+    step high) and key (seed low, seed high)."""
+    i = np.arange(first, first + count, dtype=np.uint64)
+    q = i >> np.uint64(2)
+    out = philox4x32_10(q & np.uint64(0xFFFFFFFF), q >> np.uint64(32),
+                        np.uint64(step & 0xFFFFFFFF), np.uint64(step >> 32),
+                        np.uint64(seed & 0xFFFFFFFF), np.uint64(seed >> 32))
+    words = np.stack(out)                       # 4 x count
+    return words[(i & np.uint64(3)).astype(np.int64), np.arange(count)].astype(U32)
+
+
+def randk_scale(g_segment) -> float:
+    """S = sum of |g| over the finite elements, exact, rounded once to
+    float64 (math.fsum returns the correctly rounded sum)."""
+    import math
+    a = np.abs(np.asarray(g_segment, F32))
+    return math.fsum(a[np.isfinite(a)].astype(np.float64).tolist())
+
+
+def randk_keep(g_segment, k: int, first: int, seed: int, step: int) -> np.ndarray:
+    """Keep flags of one segment starting at global element ``first``:
+    p = min(1, c |g|) with c = k / S in float64 (1 for non-finite, 0 when
+    S = 0); kept iff u < p, u = randk_words / 2^32."""
+    g = np.asarray(g_segment, F32)
+    S = randk_scale(g)
+    c = float(k) / S if S > 0 else 0.0
+    a = np.abs(g).astype(np.float64)
+    fin = np.isfinite(a)
+    p = np.ones(g.size, np.float64)
+    p[fin] = np.minimum(1.0, c * a[fin])
+    u = randk_words(first, g.size, seed, step).astype(np.float64) * 2.0 ** -32
+    return u < p
+
+
+def randk_ef_step(g_raw, e, seg_offsets, seg_k, seed: int, step: int, capacity: int):
+    """One error-feedback step with random magnitude-proportional
+    sparsification ([SPARSE] §随机稀疏化 in place of step 3 of §详细算法流程):
+    g = g_raw + e; each segment keeps elements with probability
+    proportional to |g| (randk_keep, expected count k_s up to clipping);
+    the kept values go out unscaled with their global indices, ascending;
+    e = g - g~.  A packet holds at most ``capacity`` entries: kept elements
+    past it are not sent and keep g in the residual.
+
+    Returns ``values``, ``indices`` (int32), ``e``, ``counts`` (entries sent
+    per segment) and ``kept`` (elements kept before the capacity cut)."""
+    g_raw = np.ascontiguousarray(g_raw, dtype=F32)
+    g = compensate(g_raw, e)
+    offs = [int(x) for x in seg_offsets]
+    ks = [int(x) for x in seg_k]
+    keep = np.zeros(g.size, bool)
+    for s_i, k in enumerate(ks):
+        a, b = offs[s_i], offs[s_i + 1]
+        if k > 0 and b > a:
+            keep[a:b] = randk_keep(g[a:b], k, a, seed, step)
+    kept = np.flatnonzero(keep)
+    sent = kept[:capacity]
+    e_new = g.copy()
+    e_new[sent] = F32(0.0)
+    seg_of = np.searchsorted(np.array(offs[1:]), sent, side="right")
+    counts = np.bincount(seg_of, minlength=len(ks)).astype(np.int64)
+    return {"values": g[sent].copy(), "indices": sent.astype(np.int32), "e": e_new,
+            "counts": counts, "kept": int(kept.size)}
 
 
 # --------------------------------------------------------------------------

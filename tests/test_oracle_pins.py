@@ -589,6 +589,84 @@ def test_codec_sizes_and_round_trip():
 
 
 # ---------------------------------------------------------------------------
+# random magnitude-proportional sparsification
+# ---------------------------------------------------------------------------
+
+
+def check_philox_kat(philox=None):
+    philox = philox or oracle.philox4x32_10
+    for v in _load("randk_examples.json")["philox_kat"]:
+        c = [int(x, 16) for x in v["ctr"]]
+        k = [int(x, 16) for x in v["key"]]
+        out = philox(*c, *k)
+        assert ["%08x" % int(x) for x in out] == v["out"]
+
+
+def check_randk_golden(step_fn=None):
+    step_fn = step_fn or oracle.randk_ef_step
+    for name in ("step", "step2"):
+        fx = _load("randk_examples.json")[name]
+        out = step_fn(_arr(fx["g_raw"]), np.zeros(4, F32), [0, 4], [fx["k"]], fx["seed"],
+                      fx["step"], 10)
+        assert out["values"].tolist() == fx["values"], name
+        assert out["indices"].tolist() == fx["indices"], name
+        assert out["e"].tolist() == fx["e"], name
+
+
+def test_randk_worked_example_and_generator():
+    check_philox_kat()
+    check_randk_golden()
+    # words of elements 4..7 come from counter 1: its first word differs
+    w = oracle.randk_words(0, 8, 0, 0)
+    assert ["%08x" % x for x in w[:4]] == _load("randk_examples.json")["philox_kat"][0]["out"]
+    assert w[4] != w[0]
+
+
+def test_randk_scale_is_the_exact_sum():
+    """S equals the exact rational sum of the |g| (fractions), rounded once
+    to float64 by Python's correctly rounded conversion."""
+    rng = np.random.default_rng(21)
+    for trial in range(30):
+        n = int(rng.integers(1, 3000))
+        g = (rng.standard_t(2, n) * 10.0 ** rng.uniform(-30, 30, n)).astype(F32)
+        g[rng.integers(0, n, 3)] = np.float32("nan")
+        fin = g[np.isfinite(g)]
+        exact = sum((Fraction(float(abs(x))) for x in fin), Fraction(0))
+        assert oracle.randk_scale(g) == float(exact)
+
+
+def test_randk_keep_statistics():
+    """Over many seeds the kept count averages k (no element is clipped
+    here) and each element's keep frequency is p_i = k |g_i| / S."""
+    rng = np.random.default_rng(8)
+    n, k = 400, 40
+    g = (rng.standard_normal(n) * 1e-3).astype(F32)
+    p = k * np.abs(g).astype(np.float64) / oracle.randk_scale(g)
+    assert p.max() < 1
+    trials = 2000
+    freq = np.zeros(n)
+    counts = []
+    for t in range(trials):
+        keep = oracle.randk_keep(g, k, 0, seed=1234, step=t)
+        freq += keep
+        counts.append(keep.sum())
+    assert abs(np.mean(counts) - k) < 4 * np.sqrt(np.sum(p * (1 - p)) / trials)
+    z = (freq / trials - p) / np.sqrt(p * (1 - p) / trials)
+    assert np.max(np.abs(z)) < 5.5
+
+
+def test_randk_special_cases():
+    g = np.array([0, 0, 0, 0, 0], F32)
+    assert not oracle.randk_keep(g, 3, 0, 1, 1).any()                     # S = 0
+    g = np.array([1e30, 1e-3, np.inf, np.nan, 1e-3], F32)
+    keep = oracle.randk_keep(g, 2, 0, 5, 6)
+    assert keep[0] and keep[2] and keep[3]            # clipped to 1, and the non-finite
+    out = oracle.randk_ef_step(np.ones(1000, F32), np.zeros(1000, F32), [0, 1000], [1000], 9, 9, 7)
+    assert out["kept"] == 1000 and out["indices"].tolist() == list(range(7))   # capacity cut
+    assert np.all(out["e"][7:] == 1) and np.all(out["e"][:7] == 0)
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: the pins above must catch them
 # ---------------------------------------------------------------------------
 
@@ -669,6 +747,33 @@ def _local16_starts_after_block(idx, n):
                            b[4 * (nblk + 1):]])
 
 
+def _philox_key_bumped_first(c0, c1, c2, c3, k0, k1):
+    return ef_oracle.philox4x32_10(c0, c1, c2, c3, (k0 + 0x9E3779B9) & 0xFFFFFFFF,
+                                   (k1 + 0xBB67AE85) & 0xFFFFFFFF)
+
+
+def _randk_scaled_by_inverse_p(g_raw, e, offs, ks, seed, step, capacity):
+    out = oracle.randk_ef_step(g_raw, e, offs, ks, seed, step, capacity)
+    g = oracle.compensate(g_raw, e)
+    S = oracle.randk_scale(g)
+    p = np.minimum(1.0, ks[0] * np.abs(g[out["indices"]]).astype(np.float64) / S)
+    out["values"] = (out["values"] / p).astype(F32)
+    return out
+
+
+def _randk_uses_element_index_as_counter(g_raw, e, offs, ks, seed, step, capacity):
+    g = oracle.compensate(g_raw, e)
+    S = oracle.randk_scale(g)
+    c = ks[0] / S
+    i = np.arange(g.size)
+    u = np.array([int(oracle.philox4x32_10(x, 0, step, 0, seed, 0)[0]) for x in i]) * 2.0 ** -32
+    keep = u < np.minimum(1.0, c * np.abs(g).astype(np.float64))
+    sel = np.flatnonzero(keep)[:capacity]
+    e2 = g.copy()
+    e2[sel] = 0
+    return {"values": g[sel], "indices": sel.astype(np.int32), "e": e2}
+
+
 def _q8_round_half_away(values, s):
     v = np.asarray(values, F32)
     q = np.zeros(v.size, np.int8)
@@ -709,6 +814,9 @@ def _q8_step_drops_quantisation_error(g_raw, e, offs, ks, idx_format="int32"):
     (check_q8_golden, {"scale": _q8_scale_with_inf}),
     (check_q8_ef_golden, {"step": _q8_step_drops_quantisation_error}),
     (check_leb128, {"leb": _leb128_high_group_first}),
+    (check_philox_kat, {"philox": _philox_key_bumped_first}),
+    (check_randk_golden, {"step_fn": _randk_scaled_by_inverse_p}),
+    (check_randk_golden, {"step_fn": _randk_uses_element_index_as_counter}),
     (lambda **kw: check_codec_golden("runvarint", **kw), {"encode": _runvarint_plain_delta}),
     (lambda **kw: check_codec_golden("block256", **kw), {"encode": _block256_counts_not_minus_one}),
     (lambda **kw: check_codec_golden("local16", **kw), {"encode": _local16_starts_after_block}),
