@@ -23,6 +23,7 @@ from .ef_oracle import (  # noqa: F401
     q8_dequantize,
     q8_quantize,
     q8_scale,
+    randk_coefficient,
     randk_ef_step,
     randk_keep,
     randk_scale,

@@ -57,17 +57,19 @@ Readings taken where the pages are silent (each repeated where it is used):
   each such block in order its entry count - 1 as uint8, then each index's
   uint8 offset in its block;
 * random magnitude-proportional sparsification ([SPARSE] §随机稀疏化): keep
-  element i with probability p_i = min(1, k |g_i| / S), S = the exact sum
-  of |g| over the segment's finite elements rounded once to float64 (the
-  pages normalise once so that the p_i add up to k; where k |g_i| / S > 1
-  the element is kept surely, so the expected count falls short of k by the
-  clipped excess); non-finite elements are kept surely; S = 0 keeps
-  nothing; the draw for element i is u_i = w / 2^32 with w word i % 4 of
-  Philox4x32-10 (counter (i // 4 low, high word, step low, high word),
-  key (seed low, high word)), kept iff u_i < p_i in float64; kept values
-  are sent as they are (no 1/p scaling: the residual carries the rest), in
-  ascending index order, and a packet stops at its capacity (later kept
-  elements stay in the residual);
+  element i with probability p_i = min(1, c |g_i|), c = k / S, S = the
+  exact sum of |g| over the segment's finite elements rounded once to
+  float64 (the pages normalise once so that the p_i add up to k; where
+  c |g_i| > 1 the element is kept surely, so the expected count falls short
+  of k by the clipped excess).  The per-element arithmetic is float32, the
+  gradients' precision: c is rounded to float32 once, p_i = min(1,
+  RN(c |g_i|)), and the draw u_i = (w >> 8) / 2^24 (exact in float32) with
+  w word i % 4 of Philox4x32-10 (counter (i // 4 low, high word, step low,
+  high word), key (seed low, high word)); kept iff u_i < p_i.  Non-finite
+  elements are kept surely; S = 0 keeps nothing; kept values are sent as
+  they are (no 1/p scaling: the residual carries the rest), in ascending
+  index order, and a packet stops at its capacity (later kept elements
+  stay in the residual);
 * 8-bit quantisation of a packet's values (the pages give no formula): one
   float32 scale per segment, s = max |v| / 127 over the segment's finite
   selected values (0 if none); q = round-half-even(v / s) clamped to
@@ -478,18 +480,24 @@ def randk_scale(g_segment) -> float:
     return math.fsum(a[np.isfinite(a)].astype(np.float64).tolist())
 
 
+def randk_coefficient(g_segment, k: int) -> np.float32:
+    """c = k / S (float64 division) rounded once to float32; 0 when S = 0."""
+    S = randk_scale(g_segment)
+    return np.float32(float(k) / S) if S > 0 else np.float32(0.0)
+
+
 def randk_keep(g_segment, k: int, first: int, seed: int, step: int) -> np.ndarray:
-    """Keep flags of one segment starting at global element ``first``:
-    p = min(1, c |g|) with c = k / S in float64 (1 for non-finite, 0 when
-    S = 0); kept iff u < p, u = randk_words / 2^32."""
+    """Keep flags of one segment starting at global element ``first``, in
+    float32: p = min(1, RN(c |g|)) (1 for non-finite elements); kept iff
+    u < p with u = (randk_words >> 8) / 2^24."""
     g = np.asarray(g_segment, F32)
-    S = randk_scale(g)
-    c = float(k) / S if S > 0 else 0.0
-    a = np.abs(g).astype(np.float64)
+    c = randk_coefficient(g, k)
+    a = np.abs(g)
     fin = np.isfinite(a)
-    p = np.ones(g.size, np.float64)
-    p[fin] = np.minimum(1.0, c * a[fin])
-    u = randk_words(first, g.size, seed, step).astype(np.float64) * 2.0 ** -32
+    p = np.ones(g.size, F32)
+    with np.errstate(over="ignore"):
+        p[fin] = np.minimum(F32(1.0), np.multiply(c, a[fin], dtype=F32))
+    u = (randk_words(first, g.size, seed, step) >> U32(8)).astype(F32) * F32(2.0 ** -24)
     return u < p
 
 

@@ -641,7 +641,8 @@ def test_randk_keep_statistics():
     rng = np.random.default_rng(8)
     n, k = 400, 40
     g = (rng.standard_normal(n) * 1e-3).astype(F32)
-    p = k * np.abs(g).astype(np.float64) / oracle.randk_scale(g)
+    p = np.abs(g).astype(np.float64) * float(oracle.randk_coefficient(g, k))
+    assert abs(p.sum() - k) < 1e-4 * k
     assert p.max() < 1
     trials = 2000
     freq = np.zeros(n)
@@ -755,19 +756,19 @@ def _philox_key_bumped_first(c0, c1, c2, c3, k0, k1):
 def _randk_scaled_by_inverse_p(g_raw, e, offs, ks, seed, step, capacity):
     out = oracle.randk_ef_step(g_raw, e, offs, ks, seed, step, capacity)
     g = oracle.compensate(g_raw, e)
-    S = oracle.randk_scale(g)
-    p = np.minimum(1.0, ks[0] * np.abs(g[out["indices"]]).astype(np.float64) / S)
+    c = oracle.randk_coefficient(g, ks[0])
+    p = np.minimum(F32(1), c * np.abs(g[out["indices"]]))
     out["values"] = (out["values"] / p).astype(F32)
     return out
 
 
 def _randk_uses_element_index_as_counter(g_raw, e, offs, ks, seed, step, capacity):
     g = oracle.compensate(g_raw, e)
-    S = oracle.randk_scale(g)
-    c = ks[0] / S
+    c = oracle.randk_coefficient(g, ks[0])
     i = np.arange(g.size)
-    u = np.array([int(oracle.philox4x32_10(x, 0, step, 0, seed, 0)[0]) for x in i]) * 2.0 ** -32
-    keep = u < np.minimum(1.0, c * np.abs(g).astype(np.float64))
+    w = np.array([int(oracle.philox4x32_10(x, 0, step, 0, seed, 0)[0]) for x in i], np.uint32)
+    u = (w >> np.uint32(8)).astype(F32) * F32(2.0 ** -24)
+    keep = u < np.minimum(F32(1), c * np.abs(g))
     sel = np.flatnonzero(keep)[:capacity]
     e2 = g.copy()
     e2[sel] = 0
