@@ -496,7 +496,7 @@ def randk_keep(g_segment, k: int, first: int, seed: int, step: int) -> np.ndarra
     fin = np.isfinite(a)
     p = np.ones(g.size, F32)
     with np.errstate(over="ignore"):
-        p[fin] = np.minimum(F32(1.0), np.multiply(c, a[fin], dtype=F32))
+        p[fin] = np.fmin(F32(1.0), np.multiply(c, a[fin], dtype=F32))   # NaN -> 1
     u = (randk_words(first, g.size, seed, step) >> U32(8)).astype(F32) * F32(2.0 ** -24)
     return u < p
 
