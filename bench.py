@@ -763,6 +763,39 @@ def run_next(args, dev):
                            "codecs": rows}
     del idx
     torch.cuda.empty_cache()
+
+    # random magnitude-proportional sparsification (expected k)
+    g = wl.student_t3(n, 1e-3, wl.seed(5, 0, 1), dev)
+    e = torch.zeros_like(g)
+    cap = 2 * k
+    v = torch.empty(cap, device=dev)
+    ix = torch.empty(cap, dtype=torch.int32, device=dev)
+    cnt = torch.empty(2, dtype=torch.int64, device=dev)
+    wsr = torch.empty(efg.randk_workspace_size(n, offs, ks), dtype=torch.uint8, device=dev)
+    stepno = [0]
+
+    def rk():
+        stepno[0] += 1
+        efg.randk_compress(g, e, offs, ks, 2024, stepno[0], v, ix, cnt, wsr)
+    ms_rk = timed(rk, 5)
+    kept = int(cnt[-1].item())
+    rk_bytes = 16 * n + 8 * kept
+    gs2 = (rng.standard_t(3, sample) * 1e-3).astype(np.float32)
+    t0 = time.perf_counter()
+    oracle.randk_ef_step(gs2, np.zeros(sample, np.float32), [0, sample], [ksm], 1, 1, 2 * ksm)
+    dt = time.perf_counter() - t0
+    out["random_sparsification"] = {
+        "workload": f"one tensor of {n} elements, expected k = {k}",
+        "ms_per_call": ms_rk, "kept_last_call": kept,
+        "algorithmic_bytes": rk_bytes,
+        "note": "two passes: 12 B/element (compensate + exact sum of |g|) and 4 B/element "
+                "(draws + ordered packet) + 8 B per kept element",
+        "gbs": rk_bytes / (ms_rk * 1e-3) / 1e9,
+        "g_elems_per_s": n / ms_rk / 1e6,
+        "cpu_baseline": {"g_elems_per_s": sample / dt / 1e9, "cores": 1, "kind": "oracle",
+                         "sample": f"one oracle step on {sample} elements, k = {ksm}"}}
+    del g, e, v, ix, cnt, wsr
+    torch.cuda.empty_cache()
     return out
 
 

@@ -22,6 +22,8 @@ from .binding import (  # noqa: F401
     kernel_launches,
     library,
     library_path,
+    randk_compress,
+    randk_workspace_size,
     sign_aggregate_apply,
     sign_compress,
     sparse_aggregate_apply,

@@ -78,6 +78,11 @@ _SIGNATURES = {
     "ef_index_decode": (ctypes.c_int32, [
         ctypes.c_int32, _c_vp, ctypes.c_size_t, ctypes.c_int64, ctypes.c_int64, _c_vp, _c_vp,
         ctypes.c_size_t, _c_vp]),
+    "ef_randk_workspace_size": (ctypes.c_int32, [
+        ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p, ctypes.POINTER(ctypes.c_size_t)]),
+    "ef_randk_compress": (ctypes.c_int32, [
+        _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p, ctypes.c_uint64,
+        ctypes.c_uint64, _c_vp, _c_vp, ctypes.c_int64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "ef_sign_compress": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_float, _c_vp, _c_vp]),
     "ef_aggregate_workspace_size": (ctypes.c_int32, [
@@ -234,6 +239,37 @@ def q8_dequantize(q: torch.Tensor, scales: torch.Tensor, seg_k: Sequence[int],
     _check(library().ef_q8_dequantize(
         _ptr(q), _ptr(scales), len(seg_k), _i64(seg_k), _ptr(out_values),
         _stream(stream)), "ef_q8_dequantize")
+
+
+# ---------------------------------------------------------------------------
+# random magnitude-proportional sparsification
+# ---------------------------------------------------------------------------
+
+
+def randk_workspace_size(n: int, seg_offsets: Sequence[int], seg_k: Sequence[int]) -> int:
+    out = ctypes.c_size_t(0)
+    _check(library().ef_randk_workspace_size(int(n), len(seg_k), _i64(seg_offsets),
+                                             _i64(seg_k), ctypes.byref(out)),
+           "ef_randk_workspace_size")
+    return int(out.value)
+
+
+def randk_compress(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Sequence[int],
+                   seg_k: Sequence[int], seed: int, step: int, out_values: torch.Tensor,
+                   out_indices: torch.Tensor, counts: torch.Tensor,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """ef_randk_compress: keep-with-probability-proportional-to-|g| EF step;
+    ``counts`` (int64 [nseg + 1], device) receives the entries sent per
+    segment and their total."""
+    n = g_raw.numel()
+    if workspace is None:
+        workspace = torch.empty(randk_workspace_size(n, seg_offsets, seg_k), dtype=torch.uint8,
+                                device=g_raw.device)
+    _check(library().ef_randk_compress(
+        _ptr(g_raw), _ptr(e), n, len(seg_k), _i64(seg_offsets), _i64(seg_k),
+        int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_values), _ptr(out_indices),
+        out_values.numel(), _ptr(counts), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "ef_randk_compress")
 
 
 # ---------------------------------------------------------------------------

@@ -128,6 +128,7 @@ const char* ef_status_string(ef_status s) {
     case EF_ERR_DEVICE_TIMEOUT: return "device-side bounded wait ran out";
     case EF_ERR_PACKET: return "malformed packet (unsorted, out of range or wrong count)";
     case EF_ERR_INTERNAL: return "device-side consistency check failed";
+    case EF_ERR_CAPACITY: return "more elements kept than the packet holds";
     default: return "unknown status";
   }
 }

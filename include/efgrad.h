@@ -69,6 +69,9 @@ typedef int32_t ef_status;
                                      differs from the stated k                         */
 #define EF_ERR_INTERNAL       14  /* device-side: a consistency check failed (a library
                                      defect); the offending write was skipped           */
+#define EF_ERR_CAPACITY       15  /* device-side: more elements were kept than the packet
+                                     holds; the packet stops at its capacity and the
+                                     rest stay in the residual                          */
 
 #define EF_IDX_INT32   0  /* packet = fp32 values[k] + int32 global indices[k]        */
 #define EF_IDX_BITMAP  1  /* packet = fp32 values[k] + uint32 bitmap[ceil(n/32)]      */
@@ -269,6 +272,45 @@ EF_API ef_status ef_index_encode(int32_t codec, const int32_t* indices, int64_t 
 EF_API ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in_bytes, int64_t K,
                                  int64_t n, int32_t* indices, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Random magnitude-proportional sparsification with error feedback.
+ *
+ * [SPARSE] §随机稀疏化: each element is kept with probability proportional to
+ * |g|, normalised so that the expected count is k (in place of the top-k
+ * selection of §详细算法流程 step 3; steps 2, 4 and 5 as ef_topk_compress).
+ * The page gives no formula; the reading here, per segment:
+ *   g = RN(g_raw + e), written over e;
+ *   S = the exact sum of |g| over the finite elements, rounded once to fp64;
+ *   c = RN32(k / S), 0 when S = 0;
+ *   p_i = fmin(1, RN32(c * |g_i|)), 1 for Inf / NaN;
+ *   u_i = (w_i >> 8) * 2^-24, w_i = word (i mod 4) of Philox4x32-10 at
+ *         counter (i/4 low 32 bits, i/4 high, step low, step high) and key
+ *         (seed low, seed high), i the global element index;
+ *   kept iff u_i < p_i (segments with k = 0 keep nothing).  Where c|g_i| > 1
+ *   the element is kept surely, so the expected count falls short of k by
+ *   the clipped excess.
+ * Kept elements are sent unscaled, in ascending global index order across
+ * segments: out_values[j] = g_i, out_indices[j] = i, for the first
+ * `capacity` kept elements; e = +0 where sent and g elsewhere (a kept
+ * element past the capacity is not sent and keeps g; the device status
+ * word then reads EF_ERR_CAPACITY).
+ *
+ * n            <= 2^31 (int32 indices); segments as ef_topk_compress.
+ * seed, step   the generator's key and the counter's upper half.
+ * out_values   [capacity] fp32, out_indices [capacity] int32 (device).
+ * d_counts     [nseg + 1] int64 (device, 8-byte aligned): entries sent per
+ *              segment, then their total (the packet length).
+ * workspace    >= ef_randk_workspace_size() bytes, 256-byte aligned.
+ * No buffer may overlap another.
+ * ---------------------------------------------------------------------- */
+EF_API ef_status ef_randk_workspace_size(int64_t n, int32_t nseg, const int64_t* h_seg_offsets,
+                                         const int64_t* h_seg_k, size_t* bytes);
+EF_API ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, int32_t nseg,
+                                   const int64_t* h_seg_offsets, const int64_t* h_seg_k,
+                                   uint64_t seed, uint64_t step, float* out_values,
+                                   int32_t* out_indices, int64_t capacity, int64_t* d_counts,
+                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * 1-bit sign error feedback, sender side.
