@@ -84,7 +84,29 @@ __device__ __forceinline__ void acc_clear(Acc& a) {
   for (int q = 0; q < 4; ++q) a.lo[q] = a.hi[q] = 0;
 }
 
-// Adds |x| given as its bit pattern (finite, sign cleared).
+// 128-bit add hi:lo += ah:al with the carry chain in four 32-bit
+// add-with-carry instructions.
+__device__ __forceinline__ void add128(uint64_t& lo, uint64_t& hi, uint64_t al, uint64_t ah) {
+  asm("{\n\t"
+      ".reg .u32 l0, l1, h0, h1, a0, a1, b0, b1;\n\t"
+      "mov.b64 {l0, l1}, %0;\n\t"
+      "mov.b64 {h0, h1}, %1;\n\t"
+      "mov.b64 {a0, a1}, %2;\n\t"
+      "mov.b64 {b0, b1}, %3;\n\t"
+      "add.cc.u32 l0, l0, a0;\n\t"
+      "addc.cc.u32 l1, l1, a1;\n\t"
+      "addc.cc.u32 h0, h0, b0;\n\t"
+      "addc.u32 h1, h1, b1;\n\t"
+      "mov.b64 %0, {l0, l1};\n\t"
+      "mov.b64 %1, {h0, h1};\n\t"
+      "}"
+      : "+l"(lo), "+l"(hi)
+      : "l"(al), "l"(ah));
+}
+
+// Adds |x| given as its bit pattern (finite, sign cleared): m * 2^(sh - 149)
+// goes into group sh / 64 as m << (sh % 64).  Magnitudes in [2^-62, 4)
+// (group 1) take the short path.
 __device__ __forceinline__ void acc_add(Acc& a, uint32_t bits) {
   const uint32_t E = bits >> 23;
   const uint64_t m = E ? (uint64_t)((bits & 0x7FFFFFu) | 0x800000u) : (uint64_t)(bits & 0x7FFFFFu);
@@ -92,13 +114,12 @@ __device__ __forceinline__ void acc_add(Acc& a, uint32_t bits) {
   const uint32_t g = sh >> 6, off = sh & 63u;
   const uint64_t l = m << off;
   const uint64_t h = off > 40 ? m >> (64 - off) : 0ull;
+  if (g == 1) {
+    add128(a.lo[1], a.hi[1], l, h);
+  } else {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const bool sel = q == (int)g;
-    const uint64_t al = sel ? l : 0ull, ah = sel ? h : 0ull;
-    const uint64_t nl = a.lo[q] + al;
-    a.hi[q] += ah + (nl < a.lo[q] ? 1ull : 0ull);
-    a.lo[q] = nl;
+    for (int q = 0; q < 4; ++q)
+      if (q != 1 && q == (int)g) add128(a.lo[q], a.hi[q], l, h);
   }
 }
 
@@ -271,15 +292,28 @@ struct RSelectArgs {
   int parity;  // launch number % 2
 };
 
-// Pass 2: keep draws and the ordered packet.
-__global__ void __launch_bounds__(kRT)
+// Pass 2: keep draws and the ordered packet.  A tile of 8192 elements per
+// ticket; warp w owns elements [1024 w, 1024 (w + 1)) in 32 rounds of 32
+// consecutive elements (lane l: element 32 r + l of the slice), four rounds
+// at a time: the 32 lanes first compute one Philox call each for the quads
+// the four rounds touch (33 when the slice is not quad-aligned) and leave
+// the words in a per-warp buffer, then every lane tests its element.  A
+// round's keep ballot gives the ranks inside the slice; one block scan over
+// the warps and the bounded look-back over tiles give the packet offset, and
+// each warp then writes its kept elements (values re-read from e, an L2 hit).
+constexpr int kRWarps = kRT / 32;
+constexpr int kRSlice = kRTile / kRWarps;   // 1024 elements per warp
+constexpr int kRRounds = kRSlice / 32;      // 32 rounds
+
+__global__ void __launch_bounds__(kRT, 8)
 rk_select(RBatch b, RSelectArgs a) {
-  __shared__ float tile_g[kRTile];
   __shared__ int64_t s_base[kRBatch + 1];
-  __shared__ uint32_t scratch[64];
+  __shared__ uint32_t words[kRWarps][33 * 4];
+  __shared__ uint32_t s_wtot[kRWarps], s_woff[kRWarps];
   __shared__ uint32_t s_t;
   __shared__ uint64_t s_excl;
   __shared__ int64_t s_prev;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_b[i];
   if (threadIdx.x == 0) s_prev = *reinterpret_cast<volatile int64_t*>(&a.ctl->base[a.parity]);
   __syncthreads();
@@ -287,6 +321,7 @@ rk_select(RBatch b, RSelectArgs a) {
   const int64_t prev = s_prev;
   const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
   const uint32_t st0 = (uint32_t)a.step, st1 = (uint32_t)(a.step >> 32);
+  uint32_t* wb = words[warp];
   for (;;) {
     if (threadIdx.x == 0) s_t = atomicAdd(&a.ctl->ticket, 1u);
     __syncthreads();
@@ -297,67 +332,115 @@ rk_select(RBatch b, RSelectArgs a) {
     const float c = a.coef[s];
     const int64_t j0 = (t - s_base[s]) * kRTile;
     const int64_t len = min((int64_t)kRTile, d.len - j0);
-    const int64_t i0 = d.off + j0;  // global index of the tile's first element
-    for (int j = threadIdx.x; j < len; j += kRT) tile_g[j] = a.e[i0 + j];
-    __syncthreads();
-    // this thread's 32 elements [lo, hi) of the tile
-    const int lo = threadIdx.x * kRPer, hi = min(lo + kRPer, (int)len);
-    uint32_t mask = 0;
-    if (lo < hi) {
-      const uint64_t q_first = (uint64_t)(i0 + lo) >> 2, q_last = (uint64_t)(i0 + hi - 1) >> 2;
-      for (uint64_t q = q_first; q <= q_last; ++q) {
+    const int64_t i0 = d.off + j0 + (int64_t)warp * kRSlice;  // global index of the slice start
+    const int64_t slen = max((int64_t)0, min((int64_t)kRSlice, len - (int64_t)warp * kRSlice));
+    const float* ep = a.e + i0;
+    // keep ballots of this slice: lane x holds round x's ballot and the
+    // number of kept elements before round x
+    uint32_t my_ballot = 0, my_before = 0, run = 0;
+    // the next group's values are loaded while this group's draws compute
+    float nxt[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int jl = u * 32 + (int)lane;
+      nxt[u] = jl < slen ? ep[jl] : 0.0f;
+    }
+    for (int r0 = 0; r0 < kRRounds; r0 += 4) {
+      float gv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) gv[u] = nxt[u];
+      if (r0 + 4 < kRRounds) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int jl = (r0 + 4 + u) * 32 + (int)lane;
+          nxt[u] = jl < slen ? ep[jl] : 0.0f;
+        }
+      }
+      // quads of rounds r0 .. r0 + 3: from (i0 + 32 r0) / 4, at most 33
+      const int64_t first = i0 + (int64_t)r0 * 32;
+      const uint64_t q0 = (uint64_t)first >> 2;
+      __syncwarp();
+      {
+        uint64_t q = q0 + lane;
         uint32_t w0 = (uint32_t)q, w1 = (uint32_t)(q >> 32), w2 = st0, w3 = st1;
         philox4x32_10(w0, w1, w2, w3, k0, k1);
-        const uint32_t w[4] = {w0, w1, w2, w3};
+        wb[lane * 4 + 0] = w0;
+        wb[lane * 4 + 1] = w1;
+        wb[lane * 4 + 2] = w2;
+        wb[lane * 4 + 3] = w3;
+        if ((first & 3) != 0 && lane == 0) {  // the 33rd quad
+          q = q0 + 32;
+          w0 = (uint32_t)q;
+          w1 = (uint32_t)(q >> 32);
+          w2 = st0;
+          w3 = st1;
+          philox4x32_10(w0, w1, w2, w3, k0, k1);
+          wb[128] = w0;
+          wb[129] = w1;
+          wb[130] = w2;
+          wb[131] = w3;
+        }
+      }
+      __syncwarp();
+      // element o of the group (o = 32 u + lane) is word (f + o) of the
+      // buffer, f = first % 4; u < min(1, x) is !(u >= x) for every x,
+      // since u < 1 (x >= 1, +Inf and a NaN product all keep)
+      const int f = (int)(first & 3);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int64_t i = (int64_t)(q << 2) + r;
-          const int64_t jl = i - i0;
-          if (jl < lo || jl >= hi) continue;
-          const float g = tile_g[jl];
-          const float ag = fabsf(g);
-          bool keep;
-          if (!(ag < INFINITY)) {
-            keep = true;  // Inf or NaN
-          } else {
-            const float p = fminf(1.0f, __fmul_rn(c, ag));
-            const float u = __uint2float_rn(w[r] >> 8) * 0x1p-24f;
-            keep = u < p;
-          }
-          if (keep) mask |= 1u << (jl - lo);
+      for (int u = 0; u < 4; ++u) {
+        const int jl = (r0 + u) * 32 + (int)lane;
+        bool keep = false;
+        if (jl < slen) {
+          const uint32_t w = wb[f + u * 32 + (int)lane];
+          const float x = __fmul_rn(c, fabsf(gv[u]));
+          keep = !(__uint2float_rn(w >> 8) * 0x1p-24f >= x);
+        }
+        const uint32_t bal = __ballot_sync(kFull, keep);
+        if (lane == (unsigned)(r0 + u)) {
+          my_ballot = bal;
+          my_before = run;
+        }
+        run += __popc(bal);
+      }
+    }
+    if (lane == 0) s_wtot[warp] = run;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t v = lane < kRWarps ? s_wtot[lane] : 0u;
+      const uint32_t incl = warp_incl_scan(v);
+      if (lane < kRWarps) s_woff[lane] = incl - v;
+      const uint32_t total = __shfl_sync(kFull, incl, 31);
+      const uint64_t ex = lookback_warp(a.tstate, t, 0, total, a.status);
+      if (lane == 0) {
+        s_excl = ex;
+        const int64_t tile_off = prev + (int64_t)ex;
+        const int64_t sent = max((int64_t)0, min((int64_t)total, a.capacity - tile_off));
+        if (sent) atomicAdd(&a.counts[d.id], (unsigned long long)sent);
+        if (tile_off + (int64_t)total > a.capacity) set_status(a.status, EF_ERR_CAPACITY);
+        if (t == tiles - 1) {
+          const int64_t all = tile_off + (int64_t)total;
+          a.ctl->base[a.parity ^ 1] = all;
+          a.counts[a.nseg_total] = (unsigned long long)min(all, a.capacity);
         }
       }
     }
-    uint32_t total;
-    const uint32_t mine = __popc(mask);
-    const uint32_t ex = block_excl_scan(mine, scratch, &total);
-    if (threadIdx.x < 32) {
-      const uint64_t e = lookback_warp(a.tstate, t, 0, total, a.status);
-      if (threadIdx.x == 0) s_excl = e;
-    }
     __syncthreads();
-    const int64_t tile_off = prev + (int64_t)s_excl;
-    int64_t pos = tile_off + ex;
-    uint32_t mm = mask;
-    while (mm) {
-      const int bit = __ffs(mm) - 1;
-      mm &= mm - 1;
-      const int jl = lo + bit;
-      if (pos < a.capacity) {
-        a.out_values[pos] = tile_g[jl];
-        a.out_indices[pos] = (int32_t)(i0 + jl);
-        a.e[i0 + jl] = 0.0f;
-      }
-      ++pos;
-    }
-    if (threadIdx.x == 0) {
-      const int64_t sent = max((int64_t)0, min((int64_t)total, a.capacity - tile_off));
-      if (sent) atomicAdd(&a.counts[d.id], (unsigned long long)sent);
-      if (tile_off + (int64_t)total > a.capacity) set_status(a.status, EF_ERR_CAPACITY);
-      if (t == tiles - 1) {
-        const int64_t all = tile_off + (int64_t)total;  // kept so far in the call
-        a.ctl->base[a.parity ^ 1] = all;
-        a.counts[a.nseg_total] = (unsigned long long)min(all, a.capacity);
+    const int64_t slice_off = prev + (int64_t)s_excl + s_woff[warp];
+    if (run) {  // warp-uniform
+      const unsigned lm = lanemask_lt();
+      for (int x = 0; x < kRRounds; ++x) {
+        const uint32_t bal = __shfl_sync(kFull, my_ballot, x);
+        if (!bal) continue;  // warp-uniform
+        const uint32_t before = __shfl_sync(kFull, my_before, x);
+        if ((bal >> lane) & 1u) {
+          const int64_t pos = slice_off + before + __popc(bal & lm);
+          const int64_t jl = (int64_t)x * 32 + lane;
+          if (pos < a.capacity) {
+            a.out_values[pos] = ep[jl];
+            a.out_indices[pos] = (int32_t)(i0 + jl);
+            a.e[i0 + jl] = 0.0f;
+          }
+        }
       }
     }
     __syncthreads();
