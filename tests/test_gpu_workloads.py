@@ -132,6 +132,120 @@ def test_slab_2p31_topk_one_worker_in_full():
     assert_bits_equal(out["bitmap"], oracle.pack_bits(flags), "bitmap")
     assert_bits_equal(out["values"], want["values"], "values (bitmap)")
     assert_bits_equal(e, want["e"], "residual (bitmap)")
+    del out, flags
+    # the same step with 8-bit values: the oracle's quantiser on the oracle's
+    # selection (topk_q8_ef_step is exactly this composition)
+    e.copy_(e0)
+    q = torch.empty(k, dtype=torch.int8, device=DEV)
+    sc = torch.empty(1, device=DEV)
+    idx = torch.empty(k, dtype=torch.int32, device=DEV)
+    ws = torch.empty(efg.topk_q8_workspace_size(n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                     device=DEV)
+    efg.topk_compress_q8(g, e, w.seg_offsets, w.seg_k, q, sc, idx, None, ws)
+    s_want = oracle.q8_scale(want["values"])
+    q_want = oracle.q8_quantize(want["values"], s_want)
+    e_want = want["e"]
+    e_want[want["indices"]] = np.subtract(want["values"], oracle.q8_dequantize(q_want, s_want),
+                                          dtype=np.float32)
+    torch.cuda.synchronize()
+    assert efg.workspace_status(ws) == 0
+    assert_bits_equal(idx, want["indices"], "indices (q8)")
+    assert np.array_equal(host(q), q_want), "codes (q8)"
+    assert_bits_equal(sc, np.array([s_want], np.float32), "scale (q8)")
+    assert_bits_equal(e, e_want, "residual (q8)")
+    del e, e_want, ws, q
+    # the packet's indices through the three index codecs, byte for byte
+    for codec, enc in [(efg.CODEC_LOCAL16, oracle.encode_local16),
+                       (efg.CODEC_BLOCK256, oracle.encode_block256),
+                       (efg.CODEC_RUNVARINT, oracle.encode_runvarint)]:
+        mb, wb = efg.index_codec_sizes(codec, k, n)
+        buf = torch.empty((mb + 3) // 4, dtype=torch.int32, device=DEV)
+        ob = torch.zeros(1, dtype=torch.int64, device=DEV)
+        wsc = torch.empty(wb, dtype=torch.uint8, device=DEV)
+        efg.index_encode(codec, idx, n, buf, ob, wsc)
+        stream_want = enc(want["indices"].astype(np.int64), n)
+        nbytes = int(ob.item())
+        assert efg.workspace_status(wsc) == 0 and nbytes == stream_want.size
+        assert np.array_equal(host(buf).view(np.uint8)[:nbytes], stream_want), codec
+        back = torch.empty(k, dtype=torch.int32, device=DEV)
+        efg.index_decode(codec, buf, nbytes, k, n, back, wsc)
+        assert torch.equal(back, idx) and efg.workspace_status(wsc) == 0
+
+
+def _exact_abs_sum(x: np.ndarray) -> float:
+    """Exact sum of the finite |x| of a float32 array, rounded once to
+    float64, by a route independent of the oracle's math.fsum: every |x| is
+    an integer mantissa m < 2^24 times 2^(sh - 149); per chunk of 2^27
+    elements the mantissas are summed per sh with numpy's bincount (float64
+    weights, exact: every partial sum stays below 2^51), the chunk sums are
+    combined as Python integers, and the exact rational is rounded by
+    Python's correctly rounded int/int division."""
+    from fractions import Fraction
+    acc = [0] * 254
+    for j in range(0, x.size, 1 << 27):
+        b = x[j:j + (1 << 27)].view(np.uint32) & np.uint32(0x7FFFFFFF)
+        b = b[b < np.uint32(0x7F800000)]
+        E = (b >> np.uint32(23)).astype(np.int32)
+        m = (b & np.uint32(0x7FFFFF)) | np.where(E > 0, np.uint32(1 << 23), np.uint32(0))
+        sh = np.maximum(E, 1) - 1
+        for i, v in enumerate(np.bincount(sh, weights=m.astype(np.float64), minlength=254)):
+            acc[i] += int(v)
+    total = sum(v << i for i, v in enumerate(acc))
+    return float(Fraction(total, 1 << 149))
+
+
+def test_slab_2p31_random_sparsification_sampled():
+    """Random magnitude-proportional sparsification at 2^31 elements: the
+    coefficient from an exact |g| sum computed independently on the host;
+    every kept element passes its draw (Philox word from the oracle's
+    generator), a sample of a million others fails it, values and residual
+    agree at all of them, and the count matches."""
+    w = wl.workload("slab_2p31")
+    n, k = w.n, w.total_k
+    g = w.gradient(0, 2, DEV)
+    e = torch.zeros(n, device=DEV)
+    g_np = host(g)
+    cap = 2 * k
+    vals = torch.empty(cap, device=DEV)
+    idx = torch.empty(cap, dtype=torch.int32, device=DEV)
+    counts = torch.empty(2, dtype=torch.int64, device=DEV)
+    ws = torch.empty(efg.randk_workspace_size(n, [0, n], [k]), dtype=torch.uint8, device=DEV)
+    seed, step = 0x5EED, 3
+    efg.randk_compress(g, e, [0, n], [k], seed, step, vals, idx, counts, ws)
+    S = _exact_abs_sum(g_np)
+    c = np.float32(float(k) / S)
+    torch.cuda.synchronize()
+    assert efg.workspace_status(ws) == 0
+    total = int(host(counts)[-1])
+    kept = host(idx[:total]).astype(np.int64)
+    assert np.all(np.diff(kept) > 0)
+    rng = np.random.default_rng(1)
+    others = np.setdiff1d(rng.integers(0, n, 1_000_000), kept)
+    probe = np.concatenate([kept, others])
+    # Philox words of the probed elements, one generator call per element
+    words = np.empty(probe.size, np.uint32)
+    for j in range(0, probe.size, 1 << 20):
+        p_ = probe[j:j + (1 << 20)].astype(np.uint64)
+        q_ = p_ >> np.uint64(2)
+        out = oracle.philox4x32_10(q_ & np.uint64(0xFFFFFFFF), q_ >> np.uint64(32),
+                                   np.uint64(step), np.uint64(0), np.uint64(seed), np.uint64(0))
+        words[j:j + p_.size] = np.stack(out)[(p_ & np.uint64(3)).astype(np.int64),
+                                             np.arange(p_.size)]
+    a = np.abs(g_np[probe])
+    p = np.ones(probe.size, np.float32)
+    fin = np.isfinite(a)
+    p[fin] = np.fmin(np.float32(1), np.multiply(c, a[fin], dtype=np.float32))
+    u = (words >> np.uint32(8)).astype(np.float32) * np.float32(2.0 ** -24)
+    keep = u < p
+    assert keep[:kept.size].all(), "a sent element failed its draw"
+    assert not keep[kept.size:].any(), "a sampled element passed its draw but was not sent"
+    assert_bits_equal(vals[:total], g_np[kept], "values")
+    e_probe = host(e[torch.from_numpy(probe).to(DEV)])
+    want_e = g_np[probe].copy()
+    want_e[:kept.size] = 0.0
+    assert_bits_equal(e_probe, want_e, "residual (probed)")
+    pv = np.minimum(1.0, float(c) * np.abs(g_np.astype(np.float64)))
+    assert abs(total - pv.sum()) < 6 * np.sqrt(np.sum(pv * (1 - pv)))
 
 
 def test_slab_2p31_sign_sampled():
