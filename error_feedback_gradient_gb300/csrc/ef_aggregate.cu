@@ -476,25 +476,23 @@ __device__ __forceinline__ Entry pipe_bitmap_entries(const AggArgs& a, const flo
   return e;
 }
 
-// Finishes a tile whose entries, slots and w values are in the lanes.
+// Finishes a tile whose entries, slots and w values are in the lanes.  The
+// tile of G is assembled in the warp's shared copy (zeros, then each slot's
+// sum) and stored once with 16-byte stores: no slot is written twice, so no
+// partial sector ever reaches DRAM.
 __device__ __forceinline__ void pipe_finish(const AggArgs& a, int64_t t, const Entry& e, float wv,
                                             float* G, float* wts, bool g_vec, float* vbuf,
-                                            unsigned lane) {
+                                            float* acc, unsigned lane) {
   const int64_t t0 = t * kWT;
   const int tlen = (int)min((int64_t)kWT, a.n - t0);
+  float4* acc4 = reinterpret_cast<float4*>(acc);
   if (G) {
-    float* gt = G + t0;
-    if (g_vec && tlen == kWT) {
 #pragma unroll
-      for (int r = 0; r < kWT / 128; ++r)
-        __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, make_float4(0.f, 0.f, 0.f, 0.f));
-    } else {
-      for (int i = lane; i < tlen; i += 32) gt[i] = 0.0f;
-    }
+    for (int r = 0; r < kWT / 128; ++r) acc4[r * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const unsigned grp = __match_any_sync(kFull, e.ix >= 0 ? e.ix : kWT + (int)lane);
   vbuf[lane] = e.v;
-  __syncwarp();  // also orders every lane's zero stores before the sums below
+  __syncwarp();
   if (e.ix >= 0 && (int)lane == __ffs(grp) - 1) {
     float sum = __fadd_rn(0.0f, e.v);
     unsigned m = grp & (grp - 1);
@@ -503,10 +501,21 @@ __device__ __forceinline__ void pipe_finish(const AggArgs& a, int64_t t, const E
       m &= m - 1;
       sum = __fadd_rn(sum, vbuf[i]);
     }
-    if (G) G[t0 + e.ix] = sum;
+    if (G) acc[e.ix] = sum;
     wts[t0 + e.ix] = __fsub_rn(wv, __fmul_rn(a.eta, sum));
   }
   __syncwarp();
+  if (G) {
+    float* gt = G + t0;
+    if (g_vec && tlen == kWT) {
+#pragma unroll
+      for (int r = 0; r < kWT / 128; ++r)
+        __stcs(reinterpret_cast<float4*>(gt) + r * 32 + lane, acc4[r * 32 + lane]);
+    } else {
+      for (int i = lane; i < tlen; i += 32) gt[i] = acc[i];
+    }
+  }
+  __syncwarp();  // the shared copy is reused by the next tile
 }
 
 template <bool kBitmap>
@@ -526,7 +535,7 @@ agg_apply_pipe(AggArgs a, const uint32_t* start, float* __restrict__ G, float* _
   auto finish = [&](int64_t j, const Entry& e, float wv) {
     const int64_t t = first + j * nw;
     if (e.fast)
-      pipe_finish(a, t, e, wv, G, wts, g_vec, vbuf, lane);
+      pipe_finish(a, t, e, wv, G, wts, g_vec, vbuf, acc_all[warp], lane);
     else
       tile_general<kBitmap>(a, start, t, G, wts, g_vec, acc_all[warp], touched_all[warp], lane);
   };
