@@ -802,6 +802,53 @@ def run_next(args, dev):
     return out
 
 
+def run_case(args):
+    """One entry point alone, three calls, for profiling its kernels in
+    isolation (--case): 'topk' (one tensor of n elements, top-0.1 %),
+    'aggregate' (4 workers' int32 packets of 0.1 % over n, with G and SGD)
+    or 'randk' (random sparsification of one tensor, expected 0.1 %)."""
+    import torch
+    import error_feedback_gradient_gb300 as efg
+    from error_feedback_gradient_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    n = args.n
+    k = wl.k_from_ratio(n, 1, 1000)
+    if args.case == "topk":
+        g = wl.student_t3(n, 1e-3, 1, dev)
+        e = wl.normal(n, 1e-4, 2, dev)
+        v = torch.empty(k, device=dev)
+        ix = torch.empty(k, dtype=torch.int32, device=dev)
+        ws = torch.empty(efg.topk_workspace_size(n, [0, n], [k]), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            efg.topk_compress(g, e, [0, n], [k], v, ix, None, ws)
+    elif args.case == "aggregate":
+        W = 4
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        stride = n // k
+        base = torch.arange(k, device=dev, dtype=torch.int64) * stride
+        ix = [torch.sort(base + torch.randint(0, stride, (k,), device=dev, generator=gen))
+              .values.to(torch.int32) for _ in range(W)]
+        vals = [torch.randn(k, device=dev, generator=gen) * 1e-3 for _ in range(W)]
+        G = torch.empty(n, device=dev)
+        w = torch.zeros(n, device=dev)
+        ws = torch.empty(efg.aggregate_workspace_size(W, efg.IDX_INT32, n), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            efg.sparse_aggregate_apply(vals, ix, None, [k] * W, n, 0.1, G, w, ws)
+    else:
+        g = wl.student_t3(n, 1e-3, 1, dev)
+        e = torch.zeros_like(g)
+        v = torch.empty(2 * k, device=dev)
+        ix = torch.empty(2 * k, dtype=torch.int32, device=dev)
+        cnt = torch.empty(2, dtype=torch.int64, device=dev)
+        ws = torch.empty(efg.randk_workspace_size(n, [0, n], [k]), dtype=torch.uint8, device=dev)
+        for step in range(3):
+            efg.randk_compress(g, e, [0, n], [k], 7, step, v, ix, cnt, ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": args.case, "n": n, "k": k, "status": efg.workspace_status(ws)}))
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -822,7 +869,12 @@ def main(argv=None):
     p.add_argument("--traffic-per-launch", type=float, default=None,
                    help="DRAM bytes of one topk_fused launch at this size, from ncu")
     p.add_argument("--no-extras", dest="extras", action="store_false")
+    p.add_argument("--case", choices=["topk", "aggregate", "randk"], default=None,
+                   help="run one entry point alone (three calls at --n) for profiling")
     args = p.parse_args(argv)
+    if args.case:
+        run_case(args)
+        return
     args.workload_desc = (f"slab_2p31: flat fp32 slab n={args.n} per worker, W={args.workers}, "
                           "Student-t(3)x1e-3; top-0.1% int32 + bitmap EF and 1-bit EF "
                           "(beta1=0.9), each aggregated locally with SGD eta=0.1")
