@@ -20,10 +20,14 @@
 // carry-save chunks with one atomicAdd per chunk when it leaves a segment
 // (sums of at most 2^14 flushes of 2^50 fit in 64 bits).  rk_finalize turns
 // each segment's chunks into the float64 nearest the exact sum and forms c.
-// Pass 2 (rk_select, 4 B / element + 8 B per kept element) stages each
-// 8192-element tile of g in shared memory, draws one Philox call per four
-// elements, and compacts the kept elements in ticket order with the bounded
-// decoupled look-back (the running offset carries across launches).
+// Pass 2 draws and packs in three launches with no wait between warps:
+// rk_draw (4 B / element + 1/8 B of keep bits) walks the aligned
+// 4096-element blocks of each segment, a warp per block and each lane taking
+// one quad of four elements (one Philox call, one 16-byte load), and writes
+// the block's keep bits and count; rk_offsets turns the counts into packet
+// offsets (the running offset carries across launches); rk_pack re-reads the
+// keep bits and writes the kept elements in index order (8 B per kept
+// element, + its residual write).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -57,10 +61,8 @@ struct RBatch {
 };
 
 struct RCtl {
-  uint32_t ticket;
-  uint32_t pad;
   int64_t base[2];  // kept elements before a launch: launch b reads [b % 2], its
-                    // last tile writes [(b + 1) % 2] (never the word being read)
+                    // offsets kernel writes [(b + 1) % 2] (never the word being read)
 };
 
 __device__ __forceinline__ int find_tile_seg(const int64_t* base, int nseg, int64_t t) {
@@ -75,14 +77,12 @@ __device__ __forceinline__ int find_tile_seg(const int64_t* base, int nseg, int6
 
 // ---------------------------------------------------------------- exact sum
 
-struct Acc {
-  uint64_t lo[4], hi[4];
+// Group 1 of a thread's accumulator (magnitudes in [2^-62, 4), where
+// gradients live) is held in registers; groups 0, 2 and 3 in the thread's
+// own shared-memory slots.
+struct AccSlow {
+  uint64_t v[3][2][kRT];  // [group 0, 2, 3][lo, hi][thread]
 };
-
-__device__ __forceinline__ void acc_clear(Acc& a) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) a.lo[q] = a.hi[q] = 0;
-}
 
 // 128-bit add hi:lo += ah:al with the carry chain in four 32-bit
 // add-with-carry instructions.
@@ -104,22 +104,25 @@ __device__ __forceinline__ void add128(uint64_t& lo, uint64_t& hi, uint64_t al, 
       : "l"(al), "l"(ah));
 }
 
-// Adds |x| given as its bit pattern (finite, sign cleared): m * 2^(sh - 149)
-// goes into group sh / 64 as m << (sh % 64).  Magnitudes in [2^-62, 4)
-// (group 1) take the short path.
-__device__ __forceinline__ void acc_add(Acc& a, uint32_t bits) {
+// Adds |x| given as its bit pattern (sign cleared; nothing for Inf / NaN):
+// m * 2^(sh - 149) goes into group sh / 64 as m << (sh % 64).
+__device__ __forceinline__ void acc_add(uint64_t& lo1, uint64_t& hi1, AccSlow& slow,
+                                        uint32_t bits) {
+  if (bits >= 0x7F800000u) return;
   const uint32_t E = bits >> 23;
-  const uint64_t m = E ? (uint64_t)((bits & 0x7FFFFFu) | 0x800000u) : (uint64_t)(bits & 0x7FFFFFu);
+  const uint64_t m = E ? (uint64_t)((bits & 0x7FFFFFu) | 0x800000u) : (uint64_t)bits;
   const uint32_t sh = E ? E - 1 : 0;
   const uint32_t g = sh >> 6, off = sh & 63u;
   const uint64_t l = m << off;
   const uint64_t h = off > 40 ? m >> (64 - off) : 0ull;
   if (g == 1) {
-    add128(a.lo[1], a.hi[1], l, h);
+    add128(lo1, hi1, l, h);
   } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q != 1 && q == (int)g) add128(a.lo[q], a.hi[q], l, h);
+    const int x = g == 0 ? 0 : (int)g - 1;
+    uint64_t lo = slow.v[x][0][threadIdx.x], hi = slow.v[x][1][threadIdx.x];
+    add128(lo, hi, l, h);
+    slow.v[x][0][threadIdx.x] = lo;
+    slow.v[x][1][threadIdx.x] = hi;
   }
 }
 
@@ -134,14 +137,28 @@ __device__ __forceinline__ uint64_t bits40(uint64_t hi, uint64_t lo, int pos) {
   return v & kMask40;
 }
 
-// CTA-wide flush of every thread's accumulator into the segment's chunks.
-__device__ void acc_flush(const Acc& a, uint64_t* chunks, uint64_t (*red)[kChunks]) {
+// CTA-wide flush of every thread's accumulator into the segment's chunks;
+// clears the accumulator.
+__device__ void acc_flush(uint64_t& lo1, uint64_t& hi1, AccSlow& slow, uint64_t* chunks,
+                          uint64_t (*red)[kChunks]) {
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  uint64_t lo[4], hi[4];
+  lo[1] = lo1;
+  hi[1] = hi1;
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    const int q = x == 0 ? 0 : x + 1;
+    lo[q] = slow.v[x][0][threadIdx.x];
+    hi[q] = slow.v[x][1][threadIdx.x];
+    slow.v[x][0][threadIdx.x] = 0;
+    slow.v[x][1][threadIdx.x] = 0;
+  }
+  lo1 = hi1 = 0;
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     uint64_t v = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) v += bits40(a.hi[q], a.lo[q], 40 * c - 64 * q);
+    for (int q = 0; q < 4; ++q) v += bits40(hi[q], lo[q], 40 * c - 64 * q);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     if (lane == 0) red[warp][c] = v;
@@ -155,53 +172,82 @@ __device__ void acc_flush(const Acc& a, uint64_t* chunks, uint64_t (*red)[kChunk
   __syncthreads();
 }
 
-// Pass 1: g = g_raw + e written over e; exact sum of the finite |g|.
-__global__ void __launch_bounds__(kRT)
+// Pass 1: g = g_raw + e written over e; exact sum of the finite |g|.  Tiles
+// are the aligned 8192-element blocks of the whole tensor cut to one
+// segment, strided over the grid; a whole tile with 16-byte aligned buffers
+// moves as float4 quads (thread x takes quads x + 256 u), four quads of each
+// array in flight per thread; other tiles go element by element.
+template <bool kVec>
+__global__ void __launch_bounds__(kRT, 4)
 rk_sum(RBatch b, const float* __restrict__ g_raw, float* __restrict__ e, uint64_t* acc) {
   __shared__ int64_t s_base[kRBatch + 1];
   __shared__ uint64_t red[kRT / 32][kChunks];
+  __shared__ AccSlow slow;
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_a[i];
+#pragma unroll
+  for (int x = 0; x < 3; ++x) slow.v[x][0][threadIdx.x] = slow.v[x][1][threadIdx.x] = 0;
   __syncthreads();
   const int64_t tiles = s_base[b.nseg];
-  Acc a;
-  acc_clear(a);
+  uint64_t lo1 = 0, hi1 = 0;
   int cur = -1;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     const int s = find_tile_seg(s_base, b.nseg, t);
     if (s != cur) {  // uniform across the CTA
-      if (cur >= 0) {
-        acc_flush(a, acc + (int64_t)cur * kChunks, red);
-        acc_clear(a);
-      }
+      if (cur >= 0) acc_flush(lo1, hi1, slow, acc + (int64_t)cur * kChunks, red);
       cur = s;
     }
     const RSeg& d = b.seg[s];
-    const int64_t j0 = (t - s_base[s]) * kRTile;
-    const int64_t len = min((int64_t)kRTile, d.len - j0);
-    const float* gp = g_raw + d.off + j0;
-    float* ep = e + d.off + j0;
+    const int64_t sa = (d.off / kRTile + (t - s_base[s])) * kRTile;
+    const uint32_t lo = (uint32_t)max(d.off, sa), hi = (uint32_t)min(d.off + d.len, sa + kRTile);
+    const uint32_t a0 = (uint32_t)sa;
+    if (kVec && lo == a0 && hi == a0 + kRTile) {
+      const float4* g4 = reinterpret_cast<const float4*>(g_raw) + (a0 >> 2);
+      float4* e4 = reinterpret_cast<float4*>(e) + (a0 >> 2);
 #pragma unroll 1
-    for (int r0 = 0; r0 < kRPer; r0 += 8) {
-      float gv[8], ev[8];
+      for (int r0 = 0; r0 < kRTile / 4 / kRT; r0 += 4) {
+        float4 gv[4], ev[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t j = (int64_t)(r0 + u) * kRT + threadIdx.x;
-        gv[u] = j < len ? __ldcs(gp + j) : 0.0f;
-        ev[u] = j < len ? __ldcs(ep + j) : 0.0f;
+        for (int u = 0; u < 4; ++u) {
+          gv[u] = __ldcs(g4 + (r0 + u) * kRT + threadIdx.x);
+          ev[u] = __ldcs(e4 + (r0 + u) * kRT + threadIdx.x);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float4 o;
+          o.x = __fadd_rn(gv[u].x, ev[u].x);
+          o.y = __fadd_rn(gv[u].y, ev[u].y);
+          o.z = __fadd_rn(gv[u].z, ev[u].z);
+          o.w = __fadd_rn(gv[u].w, ev[u].w);
+          __stcs(e4 + (r0 + u) * kRT + threadIdx.x, o);
+          acc_add(lo1, hi1, slow, __float_as_uint(o.x) & 0x7FFFFFFFu);
+          acc_add(lo1, hi1, slow, __float_as_uint(o.y) & 0x7FFFFFFFu);
+          acc_add(lo1, hi1, slow, __float_as_uint(o.z) & 0x7FFFFFFFu);
+          acc_add(lo1, hi1, slow, __float_as_uint(o.w) & 0x7FFFFFFFu);
+        }
       }
+    } else {
+#pragma unroll 1
+      for (int r0 = 0; r0 < kRTile / kRT; r0 += 8) {
+        float gv[8], ev[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t j = (int64_t)(r0 + u) * kRT + threadIdx.x;
-        if (j < len) {
-          const float g = __fadd_rn(gv[u], ev[u]);
-          __stcs(ep + j, g);
-          const uint32_t bits = __float_as_uint(g) & 0x7FFFFFFFu;
-          if (bits < 0x7F800000u) acc_add(a, bits);
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t i = a0 + (uint32_t)((r0 + u) * kRT) + threadIdx.x;
+          gv[u] = i >= lo && i < hi ? __ldcs(g_raw + i) : 0.0f;
+          ev[u] = i >= lo && i < hi ? __ldcs(e + i) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t i = a0 + (uint32_t)((r0 + u) * kRT) + threadIdx.x;
+          if (i >= lo && i < hi) {
+            const float g = __fadd_rn(gv[u], ev[u]);
+            __stcs(e + i, g);
+            acc_add(lo1, hi1, slow, __float_as_uint(g) & 0x7FFFFFFFu);
+          }
         }
       }
     }
   }
-  if (cur >= 0) acc_flush(a, acc + (int64_t)cur * kChunks, red);
+  if (cur >= 0) acc_flush(lo1, hi1, slow, acc + (int64_t)cur * kChunks, red);
 }
 
 // float64 nearest (ties to even) to the exact sum sum_c chunks[c] * 2^(40c)
@@ -262,18 +308,41 @@ __global__ void rk_finalize(RBatch b, const uint64_t* acc, float* coef) {
 
 // ---------------------------------------------------------------- pass 2
 
-__device__ __forceinline__ void philox4x32_10(uint32_t& c0, uint32_t& c1, uint32_t& c2,
-                                              uint32_t& c3, uint32_t k0, uint32_t k1) {
+// Round keys of Philox4x32-10 for one key: key word 0 and 1 of round r are
+// (seed low + r 0x9E3779B9, seed high + r 0xBB67AE85) mod 2^32.  Passed by
+// value to the kernels, so a round reads them as constant operands.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
+// Two independent Philox4x32-10 calls, round by round.
+__device__ __forceinline__ void philox4x32_10x2(uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                                uint32_t& a3, uint32_t& b0, uint32_t& b1,
+                                                uint32_t& b2, uint32_t& b3, const PhiloxKeys& k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    c0 = hi1 ^ c1 ^ k0;
-    c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
-    c3 = lo0;
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const uint64_t pa0 = (uint64_t)0xD2511F53u * a0, pa1 = (uint64_t)0xCD9E8D57u * a2;
+    const uint64_t pb0 = (uint64_t)0xD2511F53u * b0, pb1 = (uint64_t)0xCD9E8D57u * b2;
+    a0 = (uint32_t)(pa1 >> 32) ^ a1 ^ k.k0[r];
+    a1 = (uint32_t)pa1;
+    a2 = (uint32_t)(pa0 >> 32) ^ a3 ^ k.k1[r];
+    a3 = (uint32_t)pa0;
+    b0 = (uint32_t)(pb1 >> 32) ^ b1 ^ k.k0[r];
+    b1 = (uint32_t)pb1;
+    b2 = (uint32_t)(pb0 >> 32) ^ b3 ^ k.k1[r];
+    b3 = (uint32_t)pb0;
   }
 }
 
@@ -285,172 +354,262 @@ struct RSelectArgs {
   int64_t capacity;
   unsigned long long* counts;  // [nseg + 1] of the whole call
   int32_t nseg_total;
-  uint64_t seed, step;
-  uint64_t* tstate;
+  PhiloxKeys keys;
+  uint32_t st0, st1;  // step low, high: counter words 2 and 3
+  uint32_t* kw;      // keep words: 128 per tile, word 32 j + l = lane l's word j
+  uint32_t* cnt;     // kept elements per tile
+  uint32_t* csum;    // kept elements per chunk of kOffChunk tiles
+  int64_t* off;      // [tiles + 1] packet position of each tile's first kept element
   RCtl* ctl;
   int32_t* status;
   int parity;  // launch number % 2
 };
 
-// Pass 2: keep draws and the ordered packet.  A tile of 8192 elements per
-// ticket; warp w owns elements [1024 w, 1024 (w + 1)) in 32 rounds of 32
-// consecutive elements (lane l: element 32 r + l of the slice), four rounds
-// at a time: the 32 lanes first compute one Philox call each for the quads
-// the four rounds touch (33 when the slice is not quad-aligned) and leave
-// the words in a per-warp buffer, then every lane tests its element.  A
-// round's keep ballot gives the ranks inside the slice; one block scan over
-// the warps and the bounded look-back over tiles give the packet offset, and
-// each warp then writes its kept elements (values re-read from e, an L2 hit).
+// Pass-2 tiles are the aligned 4096-element blocks of the whole tensor
+// (global index / 4096) cut to one segment, so every quad of four elements
+// that shares a Philox counter lies in one tile.  A warp walks a tile's 1024
+// quads in 32 rounds of 32: in a round lane l takes quad 32 r + l, loads its
+// four elements at once (16 bytes when e is 16-byte aligned), computes its
+// one Philox call and sets four keep bits (bit 4 (r % 8) + u of word r / 8
+// for element u of the quad).
 constexpr int kRWarps = kRT / 32;
-constexpr int kRSlice = kRTile / kRWarps;   // 1024 elements per warp
-constexpr int kRRounds = kRSlice / 32;      // 32 rounds
+constexpr int kRSelTile = 4096;                 // elements per pass-2 tile (one warp)
+constexpr int kRWords = kRSelTile / 1024;       // 4 keep words per lane
+constexpr int kDrawCtas = 5;                    // rk_draw CTAs per SM (48 registers)
+constexpr int kOffChunk = 8192;                 // tiles per rk_offsets CTA
+constexpr int kOffPer = kOffChunk / kRT;        // 32 tiles per thread
 
-__global__ void __launch_bounds__(kRT, 8)
-rk_select(RBatch b, RSelectArgs a) {
+// The four elements of quad q; with kAll every one of them is in the tile.
+// Element indices are below 2^31, so quads and elements fit 32 bits.
+template <bool kVec, bool kAll>
+__device__ __forceinline__ float4 rk_load_quad(const float* e, uint32_t q, uint32_t lo,
+                                               uint32_t hi) {
+  const uint32_t i = 4 * q;
+  if (kAll) {
+    if (kVec) return reinterpret_cast<const float4*>(e)[q];
+    return make_float4(e[i], e[i + 1], e[i + 2], e[i + 3]);
+  }
+  float4 v;
+  v.x = (i >= lo && i < hi) ? e[i] : 0.0f;
+  v.y = (i + 1 >= lo && i + 1 < hi) ? e[i + 1] : 0.0f;
+  v.z = (i + 2 >= lo && i + 2 < hi) ? e[i + 2] : 0.0f;
+  v.w = (i + 3 >= lo && i + 3 < hi) ? e[i + 3] : 0.0f;
+  return v;
+}
+
+// u < min(1, x) is !(u >= x) for every x, since u < 1 (x >= 1, +Inf and a
+// NaN product all keep).
+__device__ __forceinline__ bool rk_keep(uint32_t w, float c, float g) {
+  const float x = __fmul_rn(c, fabsf(g));
+  return !(__uint2float_rn(w >> 8) * 0x1p-24f >= x);
+}
+
+// Keep bits of quad q (element u at bit u).
+template <bool kAll>
+__device__ __forceinline__ uint32_t rk_quad_bits(uint32_t q, const float4& v, float c,
+                                                 uint32_t w0, uint32_t w1, uint32_t w2,
+                                                 uint32_t w3, uint32_t lo, uint32_t hi) {
+  bool k[4] = {rk_keep(w0, c, v.x), rk_keep(w1, c, v.y), rk_keep(w2, c, v.z),
+               rk_keep(w3, c, v.w)};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (!kAll) k[u] = k[u] && 4 * q + u >= lo && 4 * q + u < hi;
+    if (k[u]) bits |= 1u << u;
+  }
+  return bits;
+}
+
+// Keep words of one tile starting at quad q0, written to kwt[32 j + lane];
+// returns the number of kept elements of this lane.  Two rounds at a time,
+// so that two independent Philox calls interleave.  The counter's high word
+// (quad index / 2^32) is 0 for every quad of an int32-indexed tensor.
+template <bool kVec, bool kAll>
+__device__ __forceinline__ uint32_t rk_slice(const float* e, uint32_t q0, uint32_t lo, uint32_t hi,
+                                             float c, const PhiloxKeys& keys, uint32_t st0,
+                                             uint32_t st1, uint32_t* kwt) {
+  const unsigned lane = lane_id();
+  uint32_t cnt = 0;
+#pragma unroll 1
+  for (int j = 0; j < kRWords; ++j) {
+    uint32_t kb = 0;
+#pragma unroll
+    for (int r = 0; r < 8; r += 2) {
+      const uint32_t qa = q0 + 32u * (8 * j + r) + lane, qb = qa + 32;
+      const float4 va = rk_load_quad<kVec, kAll>(e, qa, lo, hi);
+      const float4 vb = rk_load_quad<kVec, kAll>(e, qb, lo, hi);
+      uint32_t a0 = qa, a1 = 0, a2 = st0, a3 = st1;
+      uint32_t b0 = qb, b1 = 0, b2 = st0, b3 = st1;
+      philox4x32_10x2(a0, a1, a2, a3, b0, b1, b2, b3, keys);
+      kb |= rk_quad_bits<kAll>(qa, va, c, a0, a1, a2, a3, lo, hi) << (4 * r);
+      kb |= rk_quad_bits<kAll>(qb, vb, c, b0, b1, b2, b3, lo, hi) << (4 * r + 4);
+    }
+    kwt[32 * j + lane] = kb;
+    cnt += __popc(kb);
+  }
+  return cnt;
+}
+
+// Tile t's segment and the bounds [lo, hi) of its elements; returns the
+// first quad of its aligned block.
+__device__ __forceinline__ int64_t rk_tile(const RBatch& b, const int64_t* s_base, int64_t t,
+                                           int* seg, int64_t* lo, int64_t* hi) {
+  const int s = find_tile_seg(s_base, b.nseg, t);
+  const RSeg& d = b.seg[s];
+  const int64_t sa = (d.off / kRSelTile + (t - s_base[s])) * kRSelTile;
+  *seg = s;
+  *lo = max(d.off, sa);
+  *hi = min(d.off + d.len, sa + kRSelTile);
+  return sa >> 2;
+}
+
+// Pass 2a: keep bits and counts, one warp per tile, tiles strided over the
+// grid's warps.
+template <bool kVec>
+__global__ void __launch_bounds__(kRT, kDrawCtas)
+rk_draw(RBatch b, RSelectArgs a) {
   __shared__ int64_t s_base[kRBatch + 1];
-  __shared__ uint32_t words[kRWarps][33 * 4];
-  __shared__ uint32_t s_wtot[kRWarps], s_woff[kRWarps];
-  __shared__ uint32_t s_t;
-  __shared__ uint64_t s_excl;
-  __shared__ int64_t s_prev;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_b[i];
-  if (threadIdx.x == 0) s_prev = *reinterpret_cast<volatile int64_t*>(&a.ctl->base[a.parity]);
   __syncthreads();
   const int64_t tiles = s_base[b.nseg];
-  const int64_t prev = s_prev;
-  const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
-  const uint32_t st0 = (uint32_t)a.step, st1 = (uint32_t)(a.step >> 32);
-  uint32_t* wb = words[warp];
-  for (;;) {
-    if (threadIdx.x == 0) s_t = atomicAdd(&a.ctl->ticket, 1u);
-    __syncthreads();
-    const int64_t t = s_t;
-    if (t >= tiles) break;
-    const int s = find_tile_seg(s_base, b.nseg, t);
-    const RSeg& d = b.seg[s];
+  for (int64_t t = (int64_t)blockIdx.x * kRWarps + warp; t < tiles;
+       t += (int64_t)gridDim.x * kRWarps) {
+    int s;
+    int64_t lo, hi;
+    const int64_t q0 = rk_tile(b, s_base, t, &s, &lo, &hi);
     const float c = a.coef[s];
-    const int64_t j0 = (t - s_base[s]) * kRTile;
-    const int64_t len = min((int64_t)kRTile, d.len - j0);
-    const int64_t i0 = d.off + j0 + (int64_t)warp * kRSlice;  // global index of the slice start
-    const int64_t slen = max((int64_t)0, min((int64_t)kRSlice, len - (int64_t)warp * kRSlice));
-    const float* ep = a.e + i0;
-    // keep ballots of this slice: lane x holds round x's ballot and the
-    // number of kept elements before round x
-    uint32_t my_ballot = 0, my_before = 0, run = 0;
-    // the next group's values are loaded while this group's draws compute
-    float nxt[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int jl = u * 32 + (int)lane;
-      nxt[u] = jl < slen ? ep[jl] : 0.0f;
+    uint32_t* kwt = a.kw + t * (32 * kRWords);
+    const uint32_t q = (uint32_t)q0, l = (uint32_t)lo, h = (uint32_t)hi;
+    const uint32_t cnt = (l == 4 * q && h == 4 * q + kRSelTile)
+                             ? rk_slice<kVec, true>(a.e, q, l, h, c, a.keys, a.st0, a.st1, kwt)
+                             : rk_slice<kVec, false>(a.e, q, l, h, c, a.keys, a.st0, a.st1, kwt);
+    const uint32_t run = __reduce_add_sync(kFull, cnt);
+    if (lane == 0) {
+      a.cnt[t] = run;
+      if (run) atomicAdd(&a.csum[t / kOffChunk], run);
     }
-    for (int r0 = 0; r0 < kRRounds; r0 += 4) {
-      float gv[4];
+  }
+}
+
+// Pass 2b: packet offsets.  CTA c scans the counts of tiles
+// [c kOffChunk, (c + 1) kOffChunk) on top of the kept elements before the
+// launch and of the earlier chunks; the last CTA closes the launch (total,
+// capacity status, base of the next launch).
+__global__ void __launch_bounds__(kRT)
+rk_offsets(int64_t tiles, RSelectArgs a) {
+  __shared__ uint32_t scratch[40];
+  __shared__ int64_t s_pre;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int64_t c = blockIdx.x;
+  if (warp == 0) {
+    uint64_t v = 0;
+    for (int64_t x = lane; x < c; x += 32) v += a.csum[x];
+    v = warp_sum_u64(v);
+    if (lane == 0)
+      s_pre = *reinterpret_cast<volatile int64_t*>(&a.ctl->base[a.parity]) + (int64_t)v;
+  }
+  const int64_t t0 = c * kOffChunk + (int64_t)threadIdx.x * kOffPer;
+  uint32_t v[kOffPer];
+  uint32_t mine = 0;
+  if (t0 + kOffPer <= tiles) {  // 128-byte aligned: the array is, and t0 % 32 == 0
 #pragma unroll
-      for (int u = 0; u < 4; ++u) gv[u] = nxt[u];
-      if (r0 + 4 < kRRounds) {
+    for (int x = 0; x < kOffPer; x += 4) {
+      const uint4 q = *reinterpret_cast<const uint4*>(a.cnt + t0 + x);
+      v[x] = q.x;
+      v[x + 1] = q.y;
+      v[x + 2] = q.z;
+      v[x + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < kOffPer; ++x) v[x] = t0 + x < tiles ? a.cnt[t0 + x] : 0u;
+  }
+#pragma unroll
+  for (int x = 0; x < kOffPer; ++x) mine += v[x];
+  uint32_t total;
+  const uint32_t ex = block_excl_scan(mine, scratch, &total);  // synchronises s_pre too
+  int64_t pos = s_pre + (int64_t)ex;
+#pragma unroll
+  for (int x = 0; x < kOffPer; ++x) {
+    if (t0 + x < tiles) a.off[t0 + x] = pos;
+    pos += v[x];
+  }
+  if (c == gridDim.x - 1 && threadIdx.x == 0) {
+    const int64_t all = s_pre + (int64_t)total;
+    a.off[tiles] = all;
+    a.ctl->base[a.parity ^ 1] = all;
+    a.counts[a.nseg_total] = (unsigned long long)min(all, a.capacity);
+    if (all > a.capacity) set_status(a.status, EF_ERR_CAPACITY);
+  }
+}
+
+// Pass 2c: the ordered packet.  One warp per tile with kept elements: ranks
+// from a warp scan of the lanes' counts round by round, values re-read from
+// e and e set to +0 at every element that fits the packet.  The first
+// threads of CTA 0 write the per-segment counts.
+__global__ void __launch_bounds__(kRT)
+rk_pack(RBatch b, RSelectArgs a) {
+  __shared__ int64_t s_base[kRBatch + 1];
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_b[i];
+  __syncthreads();
+  const int64_t tiles = s_base[b.nseg];
+  if (blockIdx.x == 0 && threadIdx.x < b.nseg) {
+    const int64_t lo = min(a.off[s_base[threadIdx.x]], a.capacity);
+    const int64_t hi = min(a.off[s_base[threadIdx.x + 1]], a.capacity);
+    a.counts[b.seg[threadIdx.x].id] = (unsigned long long)(hi - lo);
+  }
+  for (int64_t t = (int64_t)blockIdx.x * kRWarps + warp; t < tiles;
+       t += (int64_t)gridDim.x * kRWarps) {
+    if (a.cnt[t] == 0) continue;  // warp-uniform
+    int64_t pos = a.off[t];
+    if (pos >= a.capacity) continue;
+    int s;
+    int64_t lo, hi;
+    const int64_t q0 = rk_tile(b, s_base, t, &s, &lo, &hi);
+    const uint32_t* kwt = a.kw + t * (32 * kRWords);
+    uint32_t kbs[kRWords];
+#pragma unroll
+    for (int j = 0; j < kRWords; ++j) kbs[j] = kwt[32 * j + lane];
+#pragma unroll
+    for (int j = 0; j < kRWords; ++j) {
+      const uint32_t kb = kbs[j];
+      // rounds with a kept element anywhere in the warp, lowest first
+      const uint32_t any = __reduce_or_sync(kFull, kb);
+      uint32_t rounds = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) rounds |= ((any >> (4 * r)) & 0xFu) ? 1u << r : 0u;
+      while (rounds) {
+        const int r = __ffs(rounds) - 1;
+        rounds &= rounds - 1;
+        const uint32_t nib = (kb >> (4 * r)) & 0xFu;
+        const uint32_t n4 = __popc(nib);
+        const uint32_t incl = warp_incl_scan(n4);
+        int64_t p = pos + (incl - n4);
+        const int64_t i = 4 * (q0 + 32 * (8 * j + r) + lane);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int jl = (r0 + 4 + u) * 32 + (int)lane;
-          nxt[u] = jl < slen ? ep[jl] : 0.0f;
-        }
-      }
-      // quads of rounds r0 .. r0 + 3: from (i0 + 32 r0) / 4, at most 33
-      const int64_t first = i0 + (int64_t)r0 * 32;
-      const uint64_t q0 = (uint64_t)first >> 2;
-      __syncwarp();
-      {
-        uint64_t q = q0 + lane;
-        uint32_t w0 = (uint32_t)q, w1 = (uint32_t)(q >> 32), w2 = st0, w3 = st1;
-        philox4x32_10(w0, w1, w2, w3, k0, k1);
-        wb[lane * 4 + 0] = w0;
-        wb[lane * 4 + 1] = w1;
-        wb[lane * 4 + 2] = w2;
-        wb[lane * 4 + 3] = w3;
-        if ((first & 3) != 0 && lane == 0) {  // the 33rd quad
-          q = q0 + 32;
-          w0 = (uint32_t)q;
-          w1 = (uint32_t)(q >> 32);
-          w2 = st0;
-          w3 = st1;
-          philox4x32_10(w0, w1, w2, w3, k0, k1);
-          wb[128] = w0;
-          wb[129] = w1;
-          wb[130] = w2;
-          wb[131] = w3;
-        }
-      }
-      __syncwarp();
-      // element o of the group (o = 32 u + lane) is word (f + o) of the
-      // buffer, f = first % 4; u < min(1, x) is !(u >= x) for every x,
-      // since u < 1 (x >= 1, +Inf and a NaN product all keep)
-      const int f = (int)(first & 3);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int jl = (r0 + u) * 32 + (int)lane;
-        bool keep = false;
-        if (jl < slen) {
-          const uint32_t w = wb[f + u * 32 + (int)lane];
-          const float x = __fmul_rn(c, fabsf(gv[u]));
-          keep = !(__uint2float_rn(w >> 8) * 0x1p-24f >= x);
-        }
-        const uint32_t bal = __ballot_sync(kFull, keep);
-        if (lane == (unsigned)(r0 + u)) {
-          my_ballot = bal;
-          my_before = run;
-        }
-        run += __popc(bal);
-      }
-    }
-    if (lane == 0) s_wtot[warp] = run;
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t v = lane < kRWarps ? s_wtot[lane] : 0u;
-      const uint32_t incl = warp_incl_scan(v);
-      if (lane < kRWarps) s_woff[lane] = incl - v;
-      const uint32_t total = __shfl_sync(kFull, incl, 31);
-      const uint64_t ex = lookback_warp(a.tstate, t, 0, total, a.status);
-      if (lane == 0) {
-        s_excl = ex;
-        const int64_t tile_off = prev + (int64_t)ex;
-        const int64_t sent = max((int64_t)0, min((int64_t)total, a.capacity - tile_off));
-        if (sent) atomicAdd(&a.counts[d.id], (unsigned long long)sent);
-        if (tile_off + (int64_t)total > a.capacity) set_status(a.status, EF_ERR_CAPACITY);
-        if (t == tiles - 1) {
-          const int64_t all = tile_off + (int64_t)total;
-          a.ctl->base[a.parity ^ 1] = all;
-          a.counts[a.nseg_total] = (unsigned long long)min(all, a.capacity);
-        }
-      }
-    }
-    __syncthreads();
-    const int64_t slice_off = prev + (int64_t)s_excl + s_woff[warp];
-    if (run) {  // warp-uniform
-      const unsigned lm = lanemask_lt();
-      for (int x = 0; x < kRRounds; ++x) {
-        const uint32_t bal = __shfl_sync(kFull, my_ballot, x);
-        if (!bal) continue;  // warp-uniform
-        const uint32_t before = __shfl_sync(kFull, my_before, x);
-        if ((bal >> lane) & 1u) {
-          const int64_t pos = slice_off + before + __popc(bal & lm);
-          const int64_t jl = (int64_t)x * 32 + lane;
-          if (pos < a.capacity) {
-            a.out_values[pos] = ep[jl];
-            a.out_indices[pos] = (int32_t)(i0 + jl);
-            a.e[i0 + jl] = 0.0f;
+          if ((nib >> u) & 1u) {
+            if (p < a.capacity) {
+              a.out_values[p] = a.e[i + u];
+              a.out_indices[p] = (int32_t)(i + u);
+              a.e[i + u] = 0.0f;
+            }
+            ++p;
           }
         }
+        pos += __shfl_sync(kFull, incl, 31);
       }
     }
-    __syncthreads();
   }
 }
 
 struct RPlan {
   std::vector<RBatch> batches;
   int64_t max_tiles_b = 0;
-  size_t off_acc = 0, off_coef = 0, off_ctl = 0, off_tiles = 0, clear_bytes = 0, bytes = 0;
+  size_t off_acc = 0, off_coef = 0, off_ctl = 0, off_kw = 0, off_cnt = 0, off_csum = 0,
+         off_off = 0, bytes = 0;
 };
 
 ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* ks, RPlan* p) {
@@ -472,10 +631,12 @@ ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* k
     if (k < 0 || k > len) return EF_ERR_K;
     if (len == 0) continue;
     const int t = cur.nseg;
-    const int64_t tiles = (len + kRTile - 1) / kRTile;
+    // aligned blocks the segment meets, in each pass
+    const int64_t blocks_a = (b - 1) / kRTile - a / kRTile + 1;
+    const int64_t blocks_b = (b - 1) / kRSelTile - a / kRSelTile + 1;
     cur.seg[t] = RSeg{a, len, k, cur.tiles_a[t], cur.tiles_b[t], i};
-    cur.tiles_a[t + 1] = cur.tiles_a[t] + tiles;
-    cur.tiles_b[t + 1] = cur.tiles_b[t] + (k > 0 ? tiles : 0);
+    cur.tiles_a[t + 1] = cur.tiles_a[t] + blocks_a;
+    cur.tiles_b[t + 1] = cur.tiles_b[t] + (k > 0 ? blocks_b : 0);
     if (++cur.nseg == kRBatch) flush();
   }
   flush();
@@ -486,8 +647,15 @@ ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* k
   off = round_up(off + (size_t)kRBatch * kChunks * 8, 256);
   p->off_coef = off;
   off = round_up(off + (size_t)kRBatch * 4, 256);
-  p->off_tiles = off;
-  off = round_up(off + (size_t)std::max<int64_t>(p->max_tiles_b, 1) * 8, 256);
+  const size_t tb = (size_t)std::max<int64_t>(p->max_tiles_b, 1);
+  p->off_kw = off;
+  off = round_up(off + tb * 4 * 32 * kRWords, 256);
+  p->off_cnt = off;
+  off = round_up(off + tb * 4, 256);
+  p->off_csum = off;
+  off = round_up(off + (tb + kOffChunk - 1) / kOffChunk * 4, 256);
+  p->off_off = off;
+  off = round_up(off + (tb + 1) * 8, 256);
   p->bytes = off;
   return EF_OK;
 }
@@ -542,27 +710,55 @@ extern "C" ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, 
   RCtl* ctl = reinterpret_cast<RCtl*>(ws + p.off_ctl);
   uint64_t* acc = reinterpret_cast<uint64_t*>(ws + p.off_acc);
   float* coef = reinterpret_cast<float*>(ws + p.off_coef);
-  uint64_t* tstate = reinterpret_cast<uint64_t*>(ws + p.off_tiles);
-  RSelectArgs a{coef, e, out_values, out_indices, capacity,
-                reinterpret_cast<unsigned long long*>(d_counts), nseg, seed, step, tstate, ctl,
-                reinterpret_cast<int32_t*>(ws), 0};
+  RSelectArgs a{coef,
+                e,
+                out_values,
+                out_indices,
+                capacity,
+                reinterpret_cast<unsigned long long*>(d_counts),
+                nseg,
+                philox_keys(seed),
+                (uint32_t)step,
+                (uint32_t)(step >> 32),
+                reinterpret_cast<uint32_t*>(ws + p.off_kw),
+                reinterpret_cast<uint32_t*>(ws + p.off_cnt),
+                reinterpret_cast<uint32_t*>(ws + p.off_csum),
+                reinterpret_cast<int64_t*>(ws + p.off_off),
+                ctl,
+                reinterpret_cast<int32_t*>(ws),
+                0};
+  // 16-byte accesses: pass 1 needs both arrays aligned, pass 2 only e
+  const bool vec_e = (reinterpret_cast<uintptr_t>(e) & 15u) == 0;
+  const bool vec = vec_e && (reinterpret_cast<uintptr_t>(g_raw) & 15u) == 0;
   int parity = 0;
   for (const RBatch& b : p.batches) {
     a.parity = parity;
     parity ^= 1;
-    err = cudaMemsetAsync(acc, 0, (size_t)kRBatch * kChunks * 8, s);
-    if (err == cudaSuccess) err = cudaMemsetAsync(tstate, 0, (size_t)std::max<int64_t>(b.tiles_b[b.nseg], 1) * 8, s);
-    if (err == cudaSuccess) err = cudaMemsetAsync(&ctl->ticket, 0, 4, s);
-    if (err != cudaSuccess) return cuda_fail(err);
     const int64_t ta = b.tiles_a[b.nseg], tb = b.tiles_b[b.nseg];
+    const int64_t nchunks = std::max<int64_t>(1, (tb + kOffChunk - 1) / kOffChunk);
+    err = cudaMemsetAsync(acc, 0, (size_t)kRBatch * kChunks * 8, s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(a.csum, 0, (size_t)nchunks * 4, s);
+    if (err != cudaSuccess) return cuda_fail(err);
     const int ga = (int)std::max<int64_t>(1, std::min<int64_t>(ta, (int64_t)dev.sms * 4));
-    rk_sum<<<ga, kRT, 0, s>>>(b, g_raw, e, acc);
+    if (vec) rk_sum<true><<<ga, kRT, 0, s>>>(b, g_raw, e, acc);
+    else rk_sum<false><<<ga, kRT, 0, s>>>(b, g_raw, e, acc);
     if ((st = check_launch()) != EF_OK) return st;
     rk_finalize<<<1, kRBatch, 0, s>>>(b, acc, coef);
     if ((st = check_launch()) != EF_OK) return st;
+    const int64_t warps = (tb + kRWarps - 1) / kRWarps;
     if (tb > 0) {
-      const int gb = (int)std::max<int64_t>(1, std::min<int64_t>(tb, (int64_t)dev.sms * 6));
-      rk_select<<<gb, kRT, 0, s>>>(b, a);
+      const int gd =
+          (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * kDrawCtas));
+      if (vec_e) rk_draw<true><<<gd, kRT, 0, s>>>(b, a);
+      else rk_draw<false><<<gd, kRT, 0, s>>>(b, a);
+      if ((st = check_launch()) != EF_OK) return st;
+    }
+    // always: it carries the running offset to the next launch
+    rk_offsets<<<(unsigned)nchunks, kRT, 0, s>>>(tb, a);
+    if ((st = check_launch()) != EF_OK) return st;
+    if (tb > 0) {
+      const int gp = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 8));
+      rk_pack<<<gp, kRT, 0, s>>>(b, a);
       if ((st = check_launch()) != EF_OK) return st;
     }
   }

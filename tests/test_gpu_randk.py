@@ -125,3 +125,31 @@ def test_randk_count_statistics():
     p = np.minimum(1.0, c * np.abs(gn).astype(np.float64))
     mean, var = p.sum(), np.sum(p * (1 - p))
     assert abs(np.mean(cnts) - mean) < 5 * np.sqrt(var / 40)
+
+
+def test_randk_block_edges_and_unaligned_residual():
+    """Segments that start inside a quad of four elements and straddle the
+    aligned 32768-element blocks, segments shorter than a quad, dense keep
+    fractions, and a residual buffer that is only 4-byte aligned (the
+    element-wise load path)."""
+    sizes = [3, 5, 32_765, 32_768, 32_771, 1, 2, 65_549, 4, 100_000, 6]
+    ks = [3, 2, 16_000, 300, 30_000, 1, 0, 650, 4, 99_000, 3]
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    for shift in (0, 1, 3):
+        g_big = _t(n + 4, 30 + shift)
+        e_big = _t(n + 4, 40 + shift, 1e-4)
+        g, e = g_big[shift:shift + n], e_big[shift:shift + n]
+        check_randk(g, e, offs, ks, seed=77 + shift, step=shift)
+
+
+def test_randk_launch_without_draws_carries_the_packet_offset():
+    """Segments go to the device in groups of 128; a group whose segments
+    all have k = 0 draws nothing, and the packet positions of the groups
+    after it still follow on from the groups before it."""
+    rng = np.random.default_rng(12)
+    sizes = [int(x) for x in rng.integers(1, 4000, 400)]
+    ks = [0 if 128 <= i < 256 else max(1, s // 25) for i, s in enumerate(sizes)]
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    check_randk(_t(n, 13), _t(n, 14, 1e-4), offs, ks, seed=8, step=5)
