@@ -791,8 +791,9 @@ def run_next(args, dev):
         "workload": f"one tensor of {n} elements, expected k = {k}",
         "ms_per_call": ms_rk, "kept_last_call": kept,
         "algorithmic_bytes": rk_bytes,
-        "note": "two passes: 12 B/element (compensate + exact sum of |g|) and 4 B/element "
-                "(draws + ordered packet) + 8 B per kept element",
+        "note": "algorithmic: 12 B/element (compensate + exact sum of |g|), 4 B/element "
+                "(draws) and 8 B per kept element; the keep bits add 1/4 B/element "
+                "(written, then re-read by the packing pass)",
         "gbs": rk_bytes / (ms_rk * 1e-3) / 1e9,
         "g_elems_per_s": n / ms_rk / 1e6,
         "cpu_baseline": {"g_elems_per_s": sample / dt / 1e9, "cores": 1, "kind": "oracle",

@@ -152,15 +152,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // Called by all 32 lanes of ONE warp.  `states` indexes tiles globally;
 // the chain of this tile starts at `first` (exclusive prefix 0 there).
 // Publishes this tile's aggregate, looks back, publishes the inclusive prefix
-// and returns the exclusive prefix (same value in every lane).  A wait sleeps
-// 32 ns between polls, doubling up to `max_sleep_ns`: callers whose waiting
-// warps share the SM with working ones pass a longer cap so that the polls
-// do not take their issue slots.
+// and returns the exclusive prefix (same value in every lane).
 __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile,
                                                   int64_t first, uint64_t agg,
                                                   int32_t* status,
-                                                  uint64_t limit_ns = kWaitLimitNs,
-                                                  uint32_t max_sleep_ns = 32) {
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   const unsigned lane = lane_id();
   if (tile == first) {
     if (lane == 0) st_release(&states[tile], kFlagIncl | agg);
@@ -174,7 +170,7 @@ __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile
   while (base >= first) {
     const int64_t t = base - (int64_t)lane;
     uint64_t s = (t >= first) ? ld_acquire(&states[t]) : kFlagIncl;
-    uint32_t spins = 0, nap = 32;
+    uint32_t spins = 0;
     while (__any_sync(kFull, (s >> 62) == 0)) {
       if ((s >> 62) == 0) s = ld_acquire(&states[t]);
       if ((++spins & 63u) == 0) {
@@ -189,8 +185,7 @@ __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile
           break;
         }
       }
-      __nanosleep(nap);
-      if (nap < max_sleep_ns) nap <<= 1;
+      __nanosleep(32);
     }
     if (gave_up) break;
     const unsigned incl = __ballot_sync(kFull, (s >> 62) == 2);
