@@ -806,8 +806,12 @@ def run_next(args, dev):
 def run_case(args):
     """One entry point alone, three calls, for profiling its kernels in
     isolation (--case): 'topk' (one tensor of n elements, top-0.1 %),
-    'aggregate' (4 workers' int32 packets of 0.1 % over n, with G and SGD)
-    or 'randk' (random sparsification of one tensor, expected 0.1 %)."""
+    'aggregate' (4 workers' int32 packets of 0.1 % over n, with G and SGD),
+    'randk' (random sparsification of one tensor, expected 0.1 %), 'sign'
+    (1-bit compression of 4 workers' gradients of n elements, then their
+    sign aggregate with G and SGD), 'q8' (top-0.1 % with 8-bit values, then
+    the receiver's dequantisation) or 'codec' (a top-0.1 % packet of n
+    elements encoded and decoded with each index codec)."""
     import torch
     import error_feedback_gradient_gb300 as efg
     from error_feedback_gradient_gb300 import workloads as wl
@@ -837,7 +841,7 @@ def run_case(args):
                          device=dev)
         for _ in range(3):
             efg.sparse_aggregate_apply(vals, ix, None, [k] * W, n, 0.1, G, w, ws)
-    else:
+    elif args.case == "randk":
         g = wl.student_t3(n, 1e-3, 1, dev)
         e = torch.zeros_like(g)
         v = torch.empty(2 * k, device=dev)
@@ -846,8 +850,50 @@ def run_case(args):
         ws = torch.empty(efg.randk_workspace_size(n, [0, n], [k]), dtype=torch.uint8, device=dev)
         for step in range(3):
             efg.randk_compress(g, e, [0, n], [k], 7, step, v, ix, cnt, ws)
+    elif args.case == "sign":
+        W = 4
+        g = wl.student_t3(n, 1e-3, 1, dev)
+        eps = torch.zeros_like(g)
+        bits = [torch.empty((n + 31) // 32, dtype=torch.int32, device=dev) for _ in range(W)]
+        G = torch.empty(n, device=dev)
+        w = torch.zeros(n, device=dev)
+        for _ in range(3):
+            for b in bits:
+                efg.sign_compress(g, eps, 0.9, b)
+            efg.sign_aggregate_apply(bits, n, efg.APPLY_SGD, 0.1, 0.9, G, w)
+    elif args.case == "q8":
+        g = wl.student_t3(n, 1e-3, 1, dev)
+        e = wl.normal(n, 1e-4, 2, dev)
+        q = torch.empty(k, dtype=torch.int8, device=dev)
+        sc = torch.empty(1, device=dev)
+        ix = torch.empty(k, dtype=torch.int32, device=dev)
+        v = torch.empty(k, device=dev)
+        ws = torch.empty(efg.topk_q8_workspace_size(n, [0, n], [k]), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            efg.topk_compress_q8(g, e, [0, n], [k], q, sc, ix, None, ws)
+            efg.q8_dequantize(q, sc, [k], v)
+    else:
+        g = wl.student_t3(n, 1e-3, 1, dev)
+        e = torch.zeros_like(g)
+        v = torch.empty(k, device=dev)
+        ix = torch.empty(k, dtype=torch.int32, device=dev)
+        ws = torch.empty(efg.topk_workspace_size(n, [0, n], [k]), dtype=torch.uint8, device=dev)
+        efg.topk_compress(g, e, [0, n], [k], v, ix, None, ws)
+        back = torch.empty(k, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            for codec in (efg.CODEC_LOCAL16, efg.CODEC_RUNVARINT, efg.CODEC_BLOCK256):
+                mb, wb = efg.index_codec_sizes(codec, k, n)
+                out = torch.empty((mb + 3) // 4, dtype=torch.int32, device=dev)
+                ob = torch.zeros(1, dtype=torch.int64, device=dev)
+                cws = torch.empty(wb, dtype=torch.uint8, device=dev)
+                efg.index_encode(codec, ix, n, out, ob, cws)
+                efg.index_decode(codec, out, int(ob.item()), k, n, back, cws)
+                if not torch.equal(back, ix):
+                    raise SystemExit(f"codec {codec}: round trip differs")
     torch.cuda.synchronize()
-    print(json.dumps({"case": args.case, "n": n, "k": k, "status": efg.workspace_status(ws)}))
+    status = 0 if args.case == "sign" else efg.workspace_status(ws)
+    print(json.dumps({"case": args.case, "n": n, "k": k, "status": status}))
 
 
 def main(argv=None):
@@ -870,7 +916,8 @@ def main(argv=None):
     p.add_argument("--traffic-per-launch", type=float, default=None,
                    help="DRAM bytes of one topk_fused launch at this size, from ncu")
     p.add_argument("--no-extras", dest="extras", action="store_false")
-    p.add_argument("--case", choices=["topk", "aggregate", "randk"], default=None,
+    p.add_argument("--case", choices=["topk", "aggregate", "randk", "sign", "q8", "codec"],
+                   default=None,
                    help="run one entry point alone (three calls at --n) for profiling")
     args = p.parse_args(argv)
     if args.case:
