@@ -59,10 +59,12 @@ def test_sign_zero_is_plus_one():
     assert host(bits).view(np.uint32)[0] == 0b0111_0111_0111_0111_0111_0111_0111_0111
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 6, 7, 8, 9, 64])
 @pytest.mark.parametrize("mode", [efg.APPLY_SGD, efg.APPLY_MOMENTUM])
 @pytest.mark.parametrize("n", [33, 4097, 1_000_003])
 def test_sign_aggregate(W, mode, n):
+    """Worker counts 1 to 9 and the maximum 64, sizes below one float4
+    chunk's word and with ragged tails."""
     bits, wants = [], []
     for w in range(W):
         g = wl.normal(n, 1e-3, 50 + w, DEV)
