@@ -215,6 +215,23 @@ class SlabStep:
         self.ws_ab = torch.empty(efg.aggregate_workspace_size(workers, efg.IDX_BITMAP, n),
                                  dtype=u8, device=dev)
         self.prof = None   # list of (kernel_id, start_event, stop_event) filled per launch
+        self.streams = None
+
+    def use_worker_streams(self):
+        """Run each worker's three compress calls on a stream of its own, so
+        that one worker's short selection and packing kernels overlap the
+        other workers' streaming passes; the three aggregates stay on the
+        caller's stream, each after the packets it reads.  Each worker gets
+        its own top-k workspaces."""
+        torch, efg = self.torch, self.efg
+        u8 = torch.uint8
+        self.streams = [torch.cuda.Stream() for _ in range(self.W)]
+        self.ws_int_w = [self.ws_int] + [torch.empty_like(self.ws_int) for _ in range(self.W - 1)]
+        self.ws_bm_w = [self.ws_bm] + [torch.empty_like(self.ws_bm) for _ in range(self.W - 1)]
+        ev = lambda: [torch.cuda.Event() for _ in range(self.W)]   # noqa: E731
+        self.ev_fork = torch.cuda.Event()
+        self.ev_int, self.ev_bm, self.ev_sign = ev(), ev(), ev()
+        del u8, efg
 
     # units and algorithmic bytes --------------------------------------------
     @property
@@ -247,6 +264,8 @@ class SlabStep:
         self.prof.append((kernel_id, a, b))
 
     def step(self):
+        if self.streams is not None and self.prof is None:
+            return self._step_streams()
         efg = self.efg
         for w in range(self.W):
             self._hook(efg.binding.KERNEL_TOPK_FUSED)
@@ -269,12 +288,42 @@ class SlabStep:
         efg.sign_aggregate_apply(self.bits, self.n, efg.APPLY_SGD, self.wl.eta, self.wl.beta1,
                                  self.G, self.w_sign)
 
+    def _step_streams(self):
+        torch, efg = self.torch, self.efg
+        main = torch.cuda.current_stream()
+        self.ev_fork.record(main)
+        for w, st in enumerate(self.streams):
+            st.wait_event(self.ev_fork)
+            with torch.cuda.stream(st):
+                efg.topk_compress(self.g[w], self.e_int[w], self.offs, self.ks,
+                                  self.vals_int[w], self.idx_int[w], None, self.ws_int_w[w],
+                                  efg.IDX_INT32)
+                self.ev_int[w].record(st)
+                efg.topk_compress(self.g[w], self.e_bm[w], self.offs, self.ks, self.vals_bm[w],
+                                  None, self.bm[w], self.ws_bm_w[w], efg.IDX_BITMAP)
+                self.ev_bm[w].record(st)
+                efg.sign_compress(self.g[w], self.eps[w], self.wl.beta1, self.bits[w])
+                self.ev_sign[w].record(st)
+        for ev in self.ev_int:
+            main.wait_event(ev)
+        efg.sparse_aggregate_apply(self.vals_int, self.idx_int, None, [self.k] * self.W, self.n,
+                                   self.wl.eta, self.G, self.w_int, self.ws_ai, efg.IDX_INT32)
+        for ev in self.ev_bm:
+            main.wait_event(ev)
+        efg.sparse_aggregate_apply(self.vals_bm, None, self.bm, [self.k] * self.W, self.n,
+                                   self.wl.eta, self.G, self.w_bm, self.ws_ab, efg.IDX_BITMAP)
+        for ev in self.ev_sign:
+            main.wait_event(ev)
+        efg.sign_aggregate_apply(self.bits, self.n, efg.APPLY_SGD, self.wl.eta, self.wl.beta1,
+                                 self.G, self.w_sign)
+
     def clear_hooks(self):
         for kid in (1, 2, 3, 4):
             self.efg.binding.profile_events(kid, None, None)
 
     def check_status(self):
-        for ws in (self.ws_int, self.ws_bm, self.ws_ai, self.ws_ab):
+        extra = (self.ws_int_w[1:] + self.ws_bm_w[1:]) if self.streams is not None else []
+        for ws in [self.ws_int, self.ws_bm, self.ws_ai, self.ws_ab] + extra:
             st = self.efg.workspace_status(ws)
             if st != 0:
                 raise RuntimeError(f"device status {st}")
@@ -373,6 +422,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     efg.library()
     s = SlabStep(args.n, args.workers, dev)
+    if args.worker_streams == "on":
+        s.use_worker_streams()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         s.step()
@@ -446,6 +497,9 @@ def run_ours(args, rank, world, local):
         "config": {"workload": args.workload_desc, "n": args.n, "workers": args.workers,
                    "k": s.k, "variants": ["topk_int32", "topk_bitmap", "sign_1bit"],
                    "units_per_step": s.units, "parallelism": "replicas",
+                   "schedule": ("compress calls on one stream per worker, aggregates on the "
+                                "caller's stream; per-kernel times from a serial step"
+                                if args.worker_streams == "on" else "one stream"),
                    "l2": "inputs larger than L2 (no flush)"},
         "step_hbm": {"algorithmic_bytes": step_bytes,
                      "gbs": step_bytes / (ms_max * 1e-3) / 1e9,
@@ -906,6 +960,9 @@ def main(argv=None):
     p.add_argument("--workers", type=int, default=4)
     p.add_argument("--prof-steps", type=int, default=2)
     p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--worker-streams", choices=["on", "off"], default="on",
+                   help="on: each worker's compress calls on a stream of its own; "
+                        "off: the whole step on one stream")
     p.add_argument("--e2e-mode", choices=["pipelined", "serial"], default="pipelined",
                    help="pipelined: uploads double-buffered against compute on their own "
                         "streams; serial: upload, step, download in turn")
