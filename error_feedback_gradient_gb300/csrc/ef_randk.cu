@@ -13,21 +13,24 @@
 // Shaw, SC 2011): ten rounds of two 32x32->64 multiplies by 0xD2511F53 and
 // 0xCD9E8D57, the key bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.
 //
-// Pass 1 (rk_sum, 12 B / element) writes g = g_raw + e over e and sums |g|
-// exactly: a float32 magnitude is m * 2^(sh - 149) with m < 2^24 and
-// 0 <= sh <= 253, so each thread keeps four 128-bit integer accumulators,
-// one per 64-bit-aligned group of sh, and a CTA flushes them as 40-bit
-// carry-save chunks with one atomicAdd per chunk when it leaves a segment
-// (sums of at most 2^14 flushes of 2^50 fit in 64 bits).  rk_finalize turns
-// each segment's chunks into the float64 nearest the exact sum and forms c.
-// Pass 2 draws and packs in three launches with no wait between warps:
-// rk_draw (4 B / element + 1/8 B of keep bits) walks the aligned
-// 4096-element blocks of each segment, a warp per block and each lane taking
-// one quad of four elements (one Philox call, one 16-byte load), and writes
-// the block's keep bits and count; rk_offsets turns the counts into packet
-// offsets (the running offset carries across launches); rk_pack re-reads the
-// keep bits and writes the kept elements in index order (8 B per kept
-// element, + its residual write).
+// The draws u_i do not depend on g, and RN32(c |g_i|) never decreases as c
+// grows, so for any c_max >= c every kept element passes the keep test at
+// c_max.  The passes use that to read g once:
+//   rk_sample sums |g| over a block sample of each long segment; c_max is
+//     twice the coefficient that sum predicts (+Inf for short segments);
+//   rk_sum (12 B / element + 1/8 B of candidate bits) writes g = g_raw + e
+//     over e, sums |g| exactly and, with one Philox call per quad of four
+//     elements, sets a candidate bit where u_i < RN32(c_max |g_i|);
+//   rk_finalize rounds the exact sum, forms c and checks c <= c_max;
+//   rk_refine re-tests the candidates at c (every element of a segment where
+//     c > c_max or c_max is +Inf) and leaves the exact keep bits and counts;
+//   rk_offsets turns the counts into packet offsets (the running offset
+//     carries across launches) and rk_pack writes the packet in index order.
+// The exact sum: a float32 magnitude is m * 2^(sh - 149) with m < 2^24 and
+// 0 <= sh <= 253; each thread keeps a 128-bit integer accumulator per
+// 64-bit-aligned group of sh, and a CTA flushes them as 40-bit carry-save
+// chunks with one atomicAdd per chunk when it leaves a segment (sums of at
+// most 2^14 flushes of 2^50 fit in 64 bits).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,24 +42,35 @@
 namespace ef {
 namespace {
 
-constexpr int kRT = 256;                // threads per CTA
-constexpr int kRPer = 32;               // elements per thread per tile
-constexpr int kRTile = kRT * kRPer;     // 8192 elements per tile
-constexpr int kRBatch = 128;            // segments per launch
-constexpr int kChunks = 8;              // 40-bit chunks of an exact sum (320 bits)
+constexpr int kRT = 256;                   // threads per CTA
+constexpr int kRTile = 8192;               // elements per tile (aligned blocks of the tensor)
+constexpr int kRTileWords = kRTile / 32;   // 256 keep words per tile
+constexpr int kRBatch = 128;               // segments per launch
+constexpr int kChunks = 8;                 // 40-bit chunks of an exact sum (320 bits)
 constexpr uint64_t kMask40 = (1ull << 40) - 1;
+constexpr int kSampleBlock = 64;           // elements per sampled block
+constexpr int kSampleBlocksMax = 2048;     // sampled blocks per segment
+constexpr int64_t kSampleMinLen = 65536;   // shorter segments test every element at c
+constexpr int kOffChunk = 8192;            // tiles per rk_offsets CTA
+constexpr int kOffPer = kOffChunk / kRT;   // 32 tiles per thread
 
 struct RSeg {
   int64_t off, len, k;
-  int64_t tile_a;  // first tile of the segment in pass 1
-  int64_t tile_b;  // first tile in pass 2 (segments with k = 0 have none)
-  int32_t id;      // segment number in the whole call
+  int64_t sblk;   // first sample block of the segment in the launch
+  int32_t nsamp;  // sampled blocks (0: c_max = +Inf)
+  int32_t id;     // segment number in the whole call
 };
 
+// Tiles are the aligned 8192-element blocks of the tensor cut to one
+// segment: tile t of segment s covers [max(off, B), min(off + len, B + 8192))
+// with B = (off / 8192 + t - tiles[s]) * 8192, so every quad of four
+// elements (one Philox counter) lies in one tile.  Keep word x (0..255) of a
+// tile holds quads B / 4 + x + 256 u (u = 0..7), element j of quad u at bit
+// 4 u + j.
 struct RBatch {
   RSeg seg[kRBatch];
-  int64_t tiles_a[kRBatch + 1];  // prefix of pass-1 tiles; [nseg] = total
-  int64_t tiles_b[kRBatch + 1];
+  int64_t tiles[kRBatch + 1];  // prefix of tiles; [nseg] = total
+  int64_t samp[kRBatch + 1];   // prefix of sampled blocks
   int32_t nseg;
 };
 
@@ -75,7 +89,133 @@ __device__ __forceinline__ int find_tile_seg(const int64_t* base, int nseg, int6
   return lo;
 }
 
-// ---------------------------------------------------------------- exact sum
+// First element of tile t's aligned block, and the tile's bounds [lo, hi).
+__device__ __forceinline__ uint32_t tile_bounds(const RSeg& d, int64_t first_tile, int64_t t,
+                                                uint32_t* lo, uint32_t* hi) {
+  const int64_t sa = (d.off / kRTile + (t - first_tile)) * kRTile;
+  *lo = (uint32_t)max(d.off, sa);
+  *hi = (uint32_t)min(d.off + d.len, sa + kRTile);
+  return (uint32_t)sa;
+}
+
+// ---------------------------------------------------------------- draws
+
+// Round keys of Philox4x32-10 for one key: key word 0 and 1 of round r are
+// (seed low + r 0x9E3779B9, seed high + r 0xBB67AE85) mod 2^32.  Passed by
+// value to the kernels, so a round reads them as constant operands.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
+// The four words of Philox4x32-10 at counter (q, 0, st0, st1): the counter's
+// high word (quad index / 2^32) is 0 for every quad of an int32-indexed
+// tensor.
+__device__ __forceinline__ void philox_quad(uint32_t q, uint32_t st0, uint32_t st1,
+                                            const PhiloxKeys& k, uint32_t w[4]) {
+  uint32_t c0 = q, c1 = 0, c2 = st0, c3 = st1;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;  // one 32x32->64 multiply each
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    c0 = (uint32_t)(p1 >> 32) ^ c1 ^ k.k0[r];
+    c1 = (uint32_t)p1;
+    c2 = (uint32_t)(p0 >> 32) ^ c3 ^ k.k1[r];
+    c3 = (uint32_t)p0;
+  }
+  w[0] = c0;
+  w[1] = c1;
+  w[2] = c2;
+  w[3] = c3;
+}
+
+// u < min(1, x) is !(u >= x) for every x, since u < 1 (x >= 1, +Inf and a
+// NaN product all keep).
+__device__ __forceinline__ bool rk_keep(uint32_t w, float c, float g) {
+  const float x = __fmul_rn(c, fabsf(g));
+  return !(__uint2float_rn(w >> 8) * 0x1p-24f >= x);
+}
+
+// Keep bits of one quad at coefficient c, element j at bit j, restricted to
+// `mask`.
+__device__ __forceinline__ uint32_t quad_keep(const float v[4], const uint32_t w[4], float c,
+                                              uint32_t mask) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (((mask >> j) & 1u) && rk_keep(w[j], c, v[j])) bits |= 1u << j;
+  return bits;
+}
+
+// c_max of a segment from its sampled sum: twice the coefficient the sample
+// predicts, rounded up; +Inf when the segment is not sampled or its sample
+// sums to 0.  rk_sum and rk_finalize evaluate the same expression.
+__device__ __forceinline__ float seg_cmax(const RSeg& d, double ssum) {
+  if (d.nsamp == 0 || !(ssum > 0.0)) return __int_as_float(0x7F800000);
+  const double m = (double)d.nsamp * kSampleBlock;
+  return __double2float_ru(__ddiv_rn(2.0 * (double)d.k * m, (double)d.len * ssum));
+}
+
+struct RSelectArgs {
+  float* coef;
+  int32_t* mode;     // per segment: 1 = candidate bits hold every kept element
+  const double* ssum;
+  float* e;
+  float* out_values;
+  int32_t* out_indices;
+  int64_t capacity;
+  unsigned long long* counts;  // [nseg + 1] of the whole call
+  int32_t nseg_total;
+  PhiloxKeys keys;
+  uint32_t st0, st1;  // step low, high: counter words 2 and 3
+  uint32_t* kw;       // keep words, kRTileWords per tile
+  uint32_t* cnt;      // kept elements per tile
+  uint32_t* csum;     // kept elements per chunk of kOffChunk tiles
+  int64_t* off;       // [tiles + 1] packet position of each tile's first kept element
+  RCtl* ctl;
+  int32_t* status;
+  int parity;  // launch number % 2
+};
+
+// Sampled sum of |g_raw + e| over the finite elements of up to 2048 blocks
+// of 64 per long segment (block b starts b * (len / nsamp) into it), one
+// warp per block, added into ssum[s] in float64.  It only sets c_max.
+__global__ void __launch_bounds__(kRT)
+rk_sample(RBatch b, const float* __restrict__ g_raw, const float* __restrict__ e,
+          double* ssum) {
+  __shared__ int64_t s_base[kRBatch + 1];
+  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.samp[i];
+  __syncthreads();
+  const unsigned lane = lane_id();
+  const int64_t total = s_base[b.nseg];
+  for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < total;
+       blk += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int s = find_tile_seg(s_base, b.nseg, blk);
+    const RSeg& d = b.seg[s];
+    const int64_t i0 = d.off + (blk - s_base[s]) * (d.len / d.nsamp);
+    float a = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kSampleBlock / 32; ++u) {
+      const int64_t i = i0 + 32 * u + lane;
+      const float m = fabsf(__fadd_rn(g_raw[i], e[i]));
+      if (m < __int_as_float(0x7F800000)) a += m;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
+    if (lane == 0 && a > 0.0f) atomicAdd(&ssum[s], (double)a);
+  }
+}
 
 // Group 1 of a thread's accumulator (magnitudes in [2^-62, 4), where
 // gradients live) is held in registers; groups 0, 2 and 3 in the thread's
@@ -126,6 +266,23 @@ __device__ __forceinline__ void acc_add(uint64_t& lo1, uint64_t& hi1, AccSlow& s
   }
 }
 
+// Magnitudes with biased exponent E in [97, 129) (|x| in [2^-30, 4): sh in
+// [96, 128), bits 32..63 of group 1) are added as M << (E - 97) into a
+// 64-bit window accumulator; at most 32 of them (< 2^60) between folds.
+// Others take acc_add.
+__device__ __forceinline__ void acc_add_window(uint64_t& win, uint64_t& lo1, uint64_t& hi1,
+                                               AccSlow& slow, uint32_t bits) {
+  const uint32_t d = (bits >> 23) - 97u;
+  if (d < 32u) win += (uint64_t)((bits & 0x7FFFFFu) | 0x800000u) << d;
+  else acc_add(lo1, hi1, slow, bits);
+}
+
+// Folds the window accumulator into group 1 (at bit 32) and clears it.
+__device__ __forceinline__ void acc_fold_window(uint64_t& win, uint64_t& lo1, uint64_t& hi1) {
+  add128(lo1, hi1, win << 32, win >> 32);
+  win = 0;
+}
+
 // Bits [pos, pos + 40) of the 128-bit value hi:lo (pos may be negative).
 __device__ __forceinline__ uint64_t bits40(uint64_t hi, uint64_t lo, int pos) {
   if (pos <= -40 || pos >= 128) return 0;
@@ -172,39 +329,47 @@ __device__ void acc_flush(uint64_t& lo1, uint64_t& hi1, AccSlow& slow, uint64_t*
   __syncthreads();
 }
 
-// Pass 1: g = g_raw + e written over e; exact sum of the finite |g|.  Tiles
-// are the aligned 8192-element blocks of the whole tensor cut to one
-// segment, strided over the grid; a whole tile with 16-byte aligned buffers
-// moves as float4 quads (thread x takes quads x + 256 u), four quads of each
-// array in flight per thread; other tiles go element by element.
+// Pass 1: g = g_raw + e written over e; exact sum of the finite |g|; the
+// candidate bits at c_max.  A CTA takes whole tiles, strided over the grid:
+// thread x takes quads x + 256 u of the tile (u = 0..7), so it writes keep
+// word x.  A whole tile with 16-byte aligned buffers moves as float4 quads,
+// four quads of each array in flight per thread; other tiles go element by
+// element.
 template <bool kVec>
-__global__ void __launch_bounds__(kRT, 4)
-rk_sum(RBatch b, const float* __restrict__ g_raw, float* __restrict__ e, uint64_t* acc) {
+__global__ void __launch_bounds__(kRT, 3)
+rk_sum(RBatch b, const float* __restrict__ g_raw, float* __restrict__ e, uint64_t* acc,
+       RSelectArgs a) {
   __shared__ int64_t s_base[kRBatch + 1];
   __shared__ uint64_t red[kRT / 32][kChunks];
   __shared__ AccSlow slow;
-  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_a[i];
+  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles[i];
 #pragma unroll
   for (int x = 0; x < 3; ++x) slow.v[x][0][threadIdx.x] = slow.v[x][1][threadIdx.x] = 0;
   __syncthreads();
   const int64_t tiles = s_base[b.nseg];
   uint64_t lo1 = 0, hi1 = 0;
   int cur = -1;
+  float cmax = 0.0f;
+  bool draw = false;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     const int s = find_tile_seg(s_base, b.nseg, t);
     if (s != cur) {  // uniform across the CTA
       if (cur >= 0) acc_flush(lo1, hi1, slow, acc + (int64_t)cur * kChunks, red);
       cur = s;
+      cmax = seg_cmax(b.seg[s], a.ssum[s]);
+      draw = b.seg[s].k > 0 && cmax < __int_as_float(0x7F800000);
     }
     const RSeg& d = b.seg[s];
-    const int64_t sa = (d.off / kRTile + (t - s_base[s])) * kRTile;
-    const uint32_t lo = (uint32_t)max(d.off, sa), hi = (uint32_t)min(d.off + d.len, sa + kRTile);
-    const uint32_t a0 = (uint32_t)sa;
+    uint32_t lo, hi;
+    const uint32_t a0 = tile_bounds(d, s_base[s], t, &lo, &hi);
+    const uint32_t q0 = a0 >> 2;
+    uint32_t word = 0;
+    uint64_t win = 0;
     if (kVec && lo == a0 && hi == a0 + kRTile) {
-      const float4* g4 = reinterpret_cast<const float4*>(g_raw) + (a0 >> 2);
-      float4* e4 = reinterpret_cast<float4*>(e) + (a0 >> 2);
+      const float4* g4 = reinterpret_cast<const float4*>(g_raw) + q0;
+      float4* e4 = reinterpret_cast<float4*>(e) + q0;
 #pragma unroll 1
-      for (int r0 = 0; r0 < kRTile / 4 / kRT; r0 += 4) {
+      for (int r0 = 0; r0 < 8; r0 += 4) {
         float4 gv[4], ev[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -213,39 +378,48 @@ rk_sum(RBatch b, const float* __restrict__ g_raw, float* __restrict__ e, uint64_
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          float4 o;
-          o.x = __fadd_rn(gv[u].x, ev[u].x);
-          o.y = __fadd_rn(gv[u].y, ev[u].y);
-          o.z = __fadd_rn(gv[u].z, ev[u].z);
-          o.w = __fadd_rn(gv[u].w, ev[u].w);
-          __stcs(e4 + (r0 + u) * kRT + threadIdx.x, o);
-          acc_add(lo1, hi1, slow, __float_as_uint(o.x) & 0x7FFFFFFFu);
-          acc_add(lo1, hi1, slow, __float_as_uint(o.y) & 0x7FFFFFFFu);
-          acc_add(lo1, hi1, slow, __float_as_uint(o.z) & 0x7FFFFFFFu);
-          acc_add(lo1, hi1, slow, __float_as_uint(o.w) & 0x7FFFFFFFu);
+          float o[4];
+          o[0] = __fadd_rn(gv[u].x, ev[u].x);
+          o[1] = __fadd_rn(gv[u].y, ev[u].y);
+          o[2] = __fadd_rn(gv[u].z, ev[u].z);
+          o[3] = __fadd_rn(gv[u].w, ev[u].w);
+          __stcs(e4 + (r0 + u) * kRT + threadIdx.x, make_float4(o[0], o[1], o[2], o[3]));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            acc_add_window(win, lo1, hi1, slow, __float_as_uint(o[j]) & 0x7FFFFFFFu);
+          if (draw) {
+            uint32_t w[4];
+            philox_quad(q0 + (uint32_t)((r0 + u) * kRT) + threadIdx.x, a.st0, a.st1, a.keys, w);
+            word |= quad_keep(o, w, cmax, 0xFu) << (4 * (r0 + u));
+          }
         }
       }
     } else {
 #pragma unroll 1
-      for (int r0 = 0; r0 < kRTile / kRT; r0 += 8) {
-        float gv[8], ev[8];
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t q = q0 + (uint32_t)(u * kRT) + threadIdx.x;
+        float o[4];
+        uint32_t mask = 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t i = a0 + (uint32_t)((r0 + u) * kRT) + threadIdx.x;
-          gv[u] = i >= lo && i < hi ? __ldcs(g_raw + i) : 0.0f;
-          ev[u] = i >= lo && i < hi ? __ldcs(e + i) : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t i = a0 + (uint32_t)((r0 + u) * kRT) + threadIdx.x;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t i = 4 * q + j;
+          o[j] = 0.0f;
           if (i >= lo && i < hi) {
-            const float g = __fadd_rn(gv[u], ev[u]);
-            __stcs(e + i, g);
-            acc_add(lo1, hi1, slow, __float_as_uint(g) & 0x7FFFFFFFu);
+            o[j] = __fadd_rn(__ldcs(g_raw + i), __ldcs(e + i));
+            __stcs(e + i, o[j]);
+            acc_add_window(win, lo1, hi1, slow, __float_as_uint(o[j]) & 0x7FFFFFFFu);
+            mask |= 1u << j;
           }
+        }
+        if (draw && mask) {
+          uint32_t w[4];
+          philox_quad(q, a.st0, a.st1, a.keys, w);
+          word |= quad_keep(o, w, cmax, mask) << (4 * u);
         }
       }
     }
+    acc_fold_window(win, lo1, hi1);
+    if (draw) a.kw[t * kRTileWords + threadIdx.x] = word;
   }
   if (cur >= 0) acc_flush(lo1, hi1, slow, acc + (int64_t)cur * kChunks, red);
 }
@@ -299,191 +473,85 @@ __device__ double exact_to_double(const uint64_t* chunks) {
   return __longlong_as_double((long long)(((uint64_t)be << 52) | (mant & ((1ull << 52) - 1))));
 }
 
-__global__ void rk_finalize(RBatch b, const uint64_t* acc, float* coef) {
+__global__ void rk_finalize(RBatch b, const uint64_t* acc, RSelectArgs a) {
   const int s = threadIdx.x;
   if (s >= b.nseg) return;
   const double S = exact_to_double(acc + (int64_t)s * kChunks);
-  coef[s] = S > 0.0 ? __double2float_rn(__ddiv_rn((double)b.seg[s].k, S)) : 0.0f;
+  const float c = S > 0.0 ? __double2float_rn(__ddiv_rn((double)b.seg[s].k, S)) : 0.0f;
+  const float cmax = seg_cmax(b.seg[s], a.ssum[s]);
+  a.coef[s] = c;
+  a.mode[s] = (b.seg[s].k > 0 && cmax < __int_as_float(0x7F800000) && c <= cmax) ? 1 : 0;
 }
 
-// ---------------------------------------------------------------- pass 2
-
-// Round keys of Philox4x32-10 for one key: key word 0 and 1 of round r are
-// (seed low + r 0x9E3779B9, seed high + r 0xBB67AE85) mod 2^32.  Passed by
-// value to the kernels, so a round reads them as constant operands.
-struct PhiloxKeys {
-  uint32_t k0[10], k1[10];
-};
-
-PhiloxKeys philox_keys(uint64_t seed) {
-  PhiloxKeys k;
-  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
-  for (int r = 0; r < 10; ++r) {
-    k.k0[r] = a;
-    k.k1[r] = b;
-    a += 0x9E3779B9u;
-    b += 0xBB67AE85u;
-  }
-  return k;
-}
-
-// Two independent Philox4x32-10 calls, round by round.
-__device__ __forceinline__ void philox4x32_10x2(uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                                uint32_t& a3, uint32_t& b0, uint32_t& b1,
-                                                uint32_t& b2, uint32_t& b3, const PhiloxKeys& k) {
+// Candidate bits of keep word x: every element of the tile in [lo, hi).
+__device__ __forceinline__ uint32_t all_word(uint32_t q0, uint32_t x, uint32_t lo, uint32_t hi,
+                                             bool whole) {
+  if (whole) return 0xFFFFFFFFu;
+  uint32_t w = 0;
 #pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint64_t pa0 = (uint64_t)0xD2511F53u * a0, pa1 = (uint64_t)0xCD9E8D57u * a2;
-    const uint64_t pb0 = (uint64_t)0xD2511F53u * b0, pb1 = (uint64_t)0xCD9E8D57u * b2;
-    a0 = (uint32_t)(pa1 >> 32) ^ a1 ^ k.k0[r];
-    a1 = (uint32_t)pa1;
-    a2 = (uint32_t)(pa0 >> 32) ^ a3 ^ k.k1[r];
-    a3 = (uint32_t)pa0;
-    b0 = (uint32_t)(pb1 >> 32) ^ b1 ^ k.k0[r];
-    b1 = (uint32_t)pb1;
-    b2 = (uint32_t)(pb0 >> 32) ^ b3 ^ k.k1[r];
-    b3 = (uint32_t)pb0;
-  }
-}
-
-struct RSelectArgs {
-  const float* coef;
-  float* e;
-  float* out_values;
-  int32_t* out_indices;
-  int64_t capacity;
-  unsigned long long* counts;  // [nseg + 1] of the whole call
-  int32_t nseg_total;
-  PhiloxKeys keys;
-  uint32_t st0, st1;  // step low, high: counter words 2 and 3
-  uint32_t* kw;      // keep words: 128 per tile, word 32 j + l = lane l's word j
-  uint32_t* cnt;     // kept elements per tile
-  uint32_t* csum;    // kept elements per chunk of kOffChunk tiles
-  int64_t* off;      // [tiles + 1] packet position of each tile's first kept element
-  RCtl* ctl;
-  int32_t* status;
-  int parity;  // launch number % 2
-};
-
-// Pass-2 tiles are the aligned 4096-element blocks of the whole tensor
-// (global index / 4096) cut to one segment, so every quad of four elements
-// that shares a Philox counter lies in one tile.  A warp walks a tile's 1024
-// quads in 32 rounds of 32: in a round lane l takes quad 32 r + l, loads its
-// four elements at once (16 bytes when e is 16-byte aligned), computes its
-// one Philox call and sets four keep bits (bit 4 (r % 8) + u of word r / 8
-// for element u of the quad).
-constexpr int kRWarps = kRT / 32;
-constexpr int kRSelTile = 4096;                 // elements per pass-2 tile (one warp)
-constexpr int kRWords = kRSelTile / 1024;       // 4 keep words per lane
-constexpr int kDrawCtas = 5;                    // rk_draw CTAs per SM (48 registers)
-constexpr int kOffChunk = 8192;                 // tiles per rk_offsets CTA
-constexpr int kOffPer = kOffChunk / kRT;        // 32 tiles per thread
-
-// The four elements of quad q; with kAll every one of them is in the tile.
-// Element indices are below 2^31, so quads and elements fit 32 bits.
-template <bool kVec, bool kAll>
-__device__ __forceinline__ float4 rk_load_quad(const float* e, uint32_t q, uint32_t lo,
-                                               uint32_t hi) {
-  const uint32_t i = 4 * q;
-  if (kAll) {
-    if (kVec) return reinterpret_cast<const float4*>(e)[q];
-    return make_float4(e[i], e[i + 1], e[i + 2], e[i + 3]);
-  }
-  float4 v;
-  v.x = (i >= lo && i < hi) ? e[i] : 0.0f;
-  v.y = (i + 1 >= lo && i + 1 < hi) ? e[i + 1] : 0.0f;
-  v.z = (i + 2 >= lo && i + 2 < hi) ? e[i + 2] : 0.0f;
-  v.w = (i + 3 >= lo && i + 3 < hi) ? e[i + 3] : 0.0f;
-  return v;
-}
-
-// u < min(1, x) is !(u >= x) for every x, since u < 1 (x >= 1, +Inf and a
-// NaN product all keep).
-__device__ __forceinline__ bool rk_keep(uint32_t w, float c, float g) {
-  const float x = __fmul_rn(c, fabsf(g));
-  return !(__uint2float_rn(w >> 8) * 0x1p-24f >= x);
-}
-
-// Keep bits of quad q (element u at bit u).
-template <bool kAll>
-__device__ __forceinline__ uint32_t rk_quad_bits(uint32_t q, const float4& v, float c,
-                                                 uint32_t w0, uint32_t w1, uint32_t w2,
-                                                 uint32_t w3, uint32_t lo, uint32_t hi) {
-  bool k[4] = {rk_keep(w0, c, v.x), rk_keep(w1, c, v.y), rk_keep(w2, c, v.z),
-               rk_keep(w3, c, v.w)};
-  uint32_t bits = 0;
+  for (int u = 0; u < 8; ++u)
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (!kAll) k[u] = k[u] && 4 * q + u >= lo && 4 * q + u < hi;
-    if (k[u]) bits |= 1u << u;
-  }
-  return bits;
-}
-
-// Keep words of one tile starting at quad q0, written to kwt[32 j + lane];
-// returns the number of kept elements of this lane.  Two rounds at a time,
-// so that two independent Philox calls interleave.  The counter's high word
-// (quad index / 2^32) is 0 for every quad of an int32-indexed tensor.
-template <bool kVec, bool kAll>
-__device__ __forceinline__ uint32_t rk_slice(const float* e, uint32_t q0, uint32_t lo, uint32_t hi,
-                                             float c, const PhiloxKeys& keys, uint32_t st0,
-                                             uint32_t st1, uint32_t* kwt) {
-  const unsigned lane = lane_id();
-  uint32_t cnt = 0;
-#pragma unroll 1
-  for (int j = 0; j < kRWords; ++j) {
-    uint32_t kb = 0;
-#pragma unroll
-    for (int r = 0; r < 8; r += 2) {
-      const uint32_t qa = q0 + 32u * (8 * j + r) + lane, qb = qa + 32;
-      const float4 va = rk_load_quad<kVec, kAll>(e, qa, lo, hi);
-      const float4 vb = rk_load_quad<kVec, kAll>(e, qb, lo, hi);
-      uint32_t a0 = qa, a1 = 0, a2 = st0, a3 = st1;
-      uint32_t b0 = qb, b1 = 0, b2 = st0, b3 = st1;
-      philox4x32_10x2(a0, a1, a2, a3, b0, b1, b2, b3, keys);
-      kb |= rk_quad_bits<kAll>(qa, va, c, a0, a1, a2, a3, lo, hi) << (4 * r);
-      kb |= rk_quad_bits<kAll>(qb, vb, c, b0, b1, b2, b3, lo, hi) << (4 * r + 4);
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t i = 4 * (q0 + x + 256u * u) + j;
+      if (i >= lo && i < hi) w |= 1u << (4 * u + j);
     }
-    kwt[32 * j + lane] = kb;
-    cnt += __popc(kb);
-  }
-  return cnt;
+  return w;
 }
 
-// Tile t's segment and the bounds [lo, hi) of its elements; returns the
-// first quad of its aligned block.
-__device__ __forceinline__ int64_t rk_tile(const RBatch& b, const int64_t* s_base, int64_t t,
-                                           int* seg, int64_t* lo, int64_t* hi) {
-  const int s = find_tile_seg(s_base, b.nseg, t);
-  const RSeg& d = b.seg[s];
-  const int64_t sa = (d.off / kRSelTile + (t - s_base[s])) * kRSelTile;
-  *seg = s;
-  *lo = max(d.off, sa);
-  *hi = min(d.off + d.len, sa + kRSelTile);
-  return sa >> 2;
-}
-
-// Pass 2a: keep bits and counts, one warp per tile, tiles strided over the
-// grid's warps.
+// Pass 2a: exact keep bits and counts, one warp per tile, tiles strided over
+// the grid's warps.  Lane l re-tests the candidates of words l + 32 m at c:
+// per quad with a candidate, one Philox call and the candidates' values
+// from e (a 16-byte load for a whole quad when e is 16-byte aligned).
 template <bool kVec>
-__global__ void __launch_bounds__(kRT, kDrawCtas)
-rk_draw(RBatch b, RSelectArgs a) {
+__global__ void __launch_bounds__(kRT)
+rk_refine(RBatch b, RSelectArgs a) {
   __shared__ int64_t s_base[kRBatch + 1];
-  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_b[i];
+  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles[i];
   __syncthreads();
+  const unsigned lane = lane_id();
   const int64_t tiles = s_base[b.nseg];
-  for (int64_t t = (int64_t)blockIdx.x * kRWarps + warp; t < tiles;
-       t += (int64_t)gridDim.x * kRWarps) {
-    int s;
-    int64_t lo, hi;
-    const int64_t q0 = rk_tile(b, s_base, t, &s, &lo, &hi);
-    const float c = a.coef[s];
-    uint32_t* kwt = a.kw + t * (32 * kRWords);
-    const uint32_t q = (uint32_t)q0, l = (uint32_t)lo, h = (uint32_t)hi;
-    const uint32_t cnt = (l == 4 * q && h == 4 * q + kRSelTile)
-                             ? rk_slice<kVec, true>(a.e, q, l, h, c, a.keys, a.st0, a.st1, kwt)
-                             : rk_slice<kVec, false>(a.e, q, l, h, c, a.keys, a.st0, a.st1, kwt);
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < tiles;
+       t += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int s = find_tile_seg(s_base, b.nseg, t);
+    const RSeg& d = b.seg[s];
+    uint32_t cnt = 0;
+    if (d.k > 0) {  // warp-uniform
+      const float c = a.coef[s];
+      const bool cand = a.mode[s] != 0;
+      uint32_t lo, hi;
+      const uint32_t a0 = tile_bounds(d, s_base[s], t, &lo, &hi);
+      const uint32_t q0 = a0 >> 2;
+      const bool whole = lo == a0 && hi == a0 + kRTile;
+      uint32_t* kwt = a.kw + t * kRTileWords;
+#pragma unroll 1
+      for (int m = 0; m < kRTileWords / 32; ++m) {
+        const uint32_t x = lane + 32u * m;
+        uint32_t word = cand ? kwt[x] : all_word(q0, x, lo, hi, whole);
+        uint32_t out = 0;
+        while (word) {
+          const int u = (__ffs(word) - 1) >> 2;
+          const uint32_t nib = (word >> (4 * u)) & 0xFu;
+          word &= ~(0xFu << (4 * u));
+          const uint32_t q = q0 + x + 256u * u;
+          float v[4];
+          if (kVec && nib == 0xFu) {
+            const float4 f = reinterpret_cast<const float4*>(a.e)[q];
+            v[0] = f.x;
+            v[1] = f.y;
+            v[2] = f.z;
+            v[3] = f.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = ((nib >> j) & 1u) ? a.e[4 * q + j] : 0.0f;
+          }
+          uint32_t w[4];
+          philox_quad(q, a.st0, a.st1, a.keys, w);
+          out |= quad_keep(v, w, c, nib) << (4 * u);
+        }
+        kwt[x] = out;
+        cnt += __popc(out);
+      }
+    }
     const uint32_t run = __reduce_add_sync(kFull, cnt);
     if (lane == 0) {
       a.cnt[t] = run;
@@ -544,15 +612,17 @@ rk_offsets(int64_t tiles, RSelectArgs a) {
   }
 }
 
-// Pass 2c: the ordered packet.  One warp per tile with kept elements: ranks
-// from a warp scan of the lanes' counts round by round, values re-read from
-// e and e set to +0 at every element that fits the packet.  The first
-// threads of CTA 0 write the per-segment counts.
+// Pass 2c: the ordered packet.  One warp per tile with kept elements; index
+// order is quad group u, then word, then lane, so a round (u, m) takes
+// nibble u of the lanes' words l + 32 m.  Ranks come from a warp scan of the
+// lanes' counts; values are re-read from e and e is set to +0 at every
+// element that fits the packet.  The first threads of CTA 0 write the
+// per-segment counts.
 __global__ void __launch_bounds__(kRT)
 rk_pack(RBatch b, RSelectArgs a) {
   __shared__ int64_t s_base[kRBatch + 1];
-  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles_b[i];
+  const unsigned lane = lane_id();
+  for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles[i];
   __syncthreads();
   const int64_t tiles = s_base[b.nseg];
   if (blockIdx.x == 0 && threadIdx.x < b.nseg) {
@@ -560,41 +630,41 @@ rk_pack(RBatch b, RSelectArgs a) {
     const int64_t hi = min(a.off[s_base[threadIdx.x + 1]], a.capacity);
     a.counts[b.seg[threadIdx.x].id] = (unsigned long long)(hi - lo);
   }
-  for (int64_t t = (int64_t)blockIdx.x * kRWarps + warp; t < tiles;
-       t += (int64_t)gridDim.x * kRWarps) {
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < tiles;
+       t += ((int64_t)gridDim.x * blockDim.x) >> 5) {
     if (a.cnt[t] == 0) continue;  // warp-uniform
     int64_t pos = a.off[t];
     if (pos >= a.capacity) continue;
-    int s;
-    int64_t lo, hi;
-    const int64_t q0 = rk_tile(b, s_base, t, &s, &lo, &hi);
-    const uint32_t* kwt = a.kw + t * (32 * kRWords);
-    uint32_t kbs[kRWords];
+    const int s = find_tile_seg(s_base, b.nseg, t);
+    uint32_t lo, hi;
+    const uint32_t q0 = tile_bounds(b.seg[s], s_base[s], t, &lo, &hi) >> 2;
+    const uint32_t* kwt = a.kw + t * kRTileWords;
+    uint32_t wd[kRTileWords / 32];
+    uint32_t any = 0;
 #pragma unroll
-    for (int j = 0; j < kRWords; ++j) kbs[j] = kwt[32 * j + lane];
+    for (int m = 0; m < kRTileWords / 32; ++m) {
+      wd[m] = kwt[lane + 32 * m];
+      any |= wd[m];
+    }
+    any = __reduce_or_sync(kFull, any);
+#pragma unroll 1
+    for (int u = 0; u < 8; ++u) {
+      if (((any >> (4 * u)) & 0xFu) == 0) continue;  // warp-uniform
 #pragma unroll
-    for (int j = 0; j < kRWords; ++j) {
-      const uint32_t kb = kbs[j];
-      // rounds with a kept element anywhere in the warp, lowest first
-      const uint32_t any = __reduce_or_sync(kFull, kb);
-      uint32_t rounds = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) rounds |= ((any >> (4 * r)) & 0xFu) ? 1u << r : 0u;
-      while (rounds) {
-        const int r = __ffs(rounds) - 1;
-        rounds &= rounds - 1;
-        const uint32_t nib = (kb >> (4 * r)) & 0xFu;
+      for (int m = 0; m < kRTileWords / 32; ++m) {
+        const uint32_t nib = (wd[m] >> (4 * u)) & 0xFu;
+        if (!__any_sync(kFull, nib != 0)) continue;
         const uint32_t n4 = __popc(nib);
         const uint32_t incl = warp_incl_scan(n4);
         int64_t p = pos + (incl - n4);
-        const int64_t i = 4 * (q0 + 32 * (8 * j + r) + lane);
+        const uint32_t i = 4 * (q0 + lane + 32u * m + 256u * u);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if ((nib >> u) & 1u) {
+        for (int j = 0; j < 4; ++j) {
+          if ((nib >> j) & 1u) {
             if (p < a.capacity) {
-              a.out_values[p] = a.e[i + u];
-              a.out_indices[p] = (int32_t)(i + u);
-              a.e[i + u] = 0.0f;
+              a.out_values[p] = a.e[i + j];
+              a.out_indices[p] = (int32_t)(i + j);
+              a.e[i + j] = 0.0f;
             }
             ++p;
           }
@@ -607,9 +677,9 @@ rk_pack(RBatch b, RSelectArgs a) {
 
 struct RPlan {
   std::vector<RBatch> batches;
-  int64_t max_tiles_b = 0;
-  size_t off_acc = 0, off_coef = 0, off_ctl = 0, off_kw = 0, off_cnt = 0, off_csum = 0,
-         off_off = 0, bytes = 0;
+  int64_t max_tiles = 0;
+  size_t off_acc = 0, off_coef = 0, off_mode = 0, off_ssum = 0, off_ctl = 0, off_kw = 0,
+         off_cnt = 0, off_csum = 0, off_off = 0, bytes = 0;
 };
 
 ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* ks, RPlan* p) {
@@ -620,7 +690,7 @@ ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* k
   RBatch cur{};
   auto flush = [&]() {
     if (cur.nseg == 0) return;
-    p->max_tiles_b = std::max(p->max_tiles_b, cur.tiles_b[cur.nseg]);
+    p->max_tiles = std::max(p->max_tiles, cur.tiles[cur.nseg]);
     p->batches.push_back(cur);
     cur = RBatch{};
   };
@@ -631,12 +701,14 @@ ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* k
     if (k < 0 || k > len) return EF_ERR_K;
     if (len == 0) continue;
     const int t = cur.nseg;
-    // aligned blocks the segment meets, in each pass
-    const int64_t blocks_a = (b - 1) / kRTile - a / kRTile + 1;
-    const int64_t blocks_b = (b - 1) / kRSelTile - a / kRSelTile + 1;
-    cur.seg[t] = RSeg{a, len, k, cur.tiles_a[t], cur.tiles_b[t], i};
-    cur.tiles_a[t + 1] = cur.tiles_a[t] + blocks_a;
-    cur.tiles_b[t + 1] = cur.tiles_b[t] + (k > 0 ? blocks_b : 0);
+    const int64_t blocks = (b - 1) / kRTile - a / kRTile + 1;  // aligned blocks it meets
+    const int32_t nsamp =
+        (k > 0 && len >= kSampleMinLen)
+            ? (int32_t)std::min<int64_t>(kSampleBlocksMax, len / (16 * kSampleBlock))
+            : 0;
+    cur.seg[t] = RSeg{a, len, k, cur.samp[t], nsamp, i};
+    cur.tiles[t + 1] = cur.tiles[t] + blocks;
+    cur.samp[t + 1] = cur.samp[t] + nsamp;
     if (++cur.nseg == kRBatch) flush();
   }
   flush();
@@ -645,11 +717,15 @@ ef_status rk_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* k
   off = round_up(off + sizeof(RCtl), 256);
   p->off_acc = off;
   off = round_up(off + (size_t)kRBatch * kChunks * 8, 256);
+  p->off_ssum = off;
+  off = round_up(off + (size_t)kRBatch * 8, 256);
   p->off_coef = off;
   off = round_up(off + (size_t)kRBatch * 4, 256);
-  const size_t tb = (size_t)std::max<int64_t>(p->max_tiles_b, 1);
+  p->off_mode = off;
+  off = round_up(off + (size_t)kRBatch * 4, 256);
+  const size_t tb = (size_t)std::max<int64_t>(p->max_tiles, 1);
   p->off_kw = off;
-  off = round_up(off + tb * 4 * 32 * kRWords, 256);
+  off = round_up(off + tb * 4 * kRTileWords, 256);
   p->off_cnt = off;
   off = round_up(off + tb * 4, 256);
   p->off_csum = off;
@@ -709,8 +785,10 @@ extern "C" ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, 
   if (err != cudaSuccess) return cuda_fail(err);
   RCtl* ctl = reinterpret_cast<RCtl*>(ws + p.off_ctl);
   uint64_t* acc = reinterpret_cast<uint64_t*>(ws + p.off_acc);
-  float* coef = reinterpret_cast<float*>(ws + p.off_coef);
-  RSelectArgs a{coef,
+  double* ssum = reinterpret_cast<double*>(ws + p.off_ssum);
+  RSelectArgs a{reinterpret_cast<float*>(ws + p.off_coef),
+                reinterpret_cast<int32_t*>(ws + p.off_mode),
+                ssum,
                 e,
                 out_values,
                 out_indices,
@@ -734,33 +812,34 @@ extern "C" ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, 
   for (const RBatch& b : p.batches) {
     a.parity = parity;
     parity ^= 1;
-    const int64_t ta = b.tiles_a[b.nseg], tb = b.tiles_b[b.nseg];
-    const int64_t nchunks = std::max<int64_t>(1, (tb + kOffChunk - 1) / kOffChunk);
+    const int64_t tiles = b.tiles[b.nseg], sblocks = b.samp[b.nseg];
+    const int64_t nchunks = std::max<int64_t>(1, (tiles + kOffChunk - 1) / kOffChunk);
     err = cudaMemsetAsync(acc, 0, (size_t)kRBatch * kChunks * 8, s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(ssum, 0, (size_t)kRBatch * 8, s);
     if (err == cudaSuccess) err = cudaMemsetAsync(a.csum, 0, (size_t)nchunks * 4, s);
     if (err != cudaSuccess) return cuda_fail(err);
-    const int ga = (int)std::max<int64_t>(1, std::min<int64_t>(ta, (int64_t)dev.sms * 4));
-    if (vec) rk_sum<true><<<ga, kRT, 0, s>>>(b, g_raw, e, acc);
-    else rk_sum<false><<<ga, kRT, 0, s>>>(b, g_raw, e, acc);
-    if ((st = check_launch()) != EF_OK) return st;
-    rk_finalize<<<1, kRBatch, 0, s>>>(b, acc, coef);
-    if ((st = check_launch()) != EF_OK) return st;
-    const int64_t warps = (tb + kRWarps - 1) / kRWarps;
-    if (tb > 0) {
-      const int gd =
-          (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * kDrawCtas));
-      if (vec_e) rk_draw<true><<<gd, kRT, 0, s>>>(b, a);
-      else rk_draw<false><<<gd, kRT, 0, s>>>(b, a);
+    const int64_t warps = (tiles + kRT / 32 - 1) / (kRT / 32);
+    if (sblocks > 0) {
+      const int gs = (int)std::min<int64_t>((sblocks + kRT / 32 - 1) / (kRT / 32),
+                                            (int64_t)dev.sms * 8);
+      rk_sample<<<gs, kRT, 0, s>>>(b, g_raw, e, ssum);
       if ((st = check_launch()) != EF_OK) return st;
     }
+    const int ga = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)dev.sms * 3));
+    if (vec) rk_sum<true><<<ga, kRT, 0, s>>>(b, g_raw, e, acc, a);
+    else rk_sum<false><<<ga, kRT, 0, s>>>(b, g_raw, e, acc, a);
+    if ((st = check_launch()) != EF_OK) return st;
+    rk_finalize<<<1, kRBatch, 0, s>>>(b, acc, a);
+    if ((st = check_launch()) != EF_OK) return st;
+    const int gw = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 8));
+    if (vec_e) rk_refine<true><<<gw, kRT, 0, s>>>(b, a);
+    else rk_refine<false><<<gw, kRT, 0, s>>>(b, a);
+    if ((st = check_launch()) != EF_OK) return st;
     // always: it carries the running offset to the next launch
-    rk_offsets<<<(unsigned)nchunks, kRT, 0, s>>>(tb, a);
+    rk_offsets<<<(unsigned)nchunks, kRT, 0, s>>>(tiles, a);
     if ((st = check_launch()) != EF_OK) return st;
-    if (tb > 0) {
-      const int gp = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 8));
-      rk_pack<<<gp, kRT, 0, s>>>(b, a);
-      if ((st = check_launch()) != EF_OK) return st;
-    }
+    rk_pack<<<gw, kRT, 0, s>>>(b, a);
+    if ((st = check_launch()) != EF_OK) return st;
   }
   return EF_OK;
 }
