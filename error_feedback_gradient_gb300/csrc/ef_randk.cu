@@ -498,20 +498,66 @@ __device__ __forceinline__ uint32_t all_word(uint32_t q0, uint32_t x, uint32_t l
   return w;
 }
 
-// Pass 2a: exact keep bits and counts, one warp per tile, tiles strided over
-// the grid's warps.  Lane l re-tests the candidates of words l + 32 m at c:
-// per quad with a candidate, one Philox call and the candidates' values
-// from e (a 16-byte load for a whole quad when e is 16-byte aligned).
+// Nonzero nibbles of w, as bit 4u for nibble u.
+__device__ __forceinline__ uint32_t nz_nibbles(uint32_t w) {
+  w |= w >> 1;
+  w |= w >> 2;
+  return w & 0x11111111u;
+}
+
+constexpr int kRefineList = 256;  // candidate quads a warp re-tests lane-parallel per tile
+
+// The candidates of quad q given as nibble `nib` at coefficient c: their
+// values from e (a 16-byte load for a whole quad when e is 16-byte
+// aligned), one Philox call, the keep test.
 template <bool kVec>
-__global__ void __launch_bounds__(kRT)
+__device__ __forceinline__ uint32_t refine_quad(const RSelectArgs& a, uint32_t q, uint32_t nib,
+                                                float c) {
+  float v[4];
+  if (kVec && nib == 0xFu) {
+    const float4 f = reinterpret_cast<const float4*>(a.e)[q];
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = ((nib >> j) & 1u) ? a.e[4 * q + j] : 0.0f;
+  }
+  uint32_t w[4];
+  philox_quad(q, a.st0, a.st1, a.keys, w);
+  return quad_keep(v, w, c, nib);
+}
+
+// Pass 2a: exact keep bits and counts, one warp per tile, tiles strided over
+// the grid's warps.  Lane l holds the tile's words l + 32 m.  With few
+// candidate quads the warp lists them in shared memory and re-tests them one
+// per lane (one Philox round for up to 32 quads); otherwise, and where
+// every element is tested, each lane walks its own words.
+template <bool kVec>
+__global__ void __launch_bounds__(kRT, 4)
 rk_refine(RBatch b, RSelectArgs a) {
+  constexpr int kM = kRTileWords / 32;
   __shared__ int64_t s_base[kRBatch + 1];
+  __shared__ uint32_t s_in[kRT / 32][kRTileWords], s_out[kRT / 32][kRTileWords];
+  __shared__ uint16_t s_list[kRT / 32][kRefineList];
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles[i];
   __syncthreads();
-  const unsigned lane = lane_id();
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   const int64_t tiles = s_base[b.nseg];
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < tiles;
-       t += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+  const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // the words of the warp's next tile are loaded while it works on this one
+  uint32_t nxt[kM];
+#pragma unroll
+  for (int m = 0; m < kM; ++m) nxt[m] = t < tiles ? a.kw[t * kRTileWords + lane + 32 * m] : 0u;
+  for (; t < tiles; t += stride) {
+    uint32_t wd[kM];
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+      wd[m] = nxt[m];
+      nxt[m] = t + stride < tiles ? a.kw[(t + stride) * kRTileWords + lane + 32 * m] : 0u;
+    }
     const int s = find_tile_seg(s_base, b.nseg, t);
     const RSeg& d = b.seg[s];
     uint32_t cnt = 0;
@@ -523,33 +569,58 @@ rk_refine(RBatch b, RSelectArgs a) {
       const uint32_t q0 = a0 >> 2;
       const bool whole = lo == a0 && hi == a0 + kRTile;
       uint32_t* kwt = a.kw + t * kRTileWords;
-#pragma unroll 1
-      for (int m = 0; m < kRTileWords / 32; ++m) {
-        const uint32_t x = lane + 32u * m;
-        uint32_t word = cand ? kwt[x] : all_word(q0, x, lo, hi, whole);
-        uint32_t out = 0;
-        while (word) {
-          const int u = (__ffs(word) - 1) >> 2;
-          const uint32_t nib = (word >> (4 * u)) & 0xFu;
-          word &= ~(0xFu << (4 * u));
-          const uint32_t q = q0 + x + 256u * u;
-          float v[4];
-          if (kVec && nib == 0xFu) {
-            const float4 f = reinterpret_cast<const float4*>(a.e)[q];
-            v[0] = f.x;
-            v[1] = f.y;
-            v[2] = f.z;
-            v[3] = f.w;
-          } else {
+      uint32_t nq = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = ((nib >> j) & 1u) ? a.e[4 * q + j] : 0.0f;
+      for (int m = 0; m < kM; ++m) {
+        if (!cand) wd[m] = all_word(q0, lane + 32u * m, lo, hi, whole);
+        nq += __popc(nz_nibbles(wd[m]));
+      }
+      const uint32_t incl = warp_incl_scan(nq);
+      const uint32_t total = __shfl_sync(kFull, incl, 31);
+      if (total <= (uint32_t)kRefineList) {
+        uint32_t p = incl - nq;
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+          const uint32_t x = lane + 32u * m;
+          s_in[warp][x] = wd[m];
+          s_out[warp][x] = 0;
+          uint32_t z = nz_nibbles(wd[m]);
+          while (z) {
+            const uint32_t bpos = __ffs(z) - 1;
+            z &= z - 1;
+            s_list[warp][p++] = (uint16_t)((x << 3) | (bpos >> 2));
           }
-          uint32_t w[4];
-          philox_quad(q, a.st0, a.st1, a.keys, w);
-          out |= quad_keep(v, w, c, nib) << (4 * u);
         }
-        kwt[x] = out;
-        cnt += __popc(out);
+        __syncwarp();
+        for (uint32_t i = lane; i < total; i += 32) {
+          const uint32_t ent = s_list[warp][i];
+          const uint32_t x = ent >> 3, u = ent & 7u;
+          const uint32_t nib = (s_in[warp][x] >> (4 * u)) & 0xFu;
+          const uint32_t bits = refine_quad<kVec>(a, q0 + x + 256u * u, nib, c);
+          if (bits) atomicOr(&s_out[warp][x], bits << (4 * u));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+          const uint32_t out = s_out[warp][lane + 32 * m];
+          kwt[lane + 32 * m] = out;
+          cnt += __popc(out);
+        }
+        __syncwarp();
+      } else {
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+          const uint32_t x = lane + 32u * m;
+          uint32_t word = wd[m], out = 0;
+          while (word) {
+            const int u = (__ffs(word) - 1) >> 2;
+            const uint32_t nib = (word >> (4 * u)) & 0xFu;
+            word &= ~(0xFu << (4 * u));
+            out |= refine_quad<kVec>(a, q0 + x + 256u * u, nib, c) << (4 * u);
+          }
+          kwt[x] = out;
+          cnt += __popc(out);
+        }
       }
     }
     const uint32_t run = __reduce_add_sync(kFull, cnt);
@@ -612,16 +683,20 @@ rk_offsets(int64_t tiles, RSelectArgs a) {
   }
 }
 
-// Pass 2c: the ordered packet.  One warp per tile with kept elements; index
-// order is quad group u, then word, then lane, so a round (u, m) takes
-// nibble u of the lanes' words l + 32 m.  Ranks come from a warp scan of the
-// lanes' counts; values are re-read from e and e is set to +0 at every
-// element that fits the packet.  The first threads of CTA 0 write the
-// per-segment counts.
+// Pass 2c: the ordered packet.  One warp per tile with kept elements.  With
+// at most 32 of them the warp lists their offsets in the tile in shared
+// memory, one per lane, and ranks each by counting the smaller ones.
+// Otherwise it walks the tile in index order, quad group u, then word, then
+// lane, so a round (u, m) takes nibble u of the lanes' words l + 32 m, with
+// ranks from a warp scan of the lanes' counts.  Values are re-read from e
+// and e is set to +0 at every element that fits the packet.  The first
+// threads of CTA 0 write the per-segment counts.
 __global__ void __launch_bounds__(kRT)
 rk_pack(RBatch b, RSelectArgs a) {
+  constexpr int kM = kRTileWords / 32;
   __shared__ int64_t s_base[kRBatch + 1];
-  const unsigned lane = lane_id();
+  __shared__ uint16_t s_keys[kRT / 32][32];
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.tiles[i];
   __syncthreads();
   const int64_t tiles = s_base[b.nseg];
@@ -632,26 +707,61 @@ rk_pack(RBatch b, RSelectArgs a) {
   }
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < tiles;
        t += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    if (a.cnt[t] == 0) continue;  // warp-uniform
+    const uint32_t total = a.cnt[t];
+    if (total == 0) continue;  // warp-uniform
     int64_t pos = a.off[t];
     if (pos >= a.capacity) continue;
     const int s = find_tile_seg(s_base, b.nseg, t);
     uint32_t lo, hi;
-    const uint32_t q0 = tile_bounds(b.seg[s], s_base[s], t, &lo, &hi) >> 2;
+    const uint32_t a0 = tile_bounds(b.seg[s], s_base[s], t, &lo, &hi);
+    const uint32_t q0 = a0 >> 2;
     const uint32_t* kwt = a.kw + t * kRTileWords;
-    uint32_t wd[kRTileWords / 32];
+    uint32_t wd[kM];
+    uint32_t mine = 0;
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+      wd[m] = kwt[lane + 32 * m];
+      mine += __popc(wd[m]);
+    }
+    if (total <= 32) {
+      const uint32_t incl = warp_incl_scan(mine);
+      uint32_t p = incl - mine;
+#pragma unroll
+      for (int m = 0; m < kM; ++m) {
+        uint32_t w = wd[m];
+        while (w) {
+          const uint32_t bpos = __ffs(w) - 1;
+          w &= w - 1;
+          // offset in the tile of element bpos % 4 of quad (lane + 32 m) + 256 (bpos / 4)
+          s_keys[warp][p++] = (uint16_t)(4 * (lane + 32 * m + 256 * (bpos >> 2)) + (bpos & 3u));
+        }
+      }
+      __syncwarp();
+      const uint32_t key = lane < total ? s_keys[warp][lane] : 0xFFFFu;
+      uint32_t rank = 0;
+#pragma unroll
+      for (int l2 = 0; l2 < 32; ++l2) rank += __shfl_sync(kFull, key, l2) < key ? 1u : 0u;
+      __syncwarp();
+      if (lane < total) {
+        const int64_t p2 = pos + rank;
+        const uint32_t i = a0 + key;
+        if (p2 < a.capacity) {
+          a.out_values[p2] = a.e[i];
+          a.out_indices[p2] = (int32_t)i;
+          a.e[i] = 0.0f;
+        }
+      }
+      continue;
+    }
     uint32_t any = 0;
 #pragma unroll
-    for (int m = 0; m < kRTileWords / 32; ++m) {
-      wd[m] = kwt[lane + 32 * m];
-      any |= wd[m];
-    }
+    for (int m = 0; m < kM; ++m) any |= wd[m];
     any = __reduce_or_sync(kFull, any);
 #pragma unroll 1
     for (int u = 0; u < 8; ++u) {
       if (((any >> (4 * u)) & 0xFu) == 0) continue;  // warp-uniform
 #pragma unroll
-      for (int m = 0; m < kRTileWords / 32; ++m) {
+      for (int m = 0; m < kM; ++m) {
         const uint32_t nib = (wd[m] >> (4 * u)) & 0xFu;
         if (!__any_sync(kFull, nib != 0)) continue;
         const uint32_t n4 = __popc(nib);
@@ -831,9 +941,11 @@ extern "C" ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, 
     if ((st = check_launch()) != EF_OK) return st;
     rk_finalize<<<1, kRBatch, 0, s>>>(b, acc, a);
     if ((st = check_launch()) != EF_OK) return st;
+    // rk_refine: 4 CTAs per SM (58 registers), one wave; rk_pack: 8
+    const int gr = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 4));
     const int gw = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 8));
-    if (vec_e) rk_refine<true><<<gw, kRT, 0, s>>>(b, a);
-    else rk_refine<false><<<gw, kRT, 0, s>>>(b, a);
+    if (vec_e) rk_refine<true><<<gr, kRT, 0, s>>>(b, a);
+    else rk_refine<false><<<gr, kRT, 0, s>>>(b, a);
     if ((st = check_launch()) != EF_OK) return st;
     // always: it carries the running offset to the next launch
     rk_offsets<<<(unsigned)nchunks, kRT, 0, s>>>(tiles, a);

@@ -153,3 +153,24 @@ def test_randk_launch_without_draws_carries_the_packet_offset():
     offs = wl.segments_from_sizes(sizes)
     n = offs[-1]
     check_randk(_t(n, 13), _t(n, 14, 1e-4), offs, ks, seed=8, step=5)
+
+
+def test_randk_sampled_bound_too_low_and_empty_sample():
+    """Long tensors are sampled in blocks of 64 elements at the start of
+    each of up to 2048 equal strides.  One large value inside the first
+    sampled block makes the sample overstate the sum of |g| several times,
+    so the bound taken from it falls below the true coefficient; a tensor
+    whose nonzero elements all lie outside the sampled blocks gives an
+    empty sample.  Both must still match the oracle."""
+    n = 1 << 20
+    g = _t(n, 31)
+    g[5] = 1000.0
+    check_randk(g, torch.zeros(n, device=DEV), [0, n], [1000], seed=21, step=2)
+    stride = n // 1024                       # 1024 sampled blocks of 64
+    pos = torch.arange(n, device=DEV)
+    g2 = torch.where(pos % stride >= 64, _t(n, 32), torch.zeros(n, device=DEV))
+    check_randk(g2, torch.zeros(n, device=DEV), [0, n], [1000], seed=22, step=3)
+    # both in one call, beside a segment whose sample is representative
+    g3 = torch.cat([g, g2, _t(n, 33)])
+    check_randk(g3, torch.zeros(3 * n, device=DEV), [0, n, 2 * n, 3 * n], [1000, 500, 2000],
+                seed=23, step=4)
