@@ -836,7 +836,7 @@ def run_next(args, dev):
         efg.randk_compress(g, e, offs, ks, 2024, stepno[0], v, ix, cnt, wsr)
     ms_rk = timed(rk, 5)
     kept = int(cnt[-1].item())
-    rk_bytes = 16 * n + 8 * kept
+    rk_bytes = 12 * n + 8 * kept
     gs2 = (rng.standard_t(3, sample) * 1e-3).astype(np.float32)
     t0 = time.perf_counter()
     oracle.randk_ef_step(gs2, np.zeros(sample, np.float32), [0, sample], [ksm], 1, 1, 2 * ksm)
@@ -845,9 +845,9 @@ def run_next(args, dev):
         "workload": f"one tensor of {n} elements, expected k = {k}",
         "ms_per_call": ms_rk, "kept_last_call": kept,
         "algorithmic_bytes": rk_bytes,
-        "note": "algorithmic: 12 B/element (compensate + exact sum of |g|), 4 B/element "
-                "(draws) and 8 B per kept element; the keep bits add 1/4 B/element "
-                "(written, then re-read by the packing pass)",
+        "note": "algorithmic: 12 B/element (read g_raw and e, write e) + 8 B per kept "
+                "element; the draws ride on the one pass over g at a sampled upper bound of "
+                "the coefficient, and the candidate and keep bits add 1/4 B/element",
         "gbs": rk_bytes / (ms_rk * 1e-3) / 1e9,
         "g_elems_per_s": n / ms_rk / 1e6,
         "cpu_baseline": {"g_elems_per_s": sample / dt / 1e9, "cores": 1, "kind": "oracle",

@@ -302,7 +302,7 @@ EF_API ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in_byt
  * d_counts     [nseg + 1] int64 (device, 8-byte aligned): entries sent per
  *              segment, then their total (the packet length).
  * workspace    >= ef_randk_workspace_size() bytes, 256-byte aligned: about
- *              n/8 bytes of keep bits plus 12 bytes per 4096 elements.
+ *              n/8 bytes of keep bits plus 16 bytes per 8192 elements.
  * No buffer may overlap another.
  * ---------------------------------------------------------------------- */
 EF_API ef_status ef_randk_workspace_size(int64_t n, int32_t nseg, const int64_t* h_seg_offsets,
