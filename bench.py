@@ -861,7 +861,8 @@ def run_case(args):
     """One entry point alone, three calls, for profiling its kernels in
     isolation (--case): 'topk' (one tensor of n elements, top-0.1 %),
     'aggregate' (4 workers' int32 packets of 0.1 % over n, with G and SGD),
-    'randk' (random sparsification of one tensor, expected 0.1 %), 'sign'
+    'randk' (random sparsification of one tensor, expected 0.1 %), 'resnet50'
+    (the layerwise top-k step over the 161 ResNet-50 gradient tensors), 'sign'
     (1-bit compression of 4 workers' gradients of n elements, then their
     sign aggregate with G and SGD), 'q8' (top-0.1 % with 8-bit values, then
     the receiver's dequantisation) or 'codec' (a top-0.1 % packet of n
@@ -895,6 +896,17 @@ def run_case(args):
                          device=dev)
         for _ in range(3):
             efg.sparse_aggregate_apply(vals, ix, None, [k] * W, n, 0.1, G, w, ws)
+    elif args.case == "resnet50":
+        w = wl.workload("resnet50")
+        n, k = w.n, w.total_k
+        g = w.gradient(0, 1, dev)
+        e = torch.zeros_like(g)
+        v = torch.empty(k, device=dev)
+        ix = torch.empty(k, dtype=torch.int32, device=dev)
+        ws = torch.empty(efg.topk_workspace_size(n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            efg.topk_compress(g, e, w.seg_offsets, w.seg_k, v, ix, None, ws)
     elif args.case == "randk":
         g = wl.student_t3(n, 1e-3, 1, dev)
         e = torch.zeros_like(g)
@@ -973,7 +985,8 @@ def main(argv=None):
     p.add_argument("--traffic-per-launch", type=float, default=None,
                    help="DRAM bytes of one topk_fused launch at this size, from ncu")
     p.add_argument("--no-extras", dest="extras", action="store_false")
-    p.add_argument("--case", choices=["topk", "aggregate", "randk", "sign", "q8", "codec"],
+    p.add_argument("--case", choices=["topk", "aggregate", "randk", "resnet50", "sign", "q8",
+                                       "codec"],
                    default=None,
                    help="run one entry point alone (three calls at --n) for profiling")
     args = p.parse_args(argv)

@@ -100,6 +100,12 @@ struct LargeBatch {
   LargeSeg seg[kMaxLarge];
 };
 
+// CTAs of the two sampling passes: segment s owns CTAs [base[s], base[s+1]),
+// enough for one round of sample loads per warp (kMaxLarge segments).
+struct SampleGrid {
+  int32_t base[kMaxLarge + 1];
+};
+
 struct SegState {
   LargeSeg d;
   uint32_t t_lo;
@@ -185,10 +191,24 @@ topk_small(SmallBatch b, IO io, int keys_words) {
   const int len = sg.len;
   const float* gr = io.g_raw + sg.off;
   float* e = io.e + sg.off;
-  for (int i = threadIdx.x; i < len; i += blockDim.x) {
-    const float x = __fadd_rn(gr[i], e[i]);
-    e[i] = x;
-    gbits[i] = __float_as_uint(x);
+  // eight elements of each array in flight per thread
+  for (int i0 = threadIdx.x; i0 < len; i0 += 8 * kSmallThreads) {
+    float gv[8], ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSmallThreads;
+      gv[u] = i < len ? gr[i] : 0.0f;
+      ev[u] = i < len ? e[i] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSmallThreads;
+      if (i < len) {
+        const float x = __fadd_rn(gv[u], ev[u]);
+        e[i] = x;
+        gbits[i] = __float_as_uint(x);
+      }
+    }
   }
   __syncthreads();
   if (sg.k == 0) return;
@@ -288,16 +308,31 @@ __device__ __forceinline__ bool samples_needed(const LargeSeg& d, int64_t nblk) 
   return d.rank > 0 && d.rank <= nblk * kSampleBlock;
 }
 
+// Segment and CTA rank within it of sampling CTA `blk`.
+__device__ __forceinline__ int sample_seg(const SampleGrid& g, int nseg, int blk, int* q,
+                                          int* ctas) {
+  int lo = 0, hi = nseg - 1;  // last segment whose first CTA is <= blk
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (g.base[mid] <= blk) lo = mid;
+    else hi = mid - 1;
+  }
+  *q = blk - g.base[lo];
+  *ctas = g.base[lo + 1] - g.base[lo];
+  return lo;
+}
+
 // Sampling pass 1: histogram of the top 11 key bits over all sample blocks
-// of each streaming segment (`ctas` CTAs per segment, merged in global
+// of each streaming segment (the segment's CTAs of `grid`, merged in global
 // memory); the CTA that merges last finds the bin b0 holding the rank-th
 // largest sampled key and the rank r1 left inside it.
 __global__ void __launch_bounds__(kSampleThreads)
-topk_sample(LargeBatch b, IO io, uint32_t* hist0, SampleState* ss, int ctas) {
+topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss) {
   __shared__ uint32_t sh[2048];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
-  const int s = blockIdx.x / ctas, q = blockIdx.x % ctas;
+  int q, ctas;
+  const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
   const LargeSeg& d = b.seg[s];
   const int64_t nblk = sample_blocks(d.len);
   if (!samples_needed(d, nblk)) return;  // uniform across the CTA
@@ -363,11 +398,13 @@ __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& 
 // bin holding the rank-th largest sampled key (so at least `rank` sampled
 // keys are >= T_lo) and the segment's state for the later passes.
 __global__ void __launch_bounds__(kSampleThreads)
-topk_prepare(LargeBatch b, IO io, uint32_t* hist1, SampleState* ss, SegState* st, int ctas) {
+topk_prepare(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist1, SampleState* ss,
+             SegState* st) {
   __shared__ uint32_t sh[1024];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
-  const int s = blockIdx.x / ctas, q = blockIdx.x % ctas;
+  int q, ctas;
+  const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
   const LargeSeg d = b.seg[s];
   const int64_t nblk = sample_blocks(d.len);
   if (!samples_needed(d, nblk)) {
@@ -679,14 +716,20 @@ constexpr int kRestoreThreads = 256;
 // the fused pass staged and wrote as +0, from the candidate list (its first
 // min(candidates, capacity) slots; slots of never-staged candidates hold
 // kNoEntry).  Segments selecting on their list are left alone.
+// The segments' states are read in one parallel round into shared memory,
+// so a batch without such a segment costs one load per thread.
 __global__ void __launch_bounds__(kRestoreThreads)
 topk_restore(IO io, const SegState* st, int nseg, const uint2* cand) {
+  __shared__ int64_t s_m[kMaxLarge];  // entries to restore per segment (0: none)
+  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+    const int64_t c = st[s].cand_count;  // <= 0: no candidates, or a reported error
+    s_m[s] = (st[s].mode == 1 && c > 0) ? min(c, st[s].d.cap) : 0;
+  }
+  __syncthreads();
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   for (int s = 0; s < nseg; ++s) {
-    if (st[s].mode != 1) continue;  // uniform across the grid
-    const int64_t c = st[s].cand_count;
-    if (c <= 0) continue;  // no candidates, or a pass that already reported an error
-    const int64_t m = min(c, st[s].d.cap);
+    const int64_t m = s_m[s];
+    if (m == 0) continue;  // uniform across the grid
     const int64_t len = st[s].d.len;
     const uint2* l = cand + st[s].d.cand_base;
     float* es = io.e + st[s].d.off;
@@ -1186,12 +1229,23 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(ws + p.off_hist0);
     uint32_t* hist1 = reinterpret_cast<uint32_t*>(ws + p.off_hist1);
     SampleState* sstate = reinterpret_cast<SampleState*>(ws + p.off_sstate);
-    // sampling CTAs per segment: about four per SM in all, 8 to 128 each
-    const int sctas = (int)std::max<int64_t>(
-        8, std::min<int64_t>(kSampleCtasMax, (int64_t)dev.sms * 4 / nsg));
-    topk_sample<<<nsg * sctas, kSampleThreads, 0, s>>>(lb, io, hist0, sstate, sctas);
+    // sampling CTAs per segment: one round of sample loads per warp (32
+    // blocks per CTA), at most kSampleCtasMax; one for a segment that
+    // does not sample (its prepare CTA sets the segment's state)
+    SampleGrid sg;
+    sg.base[0] = 0;
+    for (int i = 0; i < nsg; ++i) {
+      const LargeSeg& d = lb.seg[i];
+      const int64_t nblk = sample_blocks(d.len);
+      const int64_t per = (int64_t)(kSampleThreads / 32) * kSampleUnroll;
+      const int64_t c = (d.rank > 0 && d.rank <= nblk * kSampleBlock)
+                            ? std::min<int64_t>(kSampleCtasMax, (nblk + per - 1) / per)
+                            : 1;
+      sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
+    }
+    topk_sample<<<sg.base[nsg], kSampleThreads, 0, s>>>(lb, sg, nsg, io, hist0, sstate);
     if ((st = check_launch()) != EF_OK) return st;
-    topk_prepare<<<nsg * sctas, kSampleThreads, 0, s>>>(lb, io, hist1, sstate, sst, sctas);
+    topk_prepare<<<sg.base[nsg], kSampleThreads, 0, s>>>(lb, sg, nsg, io, hist1, sstate, sst);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
