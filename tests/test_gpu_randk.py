@@ -174,3 +174,23 @@ def test_randk_sampled_bound_too_low_and_empty_sample():
     g3 = torch.cat([g, g2, _t(n, 33)])
     check_randk(g3, torch.zeros(3 * n, device=DEV), [0, n, 2 * n, 3 * n], [1000, 500, 2000],
                 seed=23, step=4)
+
+
+def test_randk_sampled_segments_across_launch_groups():
+    """More than 128 segments, with segments long enough to be sampled in
+    both launch groups, dense and sparse keep fractions among them, and a
+    capacity that cuts the packet inside the second group."""
+    rng = np.random.default_rng(17)
+    sizes = [int(x) for x in rng.integers(1, 2000, 140)]
+    for i, s in ((3, 70_000), (60, 300_000), (131, 150_001), (139, 65_536)):
+        sizes[i] = s
+    ks = [max(0, s // 50) for s in sizes]
+    ks[60] = 250_000                         # dense: c |g| > 1 for many elements
+    ks[131] = 150
+    offs = wl.segments_from_sizes(sizes)
+    n = offs[-1]
+    g, e = _t(n, 40), _t(n, 41, 1e-4)
+    want = check_randk(g, e, offs, ks, seed=5, step=11)
+    # the same inputs with a capacity below the kept count
+    g2, e2 = _t(n, 40), _t(n, 41, 1e-4)
+    check_randk(g2, e2, offs, ks, seed=5, step=11, capacity=int(want["kept"]) - 1000)
