@@ -59,6 +59,7 @@ __device__ __forceinline__ int64_t clamp_tile(int64_t idx, const AggArgs& a) {
 // Run boundaries for int32 packets; validates order and range.
 __global__ void __launch_bounds__(kAThreads)
 agg_starts_int32(AggArgs a, uint32_t* start, int32_t* status) {
+  pdl_wait();
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = a.kbase[a.W];
@@ -95,6 +96,7 @@ constexpr int kScanTiles = 2048;  // tiles per chunk of the bitmap run-boundary 
 __global__ void __launch_bounds__(kAThreads)
 agg_bitmap_starts(AggArgs a, uint32_t* start, uint64_t* cstate, uint32_t* ticket,
                   int32_t* status) {
+  pdl_wait();
   __shared__ uint32_t cnt[kScanTiles];
   __shared__ uint32_t scratch[64];
   __shared__ uint32_t s_t;
@@ -327,6 +329,7 @@ __device__ __forceinline__ void tile_general(const AggArgs& a, const uint32_t* s
 template <bool kBitmap>
 __global__ void __launch_bounds__(kAThreads, 6)
 agg_apply(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
+  pdl_wait();
   __shared__ __align__(16) float acc_all[kAWarps][kWT];
   __shared__ uint32_t touched_all[kAWarps][kWT / 32];
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
@@ -521,6 +524,7 @@ __device__ __forceinline__ void pipe_finish(const AggArgs& a, int64_t t, const E
 template <bool kBitmap>
 __global__ void __launch_bounds__(kAThreads, 5)
 agg_apply_pipe(AggArgs a, const uint32_t* start, float* __restrict__ G, float* __restrict__ wts) {
+  pdl_wait();
   __shared__ __align__(16) float acc_all[kAWarps][kWT];
   __shared__ uint32_t touched_all[kAWarps][kWT / 32];
   __shared__ float vbuf_all[kAWarps][32];
@@ -675,7 +679,7 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
     const int64_t work = std::max<int64_t>(a.kbase[W], (int64_t)W * (nt + 1));
     const int grid = (int)std::max<int64_t>(
         1, std::min<int64_t>((work + kAThreads - 1) / kAThreads, (int64_t)dev.sms * 8));
-    agg_starts_int32<<<grid, kAThreads, 0, s>>>(a, start, status);
+    launch_pdl(agg_starts_int32, grid, kAThreads, 0, s, a, start, status);
     if ((st = check_launch()) != EF_OK) return st;
   } else {
     char* ctl = ws + round_up(sizeof(WsHeader) + (size_t)W * (nt + 1) * 4, 256);
@@ -684,7 +688,7 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
     if (err != cudaSuccess) return cuda_fail(err);
     const int grid = (int)std::max<int64_t>(
         1, std::min<int64_t>((int64_t)W * agg_chunks(n), (int64_t)dev.sms * 5));
-    agg_bitmap_starts<<<grid, kAThreads, 0, s>>>(a, start, reinterpret_cast<uint64_t*>(ctl + 256),
+    launch_pdl(agg_bitmap_starts, grid, kAThreads, 0, s, a, start, reinterpret_cast<uint64_t*>(ctl + 256),
                                                  reinterpret_cast<uint32_t*>(ctl), status);
     if ((st = check_launch()) != EF_OK) return st;
   }
@@ -693,13 +697,13 @@ extern "C" ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
       1, std::min<int64_t>((nt + kAWarps - 1) / kAWarps, (int64_t)dev.sms * (pipe ? 5 : 6)));
   prof_begin(EF_KERNEL_SPARSE_APPLY, s);
   if (bitmap && pipe)
-    agg_apply_pipe<true><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+    launch_pdl(agg_apply_pipe<true>, grid, kAThreads, 0, s, a, start, G, w);
   else if (bitmap)
-    agg_apply<true><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+    launch_pdl(agg_apply<true>, grid, kAThreads, 0, s, a, start, G, w);
   else if (pipe)
-    agg_apply_pipe<false><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+    launch_pdl(agg_apply_pipe<false>, grid, kAThreads, 0, s, a, start, G, w);
   else
-    agg_apply<false><<<grid, kAThreads, 0, s>>>(a, start, G, w);
+    launch_pdl(agg_apply<false>, grid, kAThreads, 0, s, a, start, G, w);
   if ((st = check_launch()) != EF_OK) return st;
   prof_end(EF_KERNEL_SPARSE_APPLY, s);
   return EF_OK;

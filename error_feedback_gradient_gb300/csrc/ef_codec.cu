@@ -77,6 +77,8 @@ __device__ __forceinline__ uint64_t cta_excl_u64(uint64_t v, uint64_t* sh, uint6
 // Pass 1: sum of value(j) over each chunk.
 template <class Op>
 __global__ void __launch_bounds__(kCT) chunk_sums(Op op, int64_t nitems, uint64_t* sums) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint64_t sh[33];
   const int64_t j0 = (int64_t)blockIdx.x * kItems + (int64_t)threadIdx.x * kPerThread;
   uint64_t v = 0;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(kCT) chunk_sums(Op op, int64_t nitems, uint64_
 __global__ void __launch_bounds__(kScanThreads)
 scan_sums(uint64_t* sums, int64_t nchunks, uint64_t* total, uint64_t* total_copy,
           uint64_t total_bias) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint64_t sh[33];
   const int64_t per = (nchunks + kScanThreads - 1) / kScanThreads;
   const int64_t c0 = (int64_t)threadIdx.x * per;
@@ -113,6 +117,7 @@ scan_sums(uint64_t* sums, int64_t nchunks, uint64_t* total, uint64_t* total_copy
 // Pass 2: apply(j, offset of j) for every item, offsets from the scanned sums.
 template <class Op>
 __global__ void __launch_bounds__(kCT) chunk_apply(Op op, int64_t nitems, const uint64_t* sums) {
+  pdl_wait();
   __shared__ uint64_t sh[33];
   const int64_t j0 = (int64_t)blockIdx.x * kItems + (int64_t)threadIdx.x * kPerThread;
   uint64_t v[kPerThread];
@@ -137,14 +142,14 @@ ef_status run_scan(Op op, int64_t nitems, uint64_t* sums, uint64_t* total,
   const int64_t nch = chunks_of(nitems);
   ef_status st;
   if (nch == 0) {  // nothing to scan: the totals are zero (plus the bias for the copy)
-    scan_sums<<<1, kScanThreads, 0, s>>>(sums, 0, total, total_copy, bias);
+    launch_pdl(scan_sums, 1, kScanThreads, 0, s, sums, 0, total, total_copy, bias);
     return check_launch();
   }
-  chunk_sums<Op><<<(unsigned)nch, kCT, 0, s>>>(op, nitems, sums);
+  launch_pdl(chunk_sums<Op>, (unsigned)nch, kCT, 0, s, op, nitems, sums);
   if ((st = check_launch()) != EF_OK) return st;
-  scan_sums<<<1, kScanThreads, 0, s>>>(sums, nch, total, total_copy, bias);
+  launch_pdl(scan_sums, 1, kScanThreads, 0, s, sums, nch, total, total_copy, bias);
   if ((st = check_launch()) != EF_OK) return st;
-  chunk_apply<Op><<<(unsigned)nch, kCT, 0, s>>>(op, nitems, sums);
+  launch_pdl(chunk_apply<Op>, (unsigned)nch, kCT, 0, s, op, nitems, sums);
   return check_launch();
 }
 
@@ -165,6 +170,7 @@ __device__ __forceinline__ int64_t checked_index(const int32_t* idx, int64_t j, 
 __global__ void __launch_bounds__(kCT)
 l16_encode(const int32_t* idx, int64_t K, int64_t n, int64_t nblk, uint8_t* out,
            uint64_t* out_bytes, int32_t* status) {
+  pdl_wait();
   uint32_t* starts = reinterpret_cast<uint32_t*>(out);
   uint16_t* low = reinterpret_cast<uint16_t*>(out + 4 * (nblk + 1));
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -184,6 +190,7 @@ l16_encode(const int32_t* idx, int64_t K, int64_t n, int64_t nblk, uint8_t* out,
 
 __global__ void __launch_bounds__(kCT)
 l16_decode(const uint8_t* in, int64_t K, int64_t n, int64_t nblk, int32_t* idx, int32_t* status) {
+  pdl_wait();
   const uint32_t* starts = reinterpret_cast<const uint32_t*>(in);
   const uint16_t* low = reinterpret_cast<const uint16_t*>(in + 4 * (nblk + 1));
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -320,6 +327,8 @@ struct B256Encode {
 __global__ void __launch_bounds__(kCT)
 b256_counts(const uint32_t* first_of, const uint64_t* nnzb, int64_t K, int64_t nfw, uint8_t* out,
             int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const uint64_t nz = *nnzb;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < (int64_t)nz; r += nthr) {
@@ -382,6 +391,7 @@ struct B256Entries {
 };
 
 __global__ void check_total(const uint64_t* total, uint64_t want, int32_t* status) {
+  pdl_wait();
   if (threadIdx.x == 0 && *total != want) set_status(status, EF_ERR_PACKET);
 }
 
@@ -479,7 +489,7 @@ extern "C" ef_status ef_index_encode(int32_t codec, const int32_t* indices, int6
       err = cudaMemsetAsync(out, 0, 4 * (nblk + 1), s);
       if (err != cudaSuccess) return cuda_fail(err);
     }
-    l16_encode<<<grid, kCT, 0, s>>>(indices, K, n, nblk, out, d_out_bytes, status);
+    launch_pdl(l16_encode, grid, kCT, 0, s, indices, K, n, nblk, out, d_out_bytes, status);
     return check_launch();
   }
   if (codec == EF_CODEC_RUNVARINT) {
@@ -496,7 +506,7 @@ extern "C" ef_status ef_index_encode(int32_t codec, const int32_t* indices, int6
   if ((st = run_scan(op, K, sums, total, d_out_bytes, (uint64_t)(4 * nfw + K), s)) != EF_OK)
     return st;
   if (K > 0) {
-    b256_counts<<<grid, kCT, 0, s>>>(first_of, total, K, nfw, out, status);
+    launch_pdl(b256_counts, grid, kCT, 0, s, first_of, total, K, nfw, out, status);
     return check_launch();
   }
   return EF_OK;
@@ -541,7 +551,7 @@ extern "C" ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in
     if (K == 0) return EF_OK;
     const int grid = (int)std::max<int64_t>(
         1, std::min<int64_t>((K + kCT - 1) / kCT, (int64_t)dev.sms * 8));
-    l16_decode<<<grid, kCT, 0, s>>>(in, K, n, nblk, indices, status);
+    launch_pdl(l16_decode, grid, kCT, 0, s, in, K, n, nblk, indices, status);
     return check_launch();
   }
   if (codec == EF_CODEC_RUNVARINT) {
@@ -551,7 +561,7 @@ extern "C" ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in
     if (err != cudaSuccess) return cuda_fail(err);
     RvTerminals t{in, K, end, status};
     if ((st = run_scan(t, (int64_t)in_bytes, sums, total, nullptr, 0, s)) != EF_OK) return st;
-    check_total<<<1, 32, 0, s>>>(total, (uint64_t)K, status);
+    launch_pdl(check_total, 1, 32, 0, s, total, (uint64_t)K, status);
     if ((st = check_launch()) != EF_OK) return st;
     RvIndices op{in, (int64_t)in_bytes, K, n, end, indices, status};
     return run_scan(op, K, sums, total, nullptr, 0, s);
@@ -560,10 +570,10 @@ extern "C" ef_status ef_index_decode(int32_t codec, const uint8_t* in, size_t in
   uint32_t* block_of = reinterpret_cast<uint32_t*>(ws + c.off_aux);
   B256Flags f{reinterpret_cast<const uint32_t*>(in), nb, nnzb, block_of, status};
   if ((st = run_scan(f, nfw, sums, total, nullptr, 0, s)) != EF_OK) return st;
-  check_total<<<1, 32, 0, s>>>(total, (uint64_t)nnzb, status);
+  launch_pdl(check_total, 1, 32, 0, s, total, (uint64_t)nnzb, status);
   if ((st = check_launch()) != EF_OK) return st;
   B256Entries en{in + 4 * nfw, in + 4 * nfw + nnzb, block_of, K, n, indices, status};
   if ((st = run_scan(en, nnzb, sums, total, nullptr, 0, s)) != EF_OK) return st;
-  check_total<<<1, 32, 0, s>>>(total, (uint64_t)K, status);
+  launch_pdl(check_total, 1, 32, 0, s, total, (uint64_t)K, status);
   return check_launch();
 }

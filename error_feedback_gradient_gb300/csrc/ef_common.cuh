@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "efgrad.h"
 
 namespace ef {
@@ -29,6 +31,27 @@ ef_status cuda_fail(cudaError_t err);
 
 // Count one kernel launch and check it; returns EF_OK or EF_ERR_CUDA.
 ef_status check_launch();
+
+// Launches `kernel` on `s` with programmatic stream serialization: it may be
+// scheduled while the kernel before it in the stream is still running, and
+// every kernel of the library calls pdl_wait() before it touches memory, so
+// the order of effects is the stream order.  Errors surface through
+// check_launch().
+template <typename... P, typename... A>
+inline void launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Profiling hook: record the thread's start/stop event for `kernel_id`
 // around a launch, if set.
@@ -56,6 +79,20 @@ struct alignas(256) WsHeader {
 // ---------------------------------------------------------------------------
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// Programmatic dependent launch.  pdl_wait() returns once every kernel this
+// one depends on in the stream has completed and its writes are visible (at
+// once for a kernel launched without the attribute); every kernel calls it
+// before its first memory access.  pdl_trigger() lets the next kernel in the
+// stream be scheduled early, to wait in its own pdl_wait().  Short kernels
+// whose successor is short call it first thing; the long streaming passes,
+// the kernels before them and the last kernel of a call leave it to their
+// exit, so that no waiting CTA holds SM resources a streaming pass on
+// another stream could use.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t abs_key(float x) {
   return __float_as_uint(x) & 0x7FFFFFFFu;

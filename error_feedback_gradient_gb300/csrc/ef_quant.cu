@@ -58,6 +58,8 @@ __device__ __forceinline__ int chunk_segment(const QBatch& b, int64_t c) {
 // atomicMax on the bit pattern.
 __global__ void __launch_bounds__(kQThreads)
 q8_max(QBatch b, const float* __restrict__ values, uint32_t* maxbits) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t red[kQThreads / 32];
   const int64_t c = blockIdx.x;
   const int s = chunk_segment(b, c);
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kQThreads)
 q8_quantize(QBatch b, const float* __restrict__ values, const uint32_t* __restrict__ pos,
             const uint32_t* __restrict__ maxbits, float* __restrict__ e,
             int8_t* __restrict__ out_q, float* __restrict__ out_scale) {
+  pdl_wait();
   const int64_t c = blockIdx.x;
   const int s = chunk_segment(b, c);
   const float sc = q8_segment_scale(maxbits[b.seg_id[s]]);
@@ -119,6 +122,7 @@ q8_quantize(QBatch b, const float* __restrict__ values, const uint32_t* __restri
 __global__ void __launch_bounds__(kQThreads)
 q8_dequantize(QBatch b, const int8_t* __restrict__ q, const float* __restrict__ scales,
               float* __restrict__ out_values) {
+  pdl_wait();
   const int64_t c = blockIdx.x;
   const int s = chunk_segment(b, c);
   const float sc = scales[b.seg_id[s]];
@@ -243,9 +247,9 @@ extern "C" ef_status ef_topk_compress_q8(const float* g_raw, float* e, int64_t n
   }
   for (const QBatch& b : q8_batches(nseg, h_seg_offsets, h_seg_k)) {
     const int64_t chunks = b.chunk_base[b.nseg];
-    q8_max<<<(unsigned)chunks, kQThreads, 0, s>>>(b, values, maxbits);
+    launch_pdl(q8_max, (unsigned)chunks, kQThreads, 0, s, b, values, maxbits);
     if ((st = check_launch()) != EF_OK) return st;
-    q8_quantize<<<(unsigned)chunks, kQThreads, 0, s>>>(b, values, pos, maxbits, e, out_q,
+    launch_pdl(q8_quantize, (unsigned)chunks, kQThreads, 0, s, b, values, pos, maxbits, e, out_q,
                                                         out_scale);
     if ((st = check_launch()) != EF_OK) return st;
   }
@@ -274,7 +278,7 @@ extern "C" ef_status ef_q8_dequantize(const int8_t* q, const float* scales, int3
   if (st != EF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (const QBatch& b : q8_batches(nseg, nullptr, h_seg_k)) {
-    q8_dequantize<<<(unsigned)b.chunk_base[b.nseg], kQThreads, 0, s>>>(b, q, scales, out_values);
+    launch_pdl(q8_dequantize, (unsigned)b.chunk_base[b.nseg], kQThreads, 0, s, b, q, scales, out_values);
     if ((st = check_launch()) != EF_OK) return st;
   }
   return EF_OK;

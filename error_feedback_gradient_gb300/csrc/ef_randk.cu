@@ -194,6 +194,7 @@ struct RSelectArgs {
 __global__ void __launch_bounds__(kRT)
 rk_sample(RBatch b, const float* __restrict__ g_raw, const float* __restrict__ e,
           double* ssum) {
+  pdl_wait();
   __shared__ int64_t s_base[kRBatch + 1];
   for (int i = threadIdx.x; i <= b.nseg; i += blockDim.x) s_base[i] = b.samp[i];
   __syncthreads();
@@ -339,6 +340,7 @@ template <bool kVec>
 __global__ void __launch_bounds__(kRT, 3)
 rk_sum(RBatch b, const float* __restrict__ g_raw, float* __restrict__ e, uint64_t* acc,
        RSelectArgs a) {
+  pdl_wait();
   __shared__ int64_t s_base[kRBatch + 1];
   __shared__ uint64_t red[kRT / 32][kChunks];
   __shared__ AccSlow slow;
@@ -474,6 +476,8 @@ __device__ double exact_to_double(const uint64_t* chunks) {
 }
 
 __global__ void rk_finalize(RBatch b, const uint64_t* acc, RSelectArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int s = threadIdx.x;
   if (s >= b.nseg) return;
   const double S = exact_to_double(acc + (int64_t)s * kChunks);
@@ -537,6 +541,8 @@ __device__ __forceinline__ uint32_t refine_quad(const RSelectArgs& a, uint32_t q
 template <bool kVec>
 __global__ void __launch_bounds__(kRT, 4)
 rk_refine(RBatch b, RSelectArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kM = kRTileWords / 32;
   __shared__ int64_t s_base[kRBatch + 1];
   __shared__ uint32_t s_in[kRT / 32][kRTileWords], s_out[kRT / 32][kRTileWords];
@@ -637,6 +643,8 @@ rk_refine(RBatch b, RSelectArgs a) {
 // capacity status, base of the next launch).
 __global__ void __launch_bounds__(kRT)
 rk_offsets(int64_t tiles, RSelectArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t scratch[40];
   __shared__ int64_t s_pre;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
@@ -693,6 +701,7 @@ rk_offsets(int64_t tiles, RSelectArgs a) {
 // threads of CTA 0 write the per-segment counts.
 __global__ void __launch_bounds__(kRT)
 rk_pack(RBatch b, RSelectArgs a) {
+  pdl_wait();
   constexpr int kM = kRTileWords / 32;
   __shared__ int64_t s_base[kRBatch + 1];
   __shared__ uint16_t s_keys[kRT / 32][32];
@@ -932,25 +941,25 @@ extern "C" ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, 
     if (sblocks > 0) {
       const int gs = (int)std::min<int64_t>((sblocks + kRT / 32 - 1) / (kRT / 32),
                                             (int64_t)dev.sms * 8);
-      rk_sample<<<gs, kRT, 0, s>>>(b, g_raw, e, ssum);
+      launch_pdl(rk_sample, gs, kRT, 0, s, b, g_raw, e, ssum);
       if ((st = check_launch()) != EF_OK) return st;
     }
     const int ga = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)dev.sms * 3));
-    if (vec) rk_sum<true><<<ga, kRT, 0, s>>>(b, g_raw, e, acc, a);
-    else rk_sum<false><<<ga, kRT, 0, s>>>(b, g_raw, e, acc, a);
+    if (vec) launch_pdl(rk_sum<true>, ga, kRT, 0, s, b, g_raw, e, acc, a);
+    else launch_pdl(rk_sum<false>, ga, kRT, 0, s, b, g_raw, e, acc, a);
     if ((st = check_launch()) != EF_OK) return st;
-    rk_finalize<<<1, kRBatch, 0, s>>>(b, acc, a);
+    launch_pdl(rk_finalize, 1, kRBatch, 0, s, b, acc, a);
     if ((st = check_launch()) != EF_OK) return st;
     // rk_refine: 4 CTAs per SM (58 registers), one wave; rk_pack: 8
     const int gr = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 4));
     const int gw = (int)std::max<int64_t>(1, std::min<int64_t>(warps, (int64_t)dev.sms * 8));
-    if (vec_e) rk_refine<true><<<gr, kRT, 0, s>>>(b, a);
-    else rk_refine<false><<<gr, kRT, 0, s>>>(b, a);
+    if (vec_e) launch_pdl(rk_refine<true>, gr, kRT, 0, s, b, a);
+    else launch_pdl(rk_refine<false>, gr, kRT, 0, s, b, a);
     if ((st = check_launch()) != EF_OK) return st;
     // always: it carries the running offset to the next launch
-    rk_offsets<<<(unsigned)nchunks, kRT, 0, s>>>(tiles, a);
+    launch_pdl(rk_offsets, (unsigned)nchunks, kRT, 0, s, tiles, a);
     if ((st = check_launch()) != EF_OK) return st;
-    rk_pack<<<gw, kRT, 0, s>>>(b, a);
+    launch_pdl(rk_pack, gw, kRT, 0, s, b, a);
     if ((st = check_launch()) != EF_OK) return st;
   }
   return EF_OK;

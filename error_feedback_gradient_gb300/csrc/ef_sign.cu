@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kThreads)
 sign_compress_vec(const float* __restrict__ g, float* __restrict__ eps,
                   uint32_t* __restrict__ bits, int64_t ngroups, float b1, float c,
                   bool bits16) {
+  pdl_wait();
   const unsigned lane = lane_id();
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads)
 sign_compress_words(const float* __restrict__ g, float* __restrict__ eps,
                     uint32_t* __restrict__ bits, int64_t n, int64_t w_begin,
                     int64_t w_end, float b1, float c) {
+  pdl_wait();
   const unsigned lane = lane_id();
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -146,6 +148,7 @@ __device__ __forceinline__ float apply_one(float x, float G, const SignApplyArgs
 __global__ void __launch_bounds__(kThreads, 8)
 sign_apply_vec(SignApplyArgs a, float* __restrict__ G, float* __restrict__ x,
                int64_t nchunks) {
+  pdl_wait();
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   for (int64_t q0 = tid; q0 < nchunks; q0 += nthr * kApplyUnroll) {
@@ -186,6 +189,7 @@ sign_apply_vec(SignApplyArgs a, float* __restrict__ G, float* __restrict__ x,
 __global__ void __launch_bounds__(kThreads)
 sign_apply_scalar(SignApplyArgs a, float* __restrict__ G, float* __restrict__ x,
                   int64_t begin, int64_t n) {
+  pdl_wait();
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = begin + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += nthr) {
     int cnt = 0;
@@ -234,11 +238,11 @@ extern "C" ef_status ef_sign_compress(const float* g, float* eps, int64_t n, flo
       const int64_t resident_warps = (int64_t)dev.sms * 8 * warps_per_block;
       if (ngroups >= 2 * resident_warps * kSpan) {
         const int grid = grid_for(ngroups, warps_per_block * kSpan, dev.sms, 8);
-        sign_compress_vec<kSpan><<<grid, kThreads, 0, s>>>(g, eps, out_bits, ngroups, b1, c,
+        launch_pdl(sign_compress_vec<kSpan>, grid, kThreads, 0, s, g, eps, out_bits, ngroups, b1, c,
                                                            aligned16(out_bits));
       } else {
         const int grid = grid_for(ngroups, warps_per_block * kUnroll, dev.sms, 8);
-        sign_compress_vec<kUnroll><<<grid, kThreads, 0, s>>>(g, eps, out_bits, ngroups, b1, c,
+        launch_pdl(sign_compress_vec<kUnroll>, grid, kThreads, 0, s, g, eps, out_bits, ngroups, b1, c,
                                                              aligned16(out_bits));
       }
       if ((st = check_launch()) != EF_OK) return st;
@@ -247,7 +251,7 @@ extern "C" ef_status ef_sign_compress(const float* g, float* eps, int64_t n, flo
   }
   if (w_begin < nwords) {
     const int grid = grid_for(nwords - w_begin, warps_per_block * kUnroll, dev.sms, 8);
-    sign_compress_words<<<grid, kThreads, 0, s>>>(g, eps, out_bits, n, w_begin, nwords, b1, c);
+    launch_pdl(sign_compress_words, grid, kThreads, 0, s, g, eps, out_bits, n, w_begin, nwords, b1, c);
     if ((st = check_launch()) != EF_OK) return st;
   }
   prof_end(EF_KERNEL_SIGN, s);
@@ -293,14 +297,14 @@ extern "C" ef_status sign_aggregate_apply(int32_t W, const uint32_t* const* h_bi
     const int64_t nchunks = n / 4;
     if (nchunks > 0) {
       const int grid = grid_for(nchunks, kThreads * kApplyUnroll, dev.sms, 8);
-      sign_apply_vec<<<grid, kThreads, 0, s>>>(a, G, w_or_m, nchunks);
+      launch_pdl(sign_apply_vec, grid, kThreads, 0, s, a, G, w_or_m, nchunks);
       if ((st = check_launch()) != EF_OK) return st;
     }
     begin = nchunks * 4;
   }
   if (begin < n) {
     const int grid = grid_for(n - begin, kThreads, dev.sms, 8);
-    sign_apply_scalar<<<grid, kThreads, 0, s>>>(a, G, w_or_m, begin, n);
+    launch_pdl(sign_apply_scalar, grid, kThreads, 0, s, a, G, w_or_m, begin, n);
     if ((st = check_launch()) != EF_OK) return st;
   }
   prof_end(EF_KERNEL_SIGN_APPLY, s);

@@ -183,6 +183,7 @@ __device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t lid
 
 __global__ void __launch_bounds__(kSmallThreads)
 topk_small(SmallBatch b, IO io, int keys_words) {
+  pdl_wait();
   extern __shared__ uint32_t sm[];
   uint32_t* gbits = sm;
   uint32_t* hist = sm + keys_words;
@@ -328,6 +329,8 @@ __device__ __forceinline__ int sample_seg(const SampleGrid& g, int nseg, int blk
 // largest sampled key and the rank r1 left inside it.
 __global__ void __launch_bounds__(kSampleThreads)
 topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t sh[2048];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
@@ -400,6 +403,7 @@ __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& 
 __global__ void __launch_bounds__(kSampleThreads)
 topk_prepare(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist1, SampleState* ss,
              SegState* st) {
+  pdl_wait();
   __shared__ uint32_t sh[1024];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
@@ -510,6 +514,7 @@ struct FusedStage {
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
            uint2* cand, Ctl* ctl, int phase, int vec) {
+  pdl_wait();
   __shared__ int64_t s_base[kMaxLarge + 1];
   __shared__ FusedStage sg;
   __shared__ int s_last;
@@ -720,6 +725,8 @@ constexpr int kRestoreThreads = 256;
 // so a batch without such a segment costs one load per thread.
 __global__ void __launch_bounds__(kRestoreThreads)
 topk_restore(IO io, const SegState* st, int nseg, const uint2* cand) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int64_t s_m[kMaxLarge];  // entries to restore per segment (0: none)
   for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
     const int64_t c = st[s].cand_count;  // <= 0: no candidates, or a reported error
@@ -744,6 +751,8 @@ topk_restore(IO io, const SegState* st, int nseg, const uint2* cand) {
 // shared memory and runs the 3-digit radix select there.
 __global__ void __launch_bounds__(kSmallThreads)
 topk_select_small(IO io, SegState* st, const uint2* cand) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t sm[];
   uint32_t* keys = sm;
   uint32_t* hist = sm + kSelSmall;
@@ -780,6 +789,8 @@ topk_select_small(IO io, SegState* st, const uint2* cand) {
 __global__ void __launch_bounds__(kSelThreads)
 topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, Ctl* ctl,
             int pass) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kPer = kChunk / kSelThreads;  // keys per thread per chunk
   __shared__ uint32_t sh[2048];
   __shared__ int64_t s_cb[kMaxLarge + 1];
@@ -869,6 +880,7 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
 
 __global__ void __launch_bounds__(kEmitThreads)
 topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ctl* ctl) {
+  pdl_wait();
   __shared__ int64_t s_cb[kMaxLarge + 1];
   __shared__ uint32_t s_wgt[kEmitThreads / 32], s_wlt[kEmitThreads / 32];
   __shared__ uint32_t s_ogt[kEmitThreads / 32], s_olt[kEmitThreads / 32];
@@ -1197,7 +1209,7 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     }
     const int keys_words = (maxlen + 3) & ~3;
     const size_t smem = (size_t)(keys_words + 2048 + 64) * 4;
-    topk_small<<<(unsigned)cnt, kSmallThreads, smem, s>>>(sb, io, keys_words);
+    launch_pdl(topk_small, (unsigned)cnt, kSmallThreads, smem, s, sb, io, keys_words);
     if ((st = check_launch()) != EF_OK) return st;
   }
 
@@ -1243,27 +1255,27 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
                             : 1;
       sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
     }
-    topk_sample<<<sg.base[nsg], kSampleThreads, 0, s>>>(lb, sg, nsg, io, hist0, sstate);
+    launch_pdl(topk_sample, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist0, sstate);
     if ((st = check_launch()) != EF_OK) return st;
-    topk_prepare<<<sg.base[nsg], kSampleThreads, 0, s>>>(lb, sg, nsg, io, hist1, sstate, sst);
+    launch_pdl(topk_prepare, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist1, sstate, sst);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
-    topk_fused<<<fgrid, kFusedThreads, 0, s>>>(io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
+    launch_pdl(topk_fused, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
-    topk_restore<<<dev.sms * 2, kRestoreThreads, 0, s>>>(io, sst, nsg, cand);
+    launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
     if ((st = check_launch()) != EF_OK) return st;
-    topk_select_small<<<nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s>>>(io, sst,
+    launch_pdl(topk_select_small, nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s, io, sst,
                                                                                       cand);
     if ((st = check_launch()) != EF_OK) return st;
     const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 3));
     for (int pass = 0; pass < 3; ++pass) {
-      topk_select<<<sgrid, kSelThreads, 0, s>>>(io, sst, nsg, cand, ghist, ctl, pass);
+      launch_pdl(topk_select, sgrid, kSelThreads, 0, s, io, sst, nsg, cand, ghist, ctl, pass);
       if ((st = check_launch()) != EF_OK) return st;
     }
     const int egrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 4));
-    topk_emit<<<egrid, kEmitThreads, 0, s>>>(io, sst, nsg, cand, cstate, ctl);
+    launch_pdl(topk_emit, egrid, kEmitThreads, 0, s, io, sst, nsg, cand, cstate, ctl);
     if ((st = check_launch()) != EF_OK) return st;
   }
   return EF_OK;
