@@ -160,3 +160,120 @@ def test_aggregate_rejects_before_device(lib):
     st = lib.sparse_aggregate_apply(1, 0, vals, inds, None, _i64([1]), 10, 0.1, w, w, ws,
                                     1 << 20, None)
     assert st == d["EF_ERR_ALIAS"]
+
+
+def _randk_ws(lib, n, offs, ks):
+    out = ctypes.c_size_t(0)
+    st = lib.ef_randk_workspace_size(n, len(ks), _i64(offs), _i64(ks), ctypes.byref(out))
+    return st, out.value
+
+
+def test_randk_workspace_and_rejects_before_device(lib):
+    d = _header_defines()
+    st, small = _randk_ws(lib, 1000, [0, 1000], [10])
+    assert st == d["EF_OK"] and small >= 256
+    st, big = _randk_ws(lib, 1 << 31, [0, 1 << 31], [1 << 21])
+    assert st == d["EF_OK"] and big >= (1 << 31) // 8          # keep bits: n / 8 bytes
+    assert _randk_ws(lib, 100, [0, 50, 100], [51, 1])[0] == d["EF_ERR_K"]
+    assert _randk_ws(lib, 100, [0, 60, 50, 100], [1, 1, 1])[0] == d["EF_ERR_SEGMENTS"]
+    assert _randk_ws(lib, (1 << 31) + 4, [0, (1 << 31) + 4], [1])[0] == d["EF_ERR_SIZE"]
+    n, offs, ks = 1000, [0, 1000], [10]
+    _, wsb = _randk_ws(lib, n, offs, ks)
+    g, e = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
+    vals, idx = ctypes.c_void_p(3 << 20), ctypes.c_void_p(4 << 20)
+    cnt, ws = ctypes.c_void_p(5 << 20), ctypes.c_void_p(6 << 20)
+
+    def call(g=g, e=e, ks=ks, vals=vals, idx=idx, cap=100, cnt=cnt, ws=ws, wsb=wsb):
+        return lib.ef_randk_compress(g, e, n, len(ks), _i64(offs), _i64(ks), 1, 0, vals, idx,
+                                     cap, cnt, ws, wsb, None)
+    assert call(ks=[1001]) == d["EF_ERR_K"]
+    assert call(ws=None) == d["EF_ERR_WORKSPACE"]
+    assert call(ws=ctypes.c_void_p((6 << 20) + 128)) == d["EF_ERR_WORKSPACE"]   # misaligned
+    assert call(wsb=wsb - 1) == d["EF_ERR_WORKSPACE"]
+    assert call(cap=-1) == d["EF_ERR_ARG"]
+    assert call(cnt=None) == d["EF_ERR_NULL"]
+    assert call(vals=None) == d["EF_ERR_NULL"]
+    assert call(cnt=ctypes.c_void_p((5 << 20) + 4)) == d["EF_ERR_ALIGN"]
+    assert call(e=g) == d["EF_ERR_ALIAS"]
+    assert call(idx=ctypes.c_void_p((3 << 20) + 8)) == d["EF_ERR_ALIAS"]  # inside the values
+
+
+def _codec_sizes(lib, codec, K, n):
+    mb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib.ef_index_codec_sizes(codec, K, n, ctypes.byref(mb), ctypes.byref(wb))
+    return st, mb.value, wb.value
+
+
+def test_codec_sizes_follow_the_header(lib):
+    d = _header_defines()
+    for K, n in [(0, 1), (1, 1), (1000, 100_000), (2_147_484, 1 << 31)]:
+        nblk = -(-n // 65536)
+        nfw = -(-(-(-n // 256)) // 32)
+        st, mb, wb = _codec_sizes(lib, d["EF_CODEC_LOCAL16"], K, n)
+        assert st == d["EF_OK"] and mb == 4 * (nblk + 1) + 2 * K and wb >= 256
+        st, mb, _ = _codec_sizes(lib, d["EF_CODEC_RUNVARINT"], K, n)
+        assert st == d["EF_OK"] and mb == 5 * K
+        st, mb, _ = _codec_sizes(lib, d["EF_CODEC_BLOCK256"], K, n)
+        assert st == d["EF_OK"] and mb == 4 * nfw + 2 * K
+    assert _codec_sizes(lib, 9, 10, 100)[0] == d["EF_ERR_ARG"]
+    assert _codec_sizes(lib, d["EF_CODEC_LOCAL16"], 101, 100)[0] == d["EF_ERR_K"]
+    assert _codec_sizes(lib, d["EF_CODEC_LOCAL16"], 1, (1 << 31) + 1)[0] == d["EF_ERR_SIZE"]
+
+
+def test_codec_rejects_before_device(lib):
+    d = _header_defines()
+    K, n = 100, 100_000
+    idx, out = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
+    ob, ws = ctypes.c_void_p(3 << 20), ctypes.c_void_p(4 << 20)
+    for codec in (d["EF_CODEC_LOCAL16"], d["EF_CODEC_RUNVARINT"], d["EF_CODEC_BLOCK256"]):
+        _, mb, wb = _codec_sizes(lib, codec, K, n)
+        enc = lambda **kw: lib.ef_index_encode(  # noqa: E731
+            codec, kw.get("idx", idx), K, n, out, kw.get("cap", mb), kw.get("ob", ob),
+            kw.get("ws", ws), wb, None)
+        assert enc(ws=None) == d["EF_ERR_WORKSPACE"]
+        assert enc(idx=None) == d["EF_ERR_NULL"]
+        assert enc(cap=mb - 1) == d["EF_ERR_SIZE"]
+        assert enc(ob=ctypes.c_void_p((3 << 20) + 4)) == d["EF_ERR_ALIGN"]
+        assert enc(idx=ctypes.c_void_p((2 << 20) + 16)) == d["EF_ERR_ALIAS"]   # inside out
+        assert lib.ef_index_decode(codec, out, mb, K, n, None, ws, wb, None) == d["EF_ERR_NULL"]
+    # lengths the formats cannot have
+    _, mb, wb = _codec_sizes(lib, d["EF_CODEC_LOCAL16"], K, n)
+    assert lib.ef_index_decode(d["EF_CODEC_LOCAL16"], out, mb - 2, K, n, idx, ws, wb,
+                               None) == d["EF_ERR_PACKET"]
+    _, mb, wb = _codec_sizes(lib, d["EF_CODEC_RUNVARINT"], K, n)
+    assert lib.ef_index_decode(d["EF_CODEC_RUNVARINT"], out, K - 1, K, n, idx, ws, wb,
+                               None) == d["EF_ERR_PACKET"]
+    _, mb, wb = _codec_sizes(lib, d["EF_CODEC_BLOCK256"], K, n)
+    nfw = -(-(-(-n // 256)) // 32)
+    assert lib.ef_index_decode(d["EF_CODEC_BLOCK256"], out, 4 * nfw + K, K, n, idx, ws, wb,
+                               None) == d["EF_ERR_PACKET"]      # no flagged block counts
+
+
+def test_q8_rejects_before_device(lib):
+    d = _header_defines()
+    out = ctypes.c_size_t(0)
+    assert lib.ef_topk_q8_workspace_size(1000, 1, _i64([0, 1000]), _i64([10]), 0,
+                                         ctypes.byref(out)) == d["EF_OK"]
+    wsb = out.value
+    assert wsb >= 256
+    assert lib.ef_topk_q8_workspace_size(1000, 1, _i64([0, 1000]), _i64([1001]), 0,
+                                         ctypes.byref(out)) == d["EF_ERR_K"]
+    g, e = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20)
+    q, sc, idx = ctypes.c_void_p(3 << 20), ctypes.c_void_p(4 << 20), ctypes.c_void_p(5 << 20)
+    ws = ctypes.c_void_p(6 << 20)
+
+    def call(q=q, sc=sc, ws=ws):
+        return lib.ef_topk_compress_q8(g, e, 1000, 1, _i64([0, 1000]), _i64([10]), 0, q, sc,
+                                       idx, None, ws, wsb, None)
+    assert call(ws=None) == d["EF_ERR_WORKSPACE"]
+    assert call(sc=None) == d["EF_ERR_NULL"]
+    assert call(q=None) == d["EF_ERR_NULL"]
+    assert call(sc=ctypes.c_void_p((4 << 20) + 2)) == d["EF_ERR_ALIGN"]
+    assert call(sc=ctypes.c_void_p((3 << 20) + 4)) == d["EF_ERR_ALIAS"]      # inside the codes
+    vals = ctypes.c_void_p(7 << 20)
+    assert lib.ef_q8_dequantize(q, sc, 0, _i64([1]), vals, None) == d["EF_ERR_SEGMENTS"]
+    assert lib.ef_q8_dequantize(q, sc, 1, _i64([-1]), vals, None) == d["EF_ERR_K"]
+    assert lib.ef_q8_dequantize(None, None, 1, _i64([0]), None, None) == d["EF_OK"]  # nothing
+    assert lib.ef_q8_dequantize(None, sc, 1, _i64([4]), vals, None) == d["EF_ERR_NULL"]
+    assert lib.ef_q8_dequantize(q, ctypes.c_void_p((4 << 20) + 1), 1, _i64([4]), vals,
+                                None) == d["EF_ERR_ALIGN"]
