@@ -40,19 +40,19 @@ METRIC = "G grad elements/s per EF compress+apply step; HBM GB/s vs GB300 peak (
 UNIT = "G grad elements/s"
 
 # DRAM traffic of one topk_fused launch from one ncu capture (--set full,
-# slab workload at n = 2^26 per worker, see profiles/): 536.95 MB read +
-# 223.93 MB written = 11.338 bytes per element.  Reported, scaled by n, only
+# slab workload at n = 2^26 per worker, see profiles/): 536.96 MB read +
+# 224.00 MB written = 11.339 bytes per element.  Reported, scaled by n, only
 # while the captured code still hashes to what was captured (the kernel's
 # region of ef_topk.cu, from its staging struct to the end of the kernel, and
 # the shared device header); otherwise null.  (Reads scale with n exactly;
 # the writes fall short of 12 B by the dirty lines still in L2 when the
 # captured launch ends.)
-FUSED_TRAFFIC_PER_ELEMENT = 11.338
+FUSED_TRAFFIC_PER_ELEMENT = 11.339
 FUSED_TRAFFIC_SOURCES = {
     # (file, first marker, end marker or None for the whole file): sha256
     ("error_feedback_gradient_gb300/csrc/ef_topk.cu", "struct FusedStage {",
      "// A segment's select list:"):
-        "1a8a2038b0d7de75062dffca2ef10bc1ed3a3e7e86fa440af5287d89c0ff643d",
+        "ac3e3b1803607664f19791741692b953ed06478e7763f53ce3f180224be6bb55",
     ("error_feedback_gradient_gb300/csrc/ef_common.cuh", None, None):
         "2bbcf9705edd30ef00918744e5b1800515cb99aba3bd167ee166c761eb82a3cc",
 }

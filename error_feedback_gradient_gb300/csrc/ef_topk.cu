@@ -57,6 +57,13 @@ constexpr int kSmallThreads = 1024;
 constexpr int kStreamWarps = 8;                 // fused pass: warps that stream the tile
 constexpr int kWarpSpan = 4096;                 // elements per streaming warp per tile
 constexpr int kTile = kStreamWarps * kWarpSpan;  // 32768 elements per fused-pass tile
+// Batches whose 32768-element tiles would occupy under half of the
+// persistent grid use 8192-element tiles, so that more SMs stream; larger
+// batches keep the longer tiles (fewer per-tile barriers and look-backs,
+// which cost more than a partial last round: 161 ResNet-50 tensors took
+// 0.155 ms per step with the long tiles and 0.177 ms with the short).
+constexpr int kWarpSpanSmall = 1024;
+constexpr int kTileSmall = kStreamWarps * kWarpSpanSmall;
 constexpr int kStreamThreads = kStreamWarps * 32;
 constexpr int kFusedThreads = kStreamThreads + 32;  // + one scan warp
 constexpr int kStageCap = 256;                  // staged candidates per warp per buffer
@@ -74,6 +81,7 @@ constexpr uint32_t kNoEntry = 0xFFFFFFFFu;      // candidate-list slot of an uns
 constexpr int kSelSmall = 32768;  // lists up to this length are selected by one CTA
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
+static_assert(kWarpSpanSmall % (128 * kBatch) == 0, "tile layout");
 static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
 static_assert(kChunk % kSelThreads == 0, "select layout");
 
@@ -92,7 +100,7 @@ struct LargeSeg {
   int64_t off, len, k, out_off;
   int64_t cand_base, cap;
   int64_t tile_base;  // global id of the segment's first fused tile
-  int64_t q_first;    // index of that tile in aligned kTile units
+  int64_t q_first;    // index of that tile in aligned units of the pass's tile
   int64_t rank;       // sample rank for T_lo (0: no candidates, > samples: all)
 };
 
@@ -511,6 +519,7 @@ struct FusedStage {
 // buffer, resolves the tile's offset in its segment's candidate list with the
 // bounded decoupled look-back, and writes the candidates out; two buffers let
 // the streaming warps run one tile ahead of it.
+template <int kSpan>
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
            uint2* cand, Ctl* ctl, int phase, int vec) {
@@ -546,17 +555,17 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
       const int64_t a = st[seg].d.off;
       const uint32_t t_lo = st[seg].t_lo;
       // this warp's 2048-element window, as pointers and 32-bit offsets
-      const int64_t w0 = (st[seg].d.q_first + (tile - s_base[seg])) * kTile +
-                         (int64_t)warp * kWarpSpan - phase;
+      const int64_t w0 = (st[seg].d.q_first + (tile - s_base[seg])) * (kStreamWarps * kSpan) +
+                         (int64_t)warp * kSpan - phase;
       const float* gp = io.g_raw + w0;
       float* ep = io.e + w0;
-      const int lo = (int)max((int64_t)-4, min(a - w0, (int64_t)kWarpSpan));
-      const int hi = (int)max((int64_t)-4, min(a + st[seg].d.len - w0, (int64_t)kWarpSpan + 4));
+      const int lo = (int)max((int64_t)-4, min(a - w0, (int64_t)kSpan));
+      const int hi = (int)max((int64_t)-4, min(a + st[seg].d.len - w0, (int64_t)kSpan + 4));
       const uint32_t loc0 = (uint32_t)(w0 - a);  // local index of window offset 0 (mod 2^32)
       uint2* stage = sg.cand[b][warp];
       uint32_t count = 0;
 #pragma unroll 1
-      for (int r0 = 0; r0 < kWarpSpan / 128; r0 += kBatch) {
+      for (int r0 = 0; r0 < kSpan / 128; r0 += kBatch) {
         float4 gr[kBatch], ee[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -573,7 +582,7 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
             }
           }
         }
-        if (r0 + kBatch == kWarpSpan / 128 && threadIdx.x == 0)
+        if (r0 + kBatch == kSpan / 128 && threadIdx.x == 0)
           ticket = atomicAdd(&ctl->fused_ticket, 1u);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -1055,7 +1064,7 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
       d.cand_base = cur.cand_total;
       d.rank = sample_rank(k, len);
       cur.cand_total += d.cap;
-      cur.max_tiles += (len + kTile - 1) / kTile + 1;
+      cur.max_tiles += (len + kTileSmall - 1) / kTileSmall + 1;  // either tile size
       cur.max_chunks += (len + kChunk - 1) / kChunk;
       cur.segs.push_back(d);
       if ((int)cur.segs.size() == kMaxLarge) {
@@ -1226,16 +1235,23 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
   uint2* cand = reinterpret_cast<uint2*>(ws + p.off_cand);
   for (Batch& b : p.batches) {
     LargeBatch lb;
-    int64_t tiles = 0;
     const int nsg = (int)b.segs.size();
-    for (int i = 0; i < nsg; ++i) {
-      LargeSeg d = b.segs[i];
-      const int64_t qa = d.off + phase, qb = d.off + d.len + phase;
-      d.q_first = qa / kTile;
-      d.tile_base = tiles;
-      tiles += (qb - 1) / kTile - d.q_first + 1;
-      lb.seg[i] = d;
-    }
+    auto count_tiles = [&](int64_t tile) {
+      int64_t n_t = 0;
+      for (int i = 0; i < nsg; ++i) {
+        LargeSeg d = b.segs[i];
+        const int64_t qa = d.off + phase, qb = d.off + d.len + phase;
+        d.q_first = qa / tile;
+        d.tile_base = n_t;
+        n_t += (qb - 1) / tile - d.q_first + 1;
+        lb.seg[i] = d;
+      }
+      return n_t;
+    };
+    const int64_t cap_ctas = (int64_t)dev.sms * kFusedCtasPerSm;
+    int64_t tiles = count_tiles(kTile);
+    const bool small_tiles = 2 * tiles <= cap_ctas;
+    if (small_tiles) tiles = count_tiles(kTileSmall);
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(ws + p.off_hist0);
@@ -1261,7 +1277,12 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
-    launch_pdl(topk_fused, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate, cand, ctl, phase, vec);
+    if (small_tiles)
+      launch_pdl(topk_fused<kWarpSpanSmall>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles,
+                 tstate, cand, ctl, phase, vec);
+    else
+      launch_pdl(topk_fused<kWarpSpan>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate,
+                 cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
     launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
