@@ -20,7 +20,13 @@
  *   may be reused by the next call on the same stream.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *   default stream).  Calls enqueue work on it and return without
- *   synchronising; no device-to-host read-back happens inside a call.
+ *   synchronising; no device-to-host read-back happens inside a call.  The
+ *   kernels are launched with programmatic stream serialization: one may be
+ *   scheduled while the kernel before it in the stream drains, but none
+ *   touches memory before every earlier kernel in the stream has completed,
+ *   so the order of effects is the stream order.  A caller's own kernel
+ *   launched with that attribute right after a call must likewise wait
+ *   (cudaGridDependencySynchronize) before reading the call's outputs.
  * Numbers.  Every float is IEEE-754 binary32; every arithmetic step is a
  *   single round-to-nearest-even operation, never a fused multiply-add, in
  *   the order stated per function, so results are reproducible bit for bit.
