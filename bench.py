@@ -873,6 +873,80 @@ def run_next(args, dev):
     return out
 
 
+def run_exchange(args, rank, world, local):
+    """The exchanged step (--exchange): one worker per rank, each with its own
+    gradient of n elements; per step a top-0.1 % int32 compress, then the
+    packet exchange across the ranks (all-gather of the packets, or the
+    index-range reduce-scatter) and the receive side with SGD.  Units per
+    step: world x n gradient elements.  With one process a world-size-1
+    group is created, so the collectives still run."""
+    import socket
+    import torch
+    import torch.distributed as dist
+    import error_feedback_gradient_gb300 as efg
+    from error_feedback_gradient_gb300 import exchange as ex
+    from error_feedback_gradient_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if not dist.is_initialized():
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1)
+    n = args.n
+    wk = wl.workload("slab_2p31", n)
+    k = wk.total_k
+    offs, ks = list(wk.seg_offsets), list(wk.seg_k)
+    g = wk.gradient(rank, 1, dev)
+    e = torch.zeros_like(g)
+    vals = torch.empty(k, device=dev)
+    idx = torch.empty(k, dtype=torch.int32, device=dev)
+    ws = torch.empty(efg.topk_workspace_size(n, offs, ks), dtype=torch.uint8, device=dev)
+    x = ex.Exchange(n, k, efg.IDX_INT32)
+    w = torch.empty(ex.padded_length(n, world), device=dev)
+    w[:n].copy_(wk.weights(dev))
+    G = torch.empty(n if args.exchange == "allgather" else x.s, device=dev)
+
+    def step():
+        efg.topk_compress(g, e, offs, ks, vals, idx, None, ws)
+        if args.exchange == "allgather":
+            x.allgather_apply(vals, idx, wk.eta, G, w[:n])
+        else:
+            x.range_apply(vals, idx, wk.eta, w, G)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    launches0 = efg.kernel_launches()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps)
+    if efg.workspace_status(ws) != 0:
+        raise RuntimeError("top-k device status")
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": world * n / (ms * 1e-3) / 1e9, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": (f"exchanged step: one worker per rank, n={n} "
+                                    f"Student-t(3)x1e-3, top-0.1% int32 (k={k}), "
+                                    f"{args.exchange} exchange, receive side + SGD eta="
+                                    f"{wk.eta}"),
+                       "exchange": args.exchange, "parallelism": f"dp{world}",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "gpu_launches": efg.kernel_launches() - launches0}), flush=True)
+
+
 def run_case(args):
     """One entry point alone, three calls, for profiling its kernels in
     isolation (--case): 'topk' (one tensor of n elements, top-0.1 %),
@@ -1001,6 +1075,9 @@ def main(argv=None):
     p.add_argument("--traffic-per-launch", type=float, default=None,
                    help="DRAM bytes of one topk_fused launch at this size, from ncu")
     p.add_argument("--no-extras", dest="extras", action="store_false")
+    p.add_argument("--exchange", choices=["allgather", "range"], default=None,
+                   help="time the exchanged step instead: one worker per rank, top-k, "
+                        "packet exchange across the ranks, receive side")
     p.add_argument("--case", choices=["topk", "aggregate", "randk", "resnet50", "sign", "q8",
                                        "codec"],
                    default=None,
@@ -1013,7 +1090,9 @@ def main(argv=None):
                           "Student-t(3)x1e-3; top-0.1% int32 + bitmap EF and 1-bit EF "
                           "(beta1=0.9), each aggregated locally with SGD eta=0.1")
     rank, world, local = dist_setup()
-    if args.impl == "reference":
+    if args.exchange and args.impl == "ours":
+        run_exchange(args, rank, world, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

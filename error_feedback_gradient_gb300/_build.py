@@ -21,7 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "lib")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["ef_api.cu", "ef_sign.cu", "ef_topk.cu", "ef_aggregate.cu", "ef_quant.cu", "ef_codec.cu", "ef_randk.cu"]
+SOURCES = ["ef_api.cu", "ef_sign.cu", "ef_topk.cu", "ef_aggregate.cu", "ef_quant.cu", "ef_codec.cu", "ef_randk.cu",
+           "ef_exchange.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,6 +61,7 @@ _SIGNATURES = {
     "ef_topk_compress_noalloc": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p,
         ctypes.c_int32, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "ef_topk_noalloc_status": (ctypes.c_int32, [_c_vp, ctypes.POINTER(ctypes.c_int32)]),
     "ef_topk_q8_workspace_size": (ctypes.c_int32, [
         ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_i64p, ctypes.c_int32,
         ctypes.POINTER(ctypes.c_size_t)]),
@@ -95,6 +96,9 @@ _SIGNATURES = {
     "sign_aggregate_apply": (ctypes.c_int32, [
         ctypes.c_int32, _c_vpp, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
         ctypes.c_float, _c_vp, _c_vp, _c_vp]),
+    "ef_packet_split": (ctypes.c_int32, [
+        _c_vp, ctypes.c_int64, ctypes.c_int32, _c_i64p, _c_vp, _c_vp]),
+    "ef_index_rebase": (ctypes.c_int32, [_c_vp, ctypes.c_int64, ctypes.c_int64, _c_vp]),
     "ef_workspace_status": (ctypes.c_int32, [
         _c_vp, _c_vp, ctypes.POINTER(ctypes.c_int32)]),
     "ef_profile_events": (ctypes.c_int32, [ctypes.c_int32, _c_vp, _c_vp]),
@@ -203,6 +207,15 @@ def topk_compress_noalloc(g_raw: torch.Tensor, e: torch.Tensor, seg_offsets: Seq
         _ptr(g_raw), _ptr(e), g_raw.numel(), len(seg_k), _i64(seg_offsets), _i64(seg_k),
         int(idx_format), _ptr(out_values), _ptr(out_indices), _ptr(out_bitmap),
         _stream(stream)), "ef_topk_compress_noalloc")
+
+
+def topk_noalloc_status(stream=None) -> int:
+    """ef_topk_noalloc_status: the device-side status of the last
+    allocation-free top-k call on the current device (synchronises)."""
+    out = ctypes.c_int32(0)
+    _check(library().ef_topk_noalloc_status(_stream(stream), ctypes.byref(out)),
+           "ef_topk_noalloc_status")
+    return int(out.value)
 
 
 def topk_q8_workspace_size(n: int, seg_offsets: Sequence[int], seg_k: Sequence[int],
@@ -387,3 +400,27 @@ def profile_events(kernel_id: int, start, stop) -> None:
     s = None if start is None else start.cuda_event
     t = None if stop is None else stop.cuda_event
     _check(library().ef_profile_events(int(kernel_id), s, t), "ef_profile_events")
+
+
+# ---------------------------------------------------------------------------
+# device steps of the index-range packet exchange
+# ---------------------------------------------------------------------------
+
+
+def packet_split(indices: torch.Tensor, k: int, bounds: Sequence[int],
+                 starts: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """ef_packet_split: starts[q] = number of the first k entries of the
+    ascending packet `indices` below bounds[q] (int64 device tensor of
+    len(bounds) entries, allocated here unless given)."""
+    if starts is None:
+        starts = torch.empty(len(bounds), dtype=torch.int64, device=indices.device)
+    _check(library().ef_packet_split(
+        _ptr(indices), int(k), len(bounds) - 1, _i64(bounds), _ptr(starts),
+        _stream(stream)), "ef_packet_split")
+    return starts
+
+
+def index_rebase(indices: torch.Tensor, count: int, base: int, stream=None) -> None:
+    """ef_index_rebase: indices[:count] -= base, in place."""
+    _check(library().ef_index_rebase(_ptr(indices), int(count), int(base), _stream(stream)),
+           "ef_index_rebase")

@@ -141,6 +141,19 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
+// Shared-memory histogram update: every lane with `valid` set counts one
+// key in hist[bin].  All 32 lanes call it together (the callers keep their
+// trip counts warp-uniform).  It is a plain shared-memory atomicAdd per key:
+// a warp-aggregated form (one atomicAdd of the lane count per distinct bin,
+// the lanes grouped with __match_any_sync) measured slower on GB300 in every
+// case tried, ties included -- the ResNet-50 layerwise call 0.156 against
+// 0.126 ms, an all-equal 2^29-element tensor 8.21 against 7.26 ms, the 2^20
+// top-k call 79.8 against 57.5 us -- and so did aggregating only when the
+// whole warp shares one bin (0.133 ms, 8.55 ms, 62.7 us).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool valid) {
+  if (valid) atomicAdd(&hist[bin], 1u);
+}
+
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -288,20 +301,33 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* hist, int nbins, 
   __syncthreads();
 }
 
-__device__ __forceinline__ SelectResult block_radix_select(const uint32_t* keys, int n, uint32_t k,
-                                                           uint32_t* hist, uint32_t* scratch) {
-  const int shifts[3] = {20, 10, 0};
-  const int widths[3] = {11, 10, 10};
+// The same over keys produced by `key_at(i)` (i < n, 64-bit), e.g. read
+// from global memory; eight keys per thread are loaded before any is
+// counted, so a global source keeps eight loads in flight per thread.
+template <typename KeyAt>
+__device__ __forceinline__ SelectResult block_radix_select_at(int64_t n, uint32_t k, uint32_t* hist,
+                                                              uint32_t* scratch, KeyAt key_at) {
   uint32_t prefix = 0, krem = k, gt = 0;
   for (int p = 0; p < 3; ++p) {
-    const int shift = shifts[p], nb = 1 << widths[p];
-    const int hi = shift + widths[p];  // bits above this digit are fixed
+    // digits: bits 30..20, 19..10, 9..0
+    const int shift = 20 - 10 * p, width = p == 0 ? 11 : 10;
+    const int nb = 1 << width;
+    const int hi = shift + width;  // bits above this digit are fixed
     for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint32_t key = keys[i] & 0x7FFFFFFFu;
-      if (hi >= 31 || (key >> hi) == (prefix >> hi))
-        atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    for (int64_t i0 = 0; i0 < n; i0 += 8 * (int64_t)blockDim.x) {
+      uint32_t key[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + u * (int64_t)blockDim.x + threadIdx.x;
+        key[u] = i < n ? key_at(i) & 0x7FFFFFFFu : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + u * (int64_t)blockDim.x + threadIdx.x;
+        const bool in = i < n && (hi >= 31 || (key[u] >> hi) == (prefix >> hi));
+        hist_add(hist, (key[u] >> shift) & (nb - 1), in);
+      }
     }
     __syncthreads();
     uint32_t bin, above;
@@ -311,6 +337,12 @@ __device__ __forceinline__ SelectResult block_radix_select(const uint32_t* keys,
     krem -= above;
   }
   return SelectResult{prefix, gt, krem};
+}
+
+__device__ __forceinline__ SelectResult block_radix_select(const uint32_t* keys, int n, uint32_t k,
+                                                           uint32_t* hist, uint32_t* scratch) {
+  return block_radix_select_at((int64_t)n, k, hist, scratch,
+                               [keys](int64_t i) { return keys[i]; });
 }
 
 }  // namespace ef

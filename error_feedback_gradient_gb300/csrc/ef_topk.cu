@@ -5,14 +5,14 @@
 //
 // Segments of at most kSmallMax elements are finished by one CTA each with
 // the whole segment in shared memory (compensate, 3-digit radix select,
-// ordered emit).  Longer segments take the streaming path, batched over all
-// such segments of a call:
-//   1. sample + prepare (32 CTAs per segment each): up to 4096 blocks of 64
+// ordered emit).  Longer segments take the streaming path, batched over the
+// streaming segments of a call:
+//   1. sample   (up to 128 CTAs per segment): up to 4096 blocks of 64
 //      contiguous elements (at most 1/16 of the segment) are compensated,
-//      and two histogram passes over their keys (top 11 bits, then the next
-//      10 inside the chosen bin) give a conservative lower threshold T_lo:
-//      the lower edge of the 21-bit bin holding the rank-th largest sampled
-//      key.  Only a speed-up: the result never depends on it.
+//      and one histogram of the top 13 bits of their keys gives a
+//      conservative lower threshold T_lo: the lower edge of the bin holding
+//      the rank-th largest sampled key.  Only a speed-up: the result never
+//      depends on it.
 //   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e,
 //      except that a key >= T_lo is written as +0 and appended, in index
 //      order, to a per-segment candidate list (warp ballots and a bounded
@@ -20,12 +20,17 @@
 //      buffer or the list keeps g in e.  The last CTA checks each list:
 //      between k and its capacity -> select on the list; otherwise (T_lo too
 //      high or overflow) -> select on the whole segment, which is always
-//      correct, only slower; `restore` then first puts g back at the listed
-//      candidates.
-//   3. select   (x3): radix select on 11/10/10-bit digits of the keys of
-//      each list, shared-memory histograms merged into one per segment; the
-//      last CTA of each pass fixes that digit.  Result: the k-th key T and
-//      need = k - #(key > T).
+//      correct, only slower, once g is back in e at the listed candidates.
+// A compact batch (every list expected to fit one CTA's shared memory, as
+// for the tensors of a layerwise model) ends with
+//   3c. finish  one CTA per segment selects on its list and emits it, in
+//      shared memory; the same launch runs the call's small segments.
+// Other batches end with
+//   3. restore, then select (x3): radix select on 11/10/10-bit digits of the
+//      keys of each list, shared-memory histograms merged into one per
+//      segment; the last CTA of each pass fixes that digit (lists of at most
+//      kSelSmall entries are resolved by one CTA first).  Result: the k-th
+//      key T and need = k - #(key > T).
 //   4. emit     ordered compaction of the list: an entry is taken when
 //      key > T, or key == T and fewer than `need` equal keys precede it;
 //      position = #(key > T before it) + min(#(key == T before it), need).
@@ -79,6 +84,12 @@ constexpr int kMaxSmall = 512;     // segments per small-path launch
 constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
 constexpr uint32_t kNoEntry = 0xFFFFFFFFu;      // candidate-list slot of an unstaged candidate
 constexpr int kSelSmall = 32768;  // lists up to this length are selected by one CTA
+// Compact batches: every streaming segment is at most kCompactLen elements
+// and its expected candidate list at most half of kFinishCap entries, so one
+// CTA finishes it in shared memory (topk_finish) and the three digit passes
+// and the look-back emit are not launched.
+constexpr int kFinishCap = kSelSmall;
+constexpr int64_t kCompactLen = int64_t(1) << 22;
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
 static_assert(kWarpSpanSmall % (128 * kBatch) == 0, "tile layout");
@@ -129,11 +140,9 @@ struct SegState {
   int64_t cand_count;       // candidates found by the fused pass (-1: unknown)
 };
 
-// Per-segment state of the two sampling passes (in the cleared control area).
+// Per-segment state of the sampling pass (in the cleared control area).
 struct SampleState {
-  uint32_t done[2];  // CTAs finished in the first / second pass
-  uint32_t b0;       // top-11-bit bin holding the rank-th largest sampled key
-  uint32_t r1;       // that key's rank inside the bin
+  uint32_t done;  // CTAs finished
 };
 
 // Sample blocks of a segment of `len` elements (> kSmallMax): at most 1/16
@@ -185,63 +194,51 @@ __device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t lid
   if (zero_e) io.e[gidx] = 0.0f;
 }
 
-// ---------------------------------------------------------------------------
-// small segments: one CTA holds the whole segment
-// ---------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(kSmallThreads)
-topk_small(SmallBatch b, IO io, int keys_words) {
-  pdl_wait();
-  extern __shared__ uint32_t sm[];
-  uint32_t* gbits = sm;
-  uint32_t* hist = sm + keys_words;
-  uint32_t* scratch = hist + 2048;
-  const SmallSeg sg = b.seg[blockIdx.x];
-  const int len = sg.len;
-  const float* gr = io.g_raw + sg.off;
-  float* e = io.e + sg.off;
-  // eight elements of each array in flight per thread
-  for (int i0 = threadIdx.x; i0 < len; i0 += 8 * kSmallThreads) {
-    float gv[8], ev[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * kSmallThreads;
-      gv[u] = i < len ? gr[i] : 0.0f;
-      ev[u] = i < len ? e[i] : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * kSmallThreads;
-      if (i < len) {
-        const float x = __fadd_rn(gv[u], ev[u]);
-        e[i] = x;
-        gbits[i] = __float_as_uint(x);
-      }
-    }
-  }
-  __syncthreads();
-  if (sg.k == 0) return;
-  const SelectResult r = block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch);
-  // Ordered emit: warp w owns the contiguous range [w * span, (w + 1) * span);
-  // one pass counts (greater, equal) per warp, one scan of the 32 warp counts
-  // gives each warp its offsets, and a second pass emits with ballots.
+// Ordered emit by one CTA over a list of n entries whose k-th key T and tie
+// count `need` are known: an entry is taken when key > T, or key == T and
+// fewer than `need` equal keys precede it; its packet position is
+// #(key > T before it) + min(#(key == T before it), need).  Warp w owns the
+// contiguous range [w * span, (w + 1) * span); one pass counts (greater,
+// equal) per warp, a scan of the warp counts gives each warp its offsets,
+// and a second pass emits with ballots.  `bits_at(j)` gives entry j's float
+// bits, `loc_at(j)` its local index in the segment.  On a candidate list
+// (`on_list`) e already holds +0 at every entry, so the entries not taken get
+// their value back in e; otherwise e is set to +0 at the taken entries.
+// Eight entries per lane are loaded before any is counted.  `shm` holds 64
+// words of shared memory.
+template <typename BitsAt, typename LocAt>
+__device__ __forceinline__ void block_ordered_emit(const IO& io, int64_t n, uint32_t T,
+                                                   uint32_t need, int64_t seg_off,
+                                                   int64_t out_off, int64_t k, bool on_list,
+                                                   uint32_t* shm, BitsAt bits_at, LocAt loc_at) {
+  constexpr int kRound = 8 * 32;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
-  const int span = ((len + nwarps - 1) / nwarps + 31) & ~31;
-  const int w0 = warp * span, w1 = min(w0 + span, len);
+  const int64_t span = ((n + nwarps - 1) / nwarps + kRound - 1) / kRound * kRound;
+  const int64_t w0 = min((int64_t)warp * span, n), w1 = min(w0 + span, n);
   uint32_t cg = 0, ce = 0;
-  for (int i = w0 + (int)lane; i < w1; i += 32) {
-    const uint32_t key = gbits[i] & 0x7FFFFFFFu;
-    cg += key > r.T;
-    ce += key == r.T;
+  for (int64_t b = w0; b < w1; b += kRound) {
+    uint32_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = b + u * 32 + lane;
+      v[u] = j < w1 ? bits_at(j) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = b + u * 32 + lane;
+      const uint32_t key = v[u] & 0x7FFFFFFFu;
+      cg += j < w1 && key > T;
+      ce += j < w1 && key == T;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     cg += __shfl_xor_sync(kFull, cg, o);
     ce += __shfl_xor_sync(kFull, ce, o);
   }
-  uint32_t* wgt = hist;            // the histogram is free again: reuse it
-  uint32_t* weq = hist + 32;
+  uint32_t* wgt = shm;
+  uint32_t* weq = shm + 32;
   if (lane == 0) {
     wgt[warp] = cg;
     weq[warp] = ce;
@@ -259,22 +256,84 @@ topk_small(SmallBatch b, IO io, int keys_words) {
   __syncthreads();
   uint32_t run_gt = wgt[warp], run_eq = weq[warp];
   const unsigned lm = lanemask_lt();
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + (int)lane;
-    const uint32_t bits = i < w1 ? gbits[i] : 0u;
-    const uint32_t key = bits & 0x7FFFFFFFu;
-    const bool gt = i < w1 && key > r.T;
-    const bool eq = i < w1 && key == r.T;
-    const unsigned bg = __ballot_sync(kFull, gt), bq = __ballot_sync(kFull, eq);
-    const uint32_t gt_before = run_gt + __popc(bg & lm);
-    const uint32_t eq_before = run_eq + __popc(bq & lm);
-    if (gt || (eq && eq_before < r.need)) {
-      const int64_t pos = sg.out_off + gt_before + min(eq_before, r.need);
-      emit_one(io, sg.off + i, i, pos, sg.out_off + sg.k, __uint_as_float(bits), true);
+  for (int64_t b = w0; b < w1; b += kRound) {
+    uint32_t v[8];
+    int64_t loc[8];  // every entry's location is loaded with its bits, before any is used
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = b + u * 32 + lane;
+      v[u] = j < w1 ? bits_at(j) : 0u;
+      loc[u] = j < w1 ? loc_at(j) : 0;
     }
-    run_gt += __popc(bg);
-    run_eq += __popc(bq);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = b + u * 32 + lane;
+      const uint32_t key = v[u] & 0x7FFFFFFFu;
+      const bool gt = j < w1 && key > T;
+      const bool eq = j < w1 && key == T;
+      const unsigned bg = __ballot_sync(kFull, gt), bq = __ballot_sync(kFull, eq);
+      const uint32_t gt_before = run_gt + __popc(bg & lm);
+      const uint32_t eq_before = run_eq + __popc(bq & lm);
+      if (gt || (eq && eq_before < need)) {
+        const int64_t pos = out_off + gt_before + min(eq_before, need);
+        emit_one(io, seg_off + loc[u], loc[u], pos, out_off + k, __uint_as_float(v[u]),
+                 !on_list);
+      } else if (on_list && j < w1) {
+        io.e[seg_off + loc[u]] = __uint_as_float(v[u]);
+      }
+      run_gt += __popc(bg);
+      run_eq += __popc(bq);
+    }
   }
+}
+
+// ---------------------------------------------------------------------------
+// small segments: one CTA holds the whole segment
+// ---------------------------------------------------------------------------
+
+// One segment of at most kSmallMax elements by one CTA of kSmallThreads:
+// g = g_raw + e into e and into shared memory, radix select there, ordered
+// emit.  `sm` holds keys_words + 2048 + 64 words of shared memory.
+__device__ __forceinline__ void small_segment(const SmallSeg& sg, const IO& io, uint32_t* sm,
+                                              int keys_words) {
+  uint32_t* gbits = sm;
+  uint32_t* hist = sm + keys_words;
+  uint32_t* scratch = hist + 2048;
+  const int len = sg.len;
+  const float* gr = io.g_raw + sg.off;
+  float* e = io.e + sg.off;
+  // eight elements of each array in flight per thread
+  for (int i0 = threadIdx.x; i0 < len; i0 += 8 * blockDim.x) {
+    float gv[8], ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      gv[u] = i < len ? gr[i] : 0.0f;
+      ev[u] = i < len ? e[i] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < len) {
+        const float x = __fadd_rn(gv[u], ev[u]);
+        e[i] = x;
+        gbits[i] = __float_as_uint(x);
+      }
+    }
+  }
+  __syncthreads();
+  if (sg.k == 0) return;  // uniform across the CTA
+  const SelectResult r = block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch);
+  block_ordered_emit(io, len, r.T, r.need, sg.off, sg.out_off, sg.k, false, scratch,
+                     [gbits](int64_t i) { return gbits[i]; },
+                     [](int64_t i) { return i; });
+}
+
+__global__ void __launch_bounds__(kSmallThreads)
+topk_small(SmallBatch b, IO io, int keys_words) {
+  pdl_wait();
+  extern __shared__ uint32_t sm[];
+  small_segment(b.seg[blockIdx.x], io, sm, keys_words);
 }
 
 // ---------------------------------------------------------------------------
@@ -284,6 +343,12 @@ topk_small(SmallBatch b, IO io, int keys_words) {
 constexpr int kSampleCtasMax = 128;  // CTAs per segment in each sampling pass, at most
 constexpr int kSampleThreads = 256;
 constexpr int kSampleUnroll = 4;     // sample blocks per warp in flight
+// The sampled lower threshold T_lo is the lower edge of a bin of the top 13
+// key bits (8 exponent + 5 mantissa bits): a bin spans at most 1/32 of its
+// value, so T_lo sits at most that far below the sampled rank's key.
+constexpr int kSampleBits = 13;
+constexpr int kSampleShift = 31 - kSampleBits;
+constexpr int kSampleBins = 1 << kSampleBits;
 
 // Compensated keys of sample blocks `bi` .. of this warp: lane l holds
 // elements l and l + 32 of each block.
@@ -331,62 +396,6 @@ __device__ __forceinline__ int sample_seg(const SampleGrid& g, int nseg, int blk
   return lo;
 }
 
-// Sampling pass 1: histogram of the top 11 key bits over all sample blocks
-// of each streaming segment (the segment's CTAs of `grid`, merged in global
-// memory); the CTA that merges last finds the bin b0 holding the rank-th
-// largest sampled key and the rank r1 left inside it.
-__global__ void __launch_bounds__(kSampleThreads)
-topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ uint32_t sh[2048];
-  __shared__ uint32_t scratch[64];
-  __shared__ int s_last;
-  int q, ctas;
-  const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
-  const LargeSeg& d = b.seg[s];
-  const int64_t nblk = sample_blocks(d.len);
-  if (!samples_needed(d, nblk)) return;  // uniform across the CTA
-  const unsigned lane = lane_id();
-  const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
-  const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  for (int64_t b0 = gw; b0 < nblk; b0 += kWarps * kSampleUnroll) {
-    uint32_t key[kSampleUnroll][2];
-    bool ok[kSampleUnroll];
-    sample_keys(io, d, nblk, b0, kWarps, lane, key, ok);
-#pragma unroll
-    for (int u = 0; u < kSampleUnroll; ++u) {
-      if (ok[u]) {
-        atomicAdd(&sh[key[u][0] >> 20], 1u);
-        atomicAdd(&sh[key[u][1] >> 20], 1u);
-      }
-    }
-  }
-  __syncthreads();
-  uint32_t* gh = hist0 + (int64_t)s * 2048;
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
-    if (sh[i]) atomicAdd(&gh[i], sh[i]);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(&ss[s].done[0], 1u) == (uint32_t)ctas - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < 2048; i += blockDim.x)
-    sh[i] = *reinterpret_cast<volatile uint32_t*>(&gh[i]);
-  __syncthreads();
-  uint32_t bin, above;
-  block_find_bin(sh, 2048, (uint32_t)d.rank, scratch, &bin, &above);
-  if (threadIdx.x == 0) {
-    ss[s].b0 = bin;
-    ss[s].r1 = (uint32_t)d.rank - above;
-  }
-}
-
 __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& d, uint32_t t_lo) {
   SegState v;
   v.d = d;
@@ -404,61 +413,63 @@ __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& 
   st[s] = v;
 }
 
-// Sampling pass 2: histogram of the next 10 key bits of the sampled keys in
-// bin b0; the CTA that merges last sets T_lo = the lower edge of the 21-bit
-// bin holding the rank-th largest sampled key (so at least `rank` sampled
-// keys are >= T_lo) and the segment's state for the later passes.
+// The sampling pass: a histogram of the top kSampleBits key bits over all
+// sample blocks of each streaming segment (the segment's CTAs of `grid`,
+// merged in global memory).  The CTA that merges last sets T_lo = the lower
+// edge of the bin holding the rank-th largest sampled key (so at least
+// `rank` sampled keys are >= T_lo) and the segment's state for the later
+// passes.  A segment that does not sample gets its state from its one CTA.
 __global__ void __launch_bounds__(kSampleThreads)
-topk_prepare(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist1, SampleState* ss,
-             SegState* st) {
+topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss,
+            SegState* st) {
   pdl_wait();
-  __shared__ uint32_t sh[1024];
+  __shared__ uint32_t sh[kSampleBins];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
   int q, ctas;
   const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
   const LargeSeg d = b.seg[s];
   const int64_t nblk = sample_blocks(d.len);
-  if (!samples_needed(d, nblk)) {
+  if (!samples_needed(d, nblk)) {  // uniform across the CTA
     if (q == 0 && threadIdx.x == 0) init_state(st, s, d, d.rank <= 0 ? kNoCandidate : 0u);
     return;
   }
-  const uint32_t b0 = *reinterpret_cast<volatile uint32_t*>(&ss[s].b0);
   const unsigned lane = lane_id();
   const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
   const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x) sh[i] = 0;
+  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  for (int64_t bb = gw; bb < nblk; bb += kWarps * kSampleUnroll) {
+  for (int64_t b0 = gw; b0 < nblk; b0 += kWarps * kSampleUnroll) {  // warp-uniform
     uint32_t key[kSampleUnroll][2];
     bool ok[kSampleUnroll];
-    sample_keys(io, d, nblk, bb, kWarps, lane, key, ok);
+    sample_keys(io, d, nblk, b0, kWarps, lane, key, ok);
 #pragma unroll
     for (int u = 0; u < kSampleUnroll; ++u) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (ok[u] && (key[u][h] >> 20) == b0) atomicAdd(&sh[(key[u][h] >> 10) & 1023u], 1u);
+      hist_add(sh, key[u][0] >> kSampleShift, ok[u]);
+      hist_add(sh, key[u][1] >> kSampleShift, ok[u]);
     }
   }
   __syncthreads();
-  uint32_t* gh = hist1 + (int64_t)s * 1024;
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+  uint32_t* gh = hist0 + (int64_t)s * kSampleBins;
+  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x)
     if (sh[i]) atomicAdd(&gh[i], sh[i]);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(&ss[s].done[1], 1u) == (uint32_t)ctas - 1;
+    s_last = atomicAdd(&ss[s].done, 1u) == (uint32_t)ctas - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x)
     sh[i] = *reinterpret_cast<volatile uint32_t*>(&gh[i]);
   __syncthreads();
   uint32_t bin, above;
-  block_find_bin(sh, 1024, *reinterpret_cast<volatile uint32_t*>(&ss[s].r1), scratch, &bin,
-                 &above);
-  if (threadIdx.x == 0) init_state(st, s, d, (b0 << 20) | (bin << 10));
+  block_find_bin(sh, kSampleBins, (uint32_t)d.rank, scratch, &bin, &above);
+  // T_lo >= 1: zeros are never candidates (a mostly-zero segment then lists
+  // its nonzeros instead of overflowing; with fewer than k of them the
+  // whole-segment select takes over as for any T_lo above the k-th key)
+  if (threadIdx.x == 0) init_state(st, s, d, max(bin << kSampleShift, 1u));
 }
 
 __device__ __forceinline__ int find_seg(const int64_t* base, int nseg, int64_t x) {
@@ -848,8 +859,8 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
     for (int r = 0; r < kPer; ++r) {
       const int64_t j = j0 + r * kSelThreads + threadIdx.x;
       const uint32_t key = bits[r] & 0x7FFFFFFFu;
-      if (j < j1 && (hi >= 31 || (key >> hi) == (prefix >> hi)))
-        atomicAdd(&sh[(key >> shift) & (nb - 1)], 1u);
+      hist_add(sh, (key >> shift) & (nb - 1),
+                    j < j1 && (hi >= 31 || (key >> hi) == (prefix >> hi)));
     }
     __syncthreads();
     for (int b = threadIdx.x; b < nb; b += blockDim.x) {
@@ -999,25 +1010,92 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
   }
 }
 
+// The last kernel of a compact batch, whose every streaming segment has a
+// candidate list that fits one CTA's shared memory (capacity kFinishCap):
+// blocks [0, nlarge) finish one such segment each -- select on the list and
+// ordered emit, both in shared memory -- and blocks [nlarge, gridDim.x) each
+// run one small segment folded into this launch.  A segment whose fused pass
+// fell back to the whole segment (list incomplete or T_lo above the k-th
+// key) is finished by its CTA from global memory: g goes back into e at the
+// staged candidates, then the radix select and the emit read e directly.
+// That path exists for correctness only; a compact segment is at most
+// kCompactLen elements long.
+__global__ void __launch_bounds__(kSmallThreads)
+topk_finish(SmallBatch sb, int nlarge, IO io, const SegState* st, const uint2* cand,
+            int keys_words) {
+  pdl_wait();
+  extern __shared__ uint32_t sm[];
+  if ((int)blockIdx.x >= nlarge) {
+    small_segment(sb.seg[blockIdx.x - nlarge], io, sm, keys_words);
+    return;
+  }
+  const int s = blockIdx.x;
+  const LargeSeg d = st[s].d;
+  const uint32_t mode = st[s].mode;
+  const int64_t len = st[s].list_len;
+  if (d.k == 0 || len == 0) return;  // uniform across the CTA
+  uint32_t* keys = sm;
+  uint32_t* hist = sm + keys_words;
+  uint32_t* scratch = hist + 2048;
+  const uint2* cl = cand + d.cand_base;
+  float* es = io.e + d.off;
+  if (mode == 0) {
+    // the candidate list: k <= len <= cap <= kFinishCap entries, eight loads
+    // in flight per thread
+    for (int j0 = 0; j0 < (int)len; j0 += 8 * kSmallThreads) {
+      uint32_t y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
+        y[u] = j < (int)len ? cl[j].y : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
+        if (j < (int)len) keys[j] = y[u];
+      }
+    }
+    __syncthreads();
+    const SelectResult r = block_radix_select(keys, (int)len, (uint32_t)d.k, hist, scratch);
+    block_ordered_emit(io, len, r.T, r.need, d.off, d.out_off, d.k, true, scratch,
+                       [keys](int64_t j) { return keys[j]; },
+                       [cl](int64_t j) { return (int64_t)cl[j].x; });
+    return;
+  }
+  const int64_t c = st[s].cand_count;  // <= 0: no candidates, or a reported error
+  const int64_t m = c > 0 ? min(c, d.cap) : 0;
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const uint2 v = cl[j];
+    if (v.x != kNoEntry && (int64_t)v.x < d.len) es[v.x] = __uint_as_float(v.y);
+  }
+  __syncthreads();  // the block's writes to e are visible to the block after this
+  const SelectResult r = block_radix_select_at(
+      d.len, (uint32_t)d.k, hist, scratch, [es](int64_t i) { return __float_as_uint(es[i]); });
+  block_ordered_emit(io, d.len, r.T, r.need, d.off, d.out_off, d.k, false, scratch,
+                     [es](int64_t i) { return __float_as_uint(es[i]); },
+                     [](int64_t i) { return i; });
+}
+
 // ---------------------------------------------------------------------------
 // host planning
 // ---------------------------------------------------------------------------
 
 struct Batch {
   std::vector<LargeSeg> segs;
+  bool compact = false;    // finished by topk_finish (see kCompactLen)
   int64_t max_tiles = 0;   // upper bound over address phases
   int64_t max_chunks = 0;  // every list at its longest (whole segment)
   int64_t cand_total = 0;
 };
 
 struct Plan {
-  std::vector<SmallSeg> small;
-  int small_max_len = 0;
+  std::vector<SmallSeg> small;  // longest first
   std::vector<Batch> batches;
+  size_t small_folded = 0;  // small segments run by the first compact batch's topk_finish
   int64_t total_k = 0;
   // workspace regions (byte offsets); batches reuse the same regions
-  size_t off_ctl = 0, off_st = 0, off_hist = 0, off_tiles = 0, off_chunks = 0, off_cand = 0;
-  size_t off_hist0 = 0, off_hist1 = 0, off_sstate = 0;
+  size_t off_ctl = 0, off_st = 0, off_sstate = 0, off_hist0 = 0, off_hist = 0;
+  size_t off_tiles = 0, off_chunks = 0, off_cand = 0;
   size_t ctl_clear_bytes = 0;  // bytes cleared from off_ctl before each batch
   size_t bytes = 0;
 };
@@ -1033,6 +1111,16 @@ int64_t sample_rank(int64_t k, int64_t len) {
   return r > (double)S ? S + 1 : (int64_t)r;
 }
 
+// Whether a streaming segment goes to a compact batch: its candidate list,
+// expected at about rank * len / S entries, fills at most half of kFinishCap.
+bool compact_segment(int64_t len, int64_t rank) {
+  if (len > kCompactLen) return false;
+  if (rank <= 0) return true;
+  const int64_t S = sample_blocks(len) * kSampleBlock;
+  if (rank > S) return false;
+  return (double)rank * (double)len / (double)S <= 0.5 * kFinishCap;
+}
+
 ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t* ks,
                     int32_t idx_format, Plan* p) {
   if (n < 0) return EF_ERR_SIZE;
@@ -1042,7 +1130,8 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
   if (idx_format == EF_IDX_INT32 && n > (int64_t(1) << 31)) return EF_ERR_SIZE;
   if (offs[0] != 0 || offs[nseg] != n) return EF_ERR_SEGMENTS;
   int64_t out_off = 0;
-  Batch cur;
+  Batch cur[2];  // [0]: general, [1]: compact
+  cur[1].compact = true;
   for (int32_t s = 0; s < nseg; ++s) {
     const int64_t a = offs[s], b = offs[s + 1];
     if (b < a) return EF_ERR_SEGMENTS;
@@ -1053,51 +1142,63 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     if (len == 0) continue;
     if (len <= kSmallMax) {
       p->small.push_back(SmallSeg{a, out_off, (int32_t)len, (int32_t)k});
-      p->small_max_len = std::max<int>(p->small_max_len, (int)len);
     } else {
       LargeSeg d{};
       d.off = a;
       d.len = len;
       d.k = k;
       d.out_off = out_off;
-      d.cap = std::min<int64_t>(len, 4 * k + 65536);
-      d.cand_base = cur.cand_total;
       d.rank = sample_rank(k, len);
-      cur.cand_total += d.cap;
-      cur.max_tiles += (len + kTileSmall - 1) / kTileSmall + 1;  // either tile size
-      cur.max_chunks += (len + kChunk - 1) / kChunk;
-      cur.segs.push_back(d);
-      if ((int)cur.segs.size() == kMaxLarge) {
-        p->batches.push_back(cur);
-        cur = Batch();
+      const bool compact = compact_segment(len, d.rank);
+      Batch& c = cur[compact ? 1 : 0];
+      d.cap = compact ? std::min<int64_t>(len, kFinishCap) : std::min<int64_t>(len, 4 * k + 65536);
+      d.cand_base = c.cand_total;
+      c.cand_total += d.cap;
+      c.max_tiles += (len + kTileSmall - 1) / kTileSmall + 1;  // either tile size
+      c.max_chunks += (len + kChunk - 1) / kChunk;
+      c.segs.push_back(d);
+      if ((int)c.segs.size() == kMaxLarge) {
+        p->batches.push_back(c);
+        c = Batch();
+        c.compact = compact;
       }
     }
     out_off += k;
   }
-  if (!cur.segs.empty()) p->batches.push_back(cur);
+  // compact batches first: the first one also runs the longest small segments
+  for (int i = 1; i >= 0; --i)
+    if (!cur[i].segs.empty()) p->batches.push_back(cur[i]);
+  std::stable_partition(p->batches.begin(), p->batches.end(),
+                        [](const Batch& b) { return b.compact; });
+  std::stable_sort(p->small.begin(), p->small.end(),
+                   [](const SmallSeg& x, const SmallSeg& y) { return x.len > y.len; });
+  if (!p->batches.empty() && p->batches[0].compact)
+    p->small_folded = std::min<size_t>(p->small.size(), kMaxSmall);
   p->total_k = out_off;
 
   int64_t tiles = 0, chunks = 0, cands = 0, segs = 0;
+  bool general = false;
   for (const Batch& b : p->batches) {
     segs = std::max(segs, (int64_t)b.segs.size());
     tiles = std::max(tiles, b.max_tiles);
-    chunks = std::max(chunks, b.max_chunks);
     cands = std::max(cands, b.cand_total);
+    if (!b.compact) {
+      general = true;
+      chunks = std::max(chunks, b.max_chunks);
+    }
   }
   size_t off = sizeof(WsHeader);
   if (!p->batches.empty()) {
     p->off_ctl = off;
     off += sizeof(Ctl);
     p->off_st = off;
-    off = round_up(off + sizeof(SegState) * kMaxLarge, 256);
-    p->off_hist = off;
-    off = round_up(off + (size_t)kMaxLarge * 2048 * 4, 256);
-    p->off_hist0 = off;
-    off = round_up(off + (size_t)kMaxLarge * 2048 * 4, 256);
-    p->off_hist1 = off;
-    off = round_up(off + (size_t)kMaxLarge * 1024 * 4, 256);
+    off = round_up(off + sizeof(SegState) * segs, 256);
     p->off_sstate = off;
-    off = round_up(off + sizeof(SampleState) * kMaxLarge, 256);
+    off = round_up(off + sizeof(SampleState) * segs, 256);
+    p->off_hist0 = off;
+    off = round_up(off + (size_t)segs * kSampleBins * 4, 256);
+    p->off_hist = off;
+    if (general) off = round_up(off + (size_t)segs * 2048 * 4, 256);
     p->off_tiles = off;
     off = round_up(off + (size_t)tiles * 8, 256);
     p->off_chunks = off;
@@ -1122,7 +1223,10 @@ ef_status set_attributes(int dev) {
     const int sel_smem = (kSelSmall + 2048 + 64) * 4;
     cudaError_t e2 = cudaFuncSetAttribute(topk_select_small,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
-    cudaError_t bad = e1 != cudaSuccess ? e1 : e2;
+    cudaError_t e3 = cudaFuncSetAttribute(topk_finish,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          std::max(small_smem, sel_smem));
+    cudaError_t bad = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
     g_attr_status[dev] = bad == cudaSuccess ? EF_OK : cuda_fail(bad);
   });
   return g_attr_status[dev];
@@ -1207,8 +1311,8 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
   IO io{g_raw, e, out_values, bitmap ? nullptr : out_indices, bitmap ? out_bitmap : nullptr,
         reinterpret_cast<int32_t*>(ws), pos_out};
 
-  // small segments
-  for (size_t i0 = 0; i0 < p.small.size(); i0 += kMaxSmall) {
+  // small segments not folded into a compact batch's finish launch
+  for (size_t i0 = p.small_folded; i0 < p.small.size(); i0 += kMaxSmall) {
     const size_t cnt = std::min<size_t>(kMaxSmall, p.small.size() - i0);
     SmallBatch sb;
     int maxlen = 0;
@@ -1230,9 +1334,12 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
   Ctl* ctl = reinterpret_cast<Ctl*>(ws + p.off_ctl);
   SegState* sst = reinterpret_cast<SegState*>(ws + p.off_st);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(ws + p.off_hist);
+  uint32_t* hist0 = reinterpret_cast<uint32_t*>(ws + p.off_hist0);
+  SampleState* sstate = reinterpret_cast<SampleState*>(ws + p.off_sstate);
   uint64_t* tstate = reinterpret_cast<uint64_t*>(ws + p.off_tiles);
   uint64_t* cstate = reinterpret_cast<uint64_t*>(ws + p.off_chunks);
   uint2* cand = reinterpret_cast<uint2*>(ws + p.off_cand);
+  bool first_batch = true;
   for (Batch& b : p.batches) {
     LargeBatch lb;
     const int nsg = (int)b.segs.size();
@@ -1254,12 +1361,9 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     if (small_tiles) tiles = count_tiles(kTileSmall);
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
-    uint32_t* hist0 = reinterpret_cast<uint32_t*>(ws + p.off_hist0);
-    uint32_t* hist1 = reinterpret_cast<uint32_t*>(ws + p.off_hist1);
-    SampleState* sstate = reinterpret_cast<SampleState*>(ws + p.off_sstate);
     // sampling CTAs per segment: one round of sample loads per warp (32
     // blocks per CTA), at most kSampleCtasMax; one for a segment that
-    // does not sample (its prepare CTA sets the segment's state)
+    // does not sample (it sets the segment's state)
     SampleGrid sg;
     sg.base[0] = 0;
     for (int i = 0; i < nsg; ++i) {
@@ -1271,9 +1375,8 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
                             : 1;
       sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
     }
-    launch_pdl(topk_sample, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist0, sstate);
-    if ((st = check_launch()) != EF_OK) return st;
-    launch_pdl(topk_prepare, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist1, sstate, sst);
+    launch_pdl(topk_sample, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist0, sstate,
+               sst);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
@@ -1285,19 +1388,37 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
                  cand, ctl, phase, vec);
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
-    launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
-    if ((st = check_launch()) != EF_OK) return st;
-    launch_pdl(topk_select_small, nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s, io, sst,
-                                                                                      cand);
-    if ((st = check_launch()) != EF_OK) return st;
-    const int sgrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 3));
-    for (int pass = 0; pass < 3; ++pass) {
-      launch_pdl(topk_select, sgrid, kSelThreads, 0, s, io, sst, nsg, cand, ghist, ctl, pass);
+    if (b.compact) {
+      // one CTA per segment, plus the folded small segments (longest first)
+      SmallBatch sb;
+      const size_t nsmall = first_batch ? p.small_folded : 0;
+      int keys_words = kFinishCap;
+      for (size_t i = 0; i < nsmall; ++i) {
+        sb.seg[i] = p.small[i];
+        keys_words = std::max(keys_words, (p.small[i].len + 3) & ~3);
+      }
+      const size_t smem = (size_t)(keys_words + 2048 + 64) * 4;
+      launch_pdl(topk_finish, (unsigned)(nsg + nsmall), kSmallThreads, smem, s, sb, nsg, io, sst,
+                 cand, keys_words);
+      if ((st = check_launch()) != EF_OK) return st;
+    } else {
+      launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
+      if ((st = check_launch()) != EF_OK) return st;
+      launch_pdl(topk_select_small, nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s,
+                 io, sst, cand);
+      if ((st = check_launch()) != EF_OK) return st;
+      const int sgrid =
+          (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 3));
+      for (int pass = 0; pass < 3; ++pass) {
+        launch_pdl(topk_select, sgrid, kSelThreads, 0, s, io, sst, nsg, cand, ghist, ctl, pass);
+        if ((st = check_launch()) != EF_OK) return st;
+      }
+      const int egrid =
+          (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 4));
+      launch_pdl(topk_emit, egrid, kEmitThreads, 0, s, io, sst, nsg, cand, cstate, ctl);
       if ((st = check_launch()) != EF_OK) return st;
     }
-    const int egrid = (int)std::max<int64_t>(1, std::min<int64_t>(b.max_chunks, (int64_t)dev.sms * 4));
-    launch_pdl(topk_emit, egrid, kEmitThreads, 0, s, io, sst, nsg, cand, cstate, ctl);
-    if ((st = check_launch()) != EF_OK) return st;
+    first_batch = false;
   }
   return EF_OK;
 }
@@ -1366,4 +1487,18 @@ extern "C" ef_status ef_topk_compress_noalloc(const float* g_raw, float* e, int6
   return ef_topk_compress(g_raw, e, n, nseg, h_seg_offsets, h_seg_k, idx_format, out_values,
                           out_indices, out_bitmap, scratch, (size_t)EF_NOALLOC_SCRATCH_BYTES,
                           stream);
+}
+
+extern "C" ef_status ef_topk_noalloc_status(void* stream, int32_t* device_status) {
+  if (!device_status) return EF_ERR_NULL;
+  void* scratch = nullptr;
+  ef_status st = ef::noalloc_scratch(&scratch);
+  if (st != EF_OK) return st;
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return ef::cuda_fail(err);
+  int32_t v = 0;
+  err = cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return ef::cuda_fail(err);
+  *device_status = v;
+  return EF_OK;
 }

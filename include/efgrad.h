@@ -170,7 +170,12 @@ EF_API ef_status ef_topk_compress(const float* g_raw, float* e, int64_t n,
  *   overlap -- on different streams, or from different threads without
  *   ordering -- race on it; issue them on one stream.
  * - Device-side conditions (EF_ERR_DEVICE_TIMEOUT, EF_ERR_INTERNAL) land in
- *   the library's array and are not reported by this entry point.
+ *   the status word at the start of the library's array; read them with
+ *   ef_topk_noalloc_status() (which synchronises `stream`), before the next
+ *   call on that device resets the word.
+ * - The array's address is cached per device for the life of the process:
+ *   after cudaDeviceReset() on a device, do not call this entry point (or
+ *   its status query) on that device again in the same process.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.
  * ---------------------------------------------------------------------- */
@@ -180,6 +185,11 @@ EF_API ef_status ef_topk_compress_noalloc(const float* g_raw, float* e, int64_t 
                                           const int64_t* h_seg_k, int32_t idx_format,
                                           float* out_values, int32_t* out_indices,
                                           uint32_t* out_bitmap, void* stream);
+/* Device-side status word of the last ef_topk_compress_noalloc call on the
+ * current device: synchronises `stream`, then copies the word (EF_OK,
+ * EF_ERR_DEVICE_TIMEOUT or EF_ERR_INTERNAL) to *device_status.  Allocates
+ * nothing. */
+EF_API ef_status ef_topk_noalloc_status(void* stream, int32_t* device_status);
 
 /* ------------------------------------------------------------------------
  * Top-k error feedback with 8-bit packet values.
@@ -377,6 +387,36 @@ EF_API ef_status sparse_aggregate_apply(int32_t W, int32_t idx_format,
                                  const int64_t* h_k, int64_t n, float eta,
                                  float* G, float* w, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Packet exchange between data-parallel ranks, index-range form.
+ *
+ * [SPARSE] §详细算法流程 step 5 and §与Allreduce的融合: the workers' sparse
+ * packets are exchanged with collectives and summed by the receivers.  In
+ * the index-range form rank q owns the indices [b_q, b_{q+1}): every rank
+ * sends each owner the slice of its ascending packet that falls in the
+ * owner's range, and each owner runs sparse_aggregate_apply on its range
+ * alone with the slices rebased to it.  These two calls are the device
+ * steps of that exchange (the collectives themselves are the caller's).
+ *
+ * ef_packet_split  d_starts[q] = number of entries j < k with
+ *                  indices[j] < h_bounds[q], for q = 0 .. nparts: in an
+ *                  ascending packet, the slice for range q is
+ *                  [d_starts[q], d_starts[q+1]).
+ *   indices   [k] int32 (device, 4-byte aligned), 0 <= k <= 2^31.
+ *   nparts    1 .. 1024 ranges; h_bounds [nparts + 1] host int64,
+ *             non-decreasing (EF_ERR_SEGMENTS otherwise).
+ *   d_starts  [nparts + 1] int64 (device, 8-byte aligned), must not overlap
+ *             indices.
+ *   Reads only indices[0 .. k); an unsorted packet gives positions in
+ *   [0, k] that the receive side then reports as malformed.
+ * ef_index_rebase  indices[j] = indices[j] - base for j < count, in place
+ *                  (0 <= count <= 2^31, 0 <= base <= 2^31).
+ * ---------------------------------------------------------------------- */
+EF_API ef_status ef_packet_split(const int32_t* indices, int64_t k, int32_t nparts,
+                                 const int64_t* h_bounds, int64_t* d_starts, void* stream);
+EF_API ef_status ef_index_rebase(int32_t* indices, int64_t count, int64_t base,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------
  * Receive side for 1-bit packets.

@@ -19,6 +19,7 @@ from .ef_oracle import (  # noqa: F401
     onebit_momentum,
     pack_bits,
     packet_indices,
+    packet_split,
     philox4x32_10,
     q8_dequantize,
     q8_quantize,

@@ -611,6 +611,20 @@ def sparse_aggregate(packets, n: int) -> np.ndarray:
     return G
 
 
+def packet_split(indices, bounds) -> np.ndarray:
+    """Slice bounds of a packet for index ranges: starts[q] = the number of
+    entries whose index is below bounds[q].
+
+    [SPARSE] §详细算法流程 step 5 and §与Allreduce的融合 exchange the packets
+    between workers; in the index-range form each receiver gets the entries
+    of its own index range, which in an ascending packet are the entries
+    [starts[q], starts[q + 1]).  Written as the count it is, one bound at a
+    time.
+    """
+    idx = np.asarray(indices, dtype=np.int64)
+    return np.array([int(np.count_nonzero(idx < int(b))) for b in bounds], dtype=np.int64)
+
+
 def sign_aggregate(bit_vectors, n: int) -> np.ndarray:
     """Step 6 for 1-bit packets: G = sum over workers of the decoded +-1 signs,
     added in worker order (exact: small integers)."""

@@ -277,3 +277,28 @@ def test_q8_rejects_before_device(lib):
     assert lib.ef_q8_dequantize(None, sc, 1, _i64([4]), vals, None) == d["EF_ERR_NULL"]
     assert lib.ef_q8_dequantize(q, ctypes.c_void_p((4 << 20) + 1), 1, _i64([4]), vals,
                                 None) == d["EF_ERR_ALIGN"]
+
+
+def test_exchange_steps_reject_before_device(lib):
+    d = _header_defines()
+    idx, starts = ctypes.c_void_p(4096), ctypes.c_void_p(1 << 20)
+    split = lib.ef_packet_split
+    assert split(idx, -1, 2, _i64([0, 5, 9]), starts, None) == d["EF_ERR_SIZE"]
+    assert split(idx, (1 << 31) + 1, 2, _i64([0, 5, 9]), starts, None) == d["EF_ERR_SIZE"]
+    assert split(idx, 10, 0, _i64([0]), starts, None) == d["EF_ERR_ARG"]
+    assert split(idx, 10, 1025, _i64(range(1026)), starts, None) == d["EF_ERR_ARG"]
+    assert split(idx, 10, 2, _i64([0, 9, 5]), starts, None) == d["EF_ERR_SEGMENTS"]
+    assert split(None, 10, 2, _i64([0, 5, 9]), starts, None) == d["EF_ERR_NULL"]
+    assert split(idx, 10, 2, None, starts, None) == d["EF_ERR_NULL"]
+    assert split(idx, 10, 2, _i64([0, 5, 9]), None, None) == d["EF_ERR_NULL"]
+    assert split(ctypes.c_void_p(4098), 10, 2, _i64([0, 5, 9]), starts, None) == d["EF_ERR_ALIGN"]
+    assert split(idx, 10, 2, _i64([0, 5, 9]), ctypes.c_void_p((1 << 20) + 4),
+                 None) == d["EF_ERR_ALIGN"]
+    assert split(idx, 10, 2, _i64([0, 5, 9]), ctypes.c_void_p(4096 + 16),
+                 None) == d["EF_ERR_ALIAS"]
+    rebase = lib.ef_index_rebase
+    assert rebase(idx, -1, 0, None) == d["EF_ERR_SIZE"]
+    assert rebase(idx, 10, -1, None) == d["EF_ERR_ARG"]
+    assert rebase(None, 10, 0, None) == d["EF_ERR_NULL"]
+    assert rebase(ctypes.c_void_p(4098), 10, 0, None) == d["EF_ERR_ALIGN"]
+    assert rebase(None, 0, 5, None) == d["EF_OK"]                     # empty: no work

@@ -4,9 +4,10 @@ separate buffers on one GPU).
 
 Steps run in lockstep: each GPU step and the oracle step get the same inputs;
 after a step both continue from the oracle's state, so a difference cannot
-cascade.  The 2^31 slab is checked on one worker in full (top-k, both index
-formats) and elsewhere on sampled positions (1-bit path) and with packets
-drawn by the input generator (receive side).
+cascade.  Every output is compared in full, at every element, including the
+2^31-element slab; the oracle's elementwise work at that size and the eight
+BERT-large workers' steps run in a pool of host processes
+(``oracle_pool``), in pieces whose results are the whole arrays'.
 """
 
 import numpy as np
@@ -17,6 +18,7 @@ import error_feedback_gradient_gb300 as efg
 from error_feedback_gradient_gb300 import workloads as wl
 from efcheck import assert_bits_equal, assert_close, check_topk_step, gpu_topk, host
 import oracle
+import oracle_pool
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -85,26 +87,40 @@ def test_resnet50_layerwise_three_steps(fmt):
         e.copy_(torch.from_numpy(want["e"]))
 
 
-def test_bert_large_eight_workers_one_step():
+def test_bert_large_eight_workers_three_steps():
+    """The configuration as stated: eight workers, each with its own
+    Laplace(0, 1e-4) gradient per step and its own residual from e0 = 0,
+    three chained steps of top-0.1 % over the flat 335,141,888-element
+    vector, each followed by the sum of the eight packets and SGD."""
     w = wl.workload("bert_large")
+    W, n = w.workers, w.n
     wt = w.weights(DEV)
-    w_before = host(wt)
-    packets, wants = [], []
-    for k in range(w.workers):
-        g = w.gradient(k, 1, DEV)
-        e = wl.laplace(w.n, 1e-4, wl.seed(4, k, 0), DEV)        # a carried residual
-        want, out = check_topk_step(g, e, w.seg_offsets, w.seg_k)
-        packets.append(out)
-        wants.append({"indices": want["indices"], "values": want["values"]})
-        del g, e, want
-    G = _apply(packets, [w.total_k] * w.workers, w.n, w.eta, wt)
-    G_want = oracle.sparse_aggregate(wants, w.n)
-    w_want = oracle.sgd_apply(w_before, G_want, w.eta)
-    torch.cuda.synchronize()
-    assert_close(G, G_want, "G")
-    assert_bits_equal(G, G_want, "G (bitwise)")
-    assert_close(wt, w_want, "w")
-    assert_bits_equal(wt, w_want, "w (bitwise)")
+    es = [torch.zeros(n, device=DEV) for _ in range(W)]
+    with oracle_pool.pool(W) as p:
+        for step in range(1, w.steps + 1):
+            gs = [w.gradient(k, step, DEV) for k in range(W)]
+            g_np, e_np = [host(g) for g in gs], [host(e) for e in es]
+            w_before = host(wt)
+            outs = [gpu_topk(g, e, w.seg_offsets, w.seg_k) for g, e in zip(gs, es)]
+            G = _apply(outs, [w.total_k] * W, n, w.eta, wt)
+            wants = oracle_pool.topk_ef_steps(p, g_np, e_np, w.seg_offsets, w.seg_k)
+            del g_np, e_np
+            torch.cuda.synchronize()
+            for k, (out, want) in enumerate(zip(outs, wants)):
+                assert efg.workspace_status(out["ws"]) == 0
+                assert_bits_equal(out["indices"], want["indices"], f"indices w{k} s{step}")
+                assert_bits_equal(out["values"], want["values"], f"values w{k} s{step}")
+                assert_bits_equal(es[k], want["e"], f"residual w{k} s{step}")
+            G_want = oracle.sparse_aggregate(wants, n)
+            w_want = oracle.sgd_apply(w_before, G_want, w.eta)
+            assert_close(G, G_want, f"G s{step}")
+            assert_bits_equal(G, G_want, f"G (bitwise) s{step}")
+            assert_close(wt, w_want, f"w s{step}")
+            assert_bits_equal(wt, w_want, f"w (bitwise) s{step}")
+            for k in range(W):       # lockstep: continue from the oracle's state
+                es[k].copy_(torch.from_numpy(wants[k]["e"]))
+            wt.copy_(torch.from_numpy(w_want))
+            del outs, wants, gs, G, G_want, w_want
 
 
 def test_slab_2p31_topk_one_worker_in_full():
@@ -248,32 +264,32 @@ def test_slab_2p31_random_sparsification_sampled():
     assert abs(total - pv.sum()) < 6 * np.sqrt(np.sum(pv * (1 - pv)))
 
 
-def test_slab_2p31_sign_sampled():
+def test_slab_2p31_sign_two_steps_in_full():
+    """1-bit error feedback on one worker's 2^31-element slab from eps0 = 0,
+    two chained steps; the bits and eps are compared at every element."""
     w = wl.workload("slab_2p31")
     n = w.n
-    g = w.gradient(1, 1, DEV)
-    eps = wl.normal(n, 0.05, wl.seed(5, 1, 0), DEV)
-    rng = np.random.default_rng(3)
-    pos = np.unique(rng.integers(0, n, 1 << 20))
-    pos = np.concatenate([pos, [0, 1, 31, 32, n - 33, n - 1]])
-    pos = np.unique(pos)
-    pt = torch.from_numpy(pos).to(DEV)
-    g_s, e_s = host(g[pt]), host(eps[pt])
+    eps = torch.zeros(n, device=DEV)
     bits = torch.empty((n + 31) // 32, dtype=torch.int32, device=DEV)
-    efg.sign_compress(g, eps, w.beta1, bits)
-    bits_want, eps_want = oracle.sign_ef_step(g_s, e_s, w.beta1)
-    torch.cuda.synchronize()
-    words = host(bits[torch.from_numpy(pos // 32).to(DEV)]).view(np.uint32)
-    got_bit = ((words >> (pos % 32).astype(np.uint32)) & 1).astype(bool)
-    assert np.array_equal(got_bit, oracle.unpack_bits(bits_want, pos.size))
-    assert_bits_equal(eps[pt], eps_want, "eps (sampled)")
-    del g, eps, bits
+    with oracle_pool.pool() as p:
+        for step in (1, 2):
+            g = w.gradient(1, step, DEV)
+            g_np, e_np = host(g), host(eps)
+            efg.sign_compress(g, eps, w.beta1, bits)
+            del g
+            bits_want, eps_want = oracle_pool.sign_ef_step(p, g_np, e_np, w.beta1)
+            del g_np, e_np
+            torch.cuda.synchronize()
+            assert_bits_equal(bits, bits_want, f"bits step {step}")
+            assert_bits_equal(eps, eps_want, f"eps step {step}")
+            eps.copy_(torch.from_numpy(eps_want))
+            del bits_want, eps_want
 
 
-def test_slab_2p31_sign_receive_sampled():
+def test_slab_2p31_sign_receive_in_full():
     """Four workers' 1-bit packets over 2^31 elements (drawn by the input
-    generator as random words), summed and applied with SGD; checked at
-    sampled positions, including both ends of the slab."""
+    generator as random words), summed and applied with SGD; G and w are
+    compared at every element."""
     w = wl.workload("slab_2p31")
     n = w.n
     nw = (n + 31) // 32
@@ -281,23 +297,19 @@ def test_slab_2p31_sign_receive_sampled():
     gen.manual_seed(wl.seed(5, 9, 9))
     bit_list = [torch.randint(-2**31, 2**31 - 1, (nw,), dtype=torch.int32, device=DEV,
                               generator=gen) for _ in range(w.workers)]
-    rng = np.random.default_rng(4)
-    pos = np.unique(np.concatenate([rng.integers(0, n, 1 << 20), [0, 1, 31, 32, n - 1]]))
-    pt = torch.from_numpy(pos).to(DEV)
-    wsel = torch.from_numpy(pos // 32).to(DEV)
-    # the sampled bits of every packet, as the oracle's packet of the samples
-    sub_bits = []
-    for b in bit_list:
-        wd = host(b[wsel]).view(np.uint32)
-        sub_bits.append(oracle.pack_bits(((wd >> (pos % 32).astype(np.uint32)) & 1).astype(bool)))
     wt = w.weights(DEV)
-    w_s = host(wt[pt])
+    w_np = host(wt)
     G = torch.empty(n, device=DEV)
     efg.sign_aggregate_apply(bit_list, n, efg.APPLY_SGD, w.eta, w.beta1, G, wt)
-    G_want = oracle.sign_aggregate(sub_bits, pos.size)
+    bits_np = [host(b).view(np.uint32) for b in bit_list]
+    del bit_list
+    with oracle_pool.pool() as p:
+        G_want, w_want = oracle_pool.sign_aggregate_sgd(p, bits_np, n, w_np, w.eta)
+    del bits_np, w_np
     torch.cuda.synchronize()
-    assert_bits_equal(G[pt], G_want, "G (sampled)")
-    assert_bits_equal(wt[pt], oracle.sgd_apply(w_s, G_want, w.eta), "w (sampled)")
+    assert_bits_equal(G, G_want, "G")
+    del G, G_want
+    assert_bits_equal(wt, w_want, "w")
 
 
 @pytest.mark.parametrize("fmt", [efg.IDX_INT32, efg.IDX_BITMAP])
@@ -305,8 +317,7 @@ def test_slab_2p31_receive_side_four_workers(fmt):
     """W = 4 packets of 2,147,484 entries each (drawn by the input generator:
     sorted random positions, Student-t values, overlapping between workers),
     as indices or as bitmaps, summed into a dense G over 2^31 elements and
-    applied with SGD; G and w are compared at every touched position and at
-    random untouched ones."""
+    applied with SGD; G and w are compared at every element."""
     w = wl.workload("slab_2p31")
     n, k = w.n, w.total_k
     rng = np.random.default_rng(11)
@@ -317,11 +328,7 @@ def test_slab_2p31_receive_side_four_workers(fmt):
         vals = (rng.standard_t(3, idx.size) * 1e-3).astype(np.float32)
         packets.append({"indices": idx.astype(np.int32), "values": vals})
     wt = w.weights(DEV)
-    touched = np.unique(np.concatenate([p["indices"] for p in packets])).astype(np.int64)
-    untouched = rng.integers(0, n, 1 << 18)
-    probe = np.unique(np.concatenate([touched, untouched, [0, n - 1]]))
-    pt = torch.from_numpy(probe).to(DEV)
-    w_probe = host(wt[pt])
+    w_np = host(wt)
     gpu_pk = []
     for p in packets:
         q = {"values": torch.from_numpy(p["values"]).to(DEV)}
@@ -334,15 +341,14 @@ def test_slab_2p31_receive_side_four_workers(fmt):
             q["bitmap"] = torch.from_numpy(words.view(np.int32)).to(DEV)
         gpu_pk.append(q)
     G = _apply(gpu_pk, [p["values"].size for p in packets], n, w.eta, wt, fmt)
-    # oracle on the probed positions only: restrict every packet to them
-    pos_in_probe = [np.searchsorted(probe, p["indices"]) for p in packets]
-    sub = [{"indices": pi.astype(np.int32), "values": p["values"]}
-           for pi, p in zip(pos_in_probe, packets)]
-    G_want = oracle.sparse_aggregate(sub, probe.size)
-    w_want = oracle.sgd_apply(w_probe, G_want, w.eta)
+    del gpu_pk
+    G_want = oracle.sparse_aggregate(packets, n)
     torch.cuda.synchronize()
-    assert_bits_equal(G[pt], G_want, "G (touched + sampled)")
-    assert_bits_equal(wt[pt], w_want, "w (touched + sampled)")
+    assert_bits_equal(G, G_want, "G")
+    del G
+    w_want = oracle.sgd_apply(w_np, G_want, w.eta)
+    del G_want, w_np
+    assert_bits_equal(wt, w_want, "w")
 
 
 def test_bitmap_format_beyond_int32_range():
@@ -367,34 +373,28 @@ def test_bitmap_format_beyond_int32_range():
     assert_bits_equal(out["bitmap"], want["bitmap"], "bitmap")
     assert_bits_equal(e, want["e"], "residual")
     del e, e_np
-    # receive side of the bitmap packet over the same 2^31+ index space
+    # receive side of the bitmap packet over the same 2^31+ index space,
+    # every element of G and w (the bitmap's set bits are want's selection)
     wt = wl.normal(n, 0.02, wl.seed(5, 7, 3), DEV)
-    sel = np.flatnonzero(oracle.unpack_bits(want["bitmap"], n))
-    probe = np.unique(np.concatenate([sel, [0, (1 << 31) - 1, 1 << 31, n - 1]]))
-    pt = torch.from_numpy(probe).to(DEV)
-    w_probe = host(wt[pt])
+    w_np = host(wt)
+    sel = want["selected"]
     G = torch.empty(n, device=DEV)
     efg.sparse_aggregate_apply([out["values"]], None, [out["bitmap"]], [sum(ks)], n, 0.1, G, wt,
                                idx_format=efg.IDX_BITMAP)
-    sub = {"indices": np.searchsorted(probe, sel).astype(np.int32), "values": want["values"]}
-    G_want = oracle.sparse_aggregate([sub], probe.size)
+    G_want = oracle.sparse_aggregate([{"indices": sel, "values": want["values"]}], n)
     torch.cuda.synchronize()
-    assert_bits_equal(G[pt], G_want, "G")
-    assert_bits_equal(wt[pt], oracle.sgd_apply(w_probe, G_want, 0.1), "w")
-    del G, wt
-    # 1-bit step over the same length (ragged tail past 2^31), sampled
+    assert_bits_equal(G, G_want, "G")
+    assert_bits_equal(wt, oracle.sgd_apply(w_np, G_want, 0.1), "w")
+    del G, wt, w_np, G_want
+    # 1-bit step over the same length (ragged tail past 2^31), every element
     eps = wl.normal(n, 0.05, wl.seed(5, 7, 4), DEV)
-    rng = np.random.default_rng(8)
-    pos = np.unique(np.concatenate([rng.integers(0, n, 1 << 18), np.arange(n - 70, n)]))
-    pt = torch.from_numpy(pos).to(DEV)
-    g_s, e_s = g_np[pos], host(eps[pt])
+    e_np = host(eps)
     bits = torch.empty((n + 31) // 32, dtype=torch.int32, device=DEV)
     efg.sign_compress(g, eps, 0.9, bits)
-    bits_want, eps_want = oracle.sign_ef_step(g_s, e_s, 0.9)
+    with oracle_pool.pool() as p:
+        bits_want, eps_want = oracle_pool.sign_ef_step(p, g_np, e_np, 0.9)
     torch.cuda.synchronize()
-    words = host(bits[torch.from_numpy(pos // 32).to(DEV)]).view(np.uint32)
-    got = ((words >> (pos % 32).astype(np.uint32)) & 1).astype(bool)
-    assert np.array_equal(got, oracle.unpack_bits(bits_want, pos.size))
-    assert_bits_equal(eps[pt], eps_want, "eps (sampled)")
+    assert_bits_equal(bits, bits_want, "bits")
+    assert_bits_equal(eps, eps_want, "eps")
     last = host(bits[-1:]).view(np.uint32)[0]
     assert last >> (n % 32) == 0                         # padding bits are 0

@@ -9,6 +9,7 @@ on inputs where every float32 operation is exact, a library routine
 plausible mistakes into copies of the oracle and checks that the pins fail.
 """
 
+import bisect
 import json
 import math
 import os
@@ -668,6 +669,35 @@ def test_randk_special_cases():
 
 
 # ---------------------------------------------------------------------------
+# packet split for the index-range exchange ([SPARSE] §详细算法流程 step 5)
+# ---------------------------------------------------------------------------
+
+
+def check_packet_split(split=oracle.packet_split):
+    # worked by hand: entries 2, 5, 9, 10; ranges [0,5), [5,10), [10,11), [11,...)
+    assert split([2, 5, 9, 10], [0, 5, 10, 11, 20]).tolist() == [0, 1, 3, 4, 4]
+    assert split([], [0, 7]).tolist() == [0, 0]
+    assert split([0], [0, 1]).tolist() == [0, 1]
+    # the lower bound of a sorted list, as the standard library's bisection finds it
+    rng = np.random.default_rng(33)
+    for _ in range(200):
+        n = int(rng.integers(1, 80))
+        idx = np.sort(rng.choice(n, int(rng.integers(0, n + 1)), replace=False))
+        bounds = np.sort(rng.integers(0, n + 2, int(rng.integers(1, 9))))
+        got = split(idx, bounds)
+        want = [bisect.bisect_left(idx.tolist(), int(b)) for b in bounds]
+        assert got.tolist() == want
+        # consecutive slices hold exactly the entries of their ranges
+        for q in range(len(bounds) - 1):
+            part = idx[got[q]:got[q + 1]]
+            assert np.all((part >= bounds[q]) & (part < bounds[q + 1]))
+
+
+def test_packet_split_pins():
+    check_packet_split()
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: the pins above must catch them
 # ---------------------------------------------------------------------------
 
@@ -802,6 +832,11 @@ def _q8_step_drops_quantisation_error(g_raw, e, offs, ks, idx_format="int32"):
     return out
 
 
+def _split_counts_equal_too(indices, bounds):
+    idx = np.asarray(indices, dtype=np.int64)
+    return np.array([int(np.count_nonzero(idx <= int(b))) for b in bounds], dtype=np.int64)
+
+
 @pytest.mark.parametrize("check,kwargs", [
     (check_topk_bruteforce, {"topk_indices": _topk_ties_to_higher_index}),
     (check_topk_bruteforce, {"topk_indices": _topk_signed_not_abs}),
@@ -821,6 +856,7 @@ def _q8_step_drops_quantisation_error(g_raw, e, offs, ks, idx_format="int32"):
     (lambda **kw: check_codec_golden("runvarint", **kw), {"encode": _runvarint_plain_delta}),
     (lambda **kw: check_codec_golden("block256", **kw), {"encode": _block256_counts_not_minus_one}),
     (lambda **kw: check_codec_golden("local16", **kw), {"encode": _local16_starts_after_block}),
+    (check_packet_split, {"split": _split_counts_equal_too}),
 ])
 def test_pins_catch_planted_mistakes(check, kwargs):
     with pytest.raises(AssertionError):
