@@ -617,11 +617,23 @@ def run_e2e(args, s):
 
 def run_extras(args, dev):
     """The other configurations, timed briefly with CUDA events (context for
-    the main line; each is also a parity test case)."""
+    the main line; each is also a parity test case), each with one step of
+    the CPU oracle timed on one host core beside it (``cpu_oracle``)."""
+    import numpy as np
     import torch
     import error_feedback_gradient_gb300 as efg
     from error_feedback_gradient_gb300 import workloads as wl
+    import oracle   # the CPU-baseline leg of each configuration only
     out = {}
+
+    def oracle_time(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def cpu_line(units, dt, sample):
+        return {"g_elems_per_s": units / dt / 1e9, "seconds": dt, "cores": 1,
+                "kind": "oracle", "sample": sample}
 
     def timed(fn, reps):
         for _ in range(3):
@@ -662,10 +674,18 @@ def run_extras(args, dev):
     with torch.cuda.graph(graph):
         c1()
     ms_graph = timed(graph.replay, 50)
+    g_np, w_np = g.cpu().numpy(), wt.cpu().numpy()
+
+    def o1():
+        pk = oracle.topk_ef_step(g_np, np.zeros(w.n, np.float32), w.seg_offsets, w.seg_k)
+        oracle.sgd_apply(w_np, oracle.sparse_aggregate([pk], w.n), w.eta)
+    dt = oracle_time(o1)
     out["topk_2p20"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
                         "ms_per_step_cuda_graph": ms_graph,
-                        "note": "L2-resident and launch-bound"}
-    del g, e, v, i, ws, wa, G, wt
+                        "note": "L2-resident and launch-bound",
+                        "cpu_oracle": cpu_line(w.n, dt, "one whole step (compress, receive "
+                                               "side, SGD)")}
+    del g, e, v, i, ws, wa, G, wt, g_np, w_np
 
     # 1-bit on 2^24 with the momentum
     w = wl.workload("sign_2p24")
@@ -678,9 +698,18 @@ def run_extras(args, dev):
         efg.sign_compress(g, eps, w.beta1, bits)
         efg.sign_aggregate_apply([bits], w.n, efg.APPLY_MOMENTUM, 0.0, w.beta1, None, m)
     ms = timed(c2, 50)
+    g_np = g.cpu().numpy()
+
+    def o2():
+        z = np.zeros(w.n, np.float32)
+        b, _ = oracle.sign_ef_step(g_np, z, w.beta1)
+        oracle.onebit_momentum(z, oracle.decode_signs(b, w.n), w.beta1)
+    dt = oracle_time(o2)
     out["sign_2p24"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
-                        "gbs": (12.125 + 8.125) * w.n / ms / 1e6}
-    del g, eps, m, bits
+                        "gbs": (12.125 + 8.125) * w.n / ms / 1e6,
+                        "cpu_oracle": cpu_line(w.n, dt, "one whole step (1-bit compress, "
+                                               "momentum)")}
+    del g, eps, m, bits, g_np
 
     # layerwise ResNet-50
     w = wl.workload("resnet50")
@@ -694,9 +723,14 @@ def run_extras(args, dev):
     def c3():
         efg.topk_compress(g, e, w.seg_offsets, w.seg_k, v, i, None, ws)
     ms = timed(c3, 30)
+    g_np = g.cpu().numpy()
+    dt = oracle_time(lambda: oracle.topk_ef_step(g_np, np.zeros(w.n, np.float32),
+                                                 w.seg_offsets, w.seg_k))
     out["resnet50"] = {"ms_per_step": ms, "g_elems_per_s": w.n / ms / 1e6,
-                       "gbs": (12 * w.n + 8 * w.total_k) / ms / 1e6}
-    del g, e, v, i, ws
+                       "gbs": (12 * w.n + 8 * w.total_k) / ms / 1e6,
+                       "cpu_oracle": cpu_line(w.n, dt, "one whole layerwise step (161 "
+                                              "tensors)")}
+    del g, e, v, i, ws, g_np
 
     # BERT-large flat, 8 workers + aggregate
     w = wl.workload("bert_large")
@@ -732,9 +766,24 @@ def run_extras(args, dev):
         efg.sparse_aggregate_apply(vs, idx, None, [w.total_k] * w.workers, w.n, w.eta, G, wt, wa)
     ms = timed(c4, 10)
     bytes_ = w.workers * (12 * w.n + 8 * w.total_k) + 4 * w.n + 16 * w.workers * w.total_k
+    # oracle: one worker's compress in full, then the receive side of the
+    # eight packets the GPU produced (the oracle's apply takes them as input)
+    g_np = gs[0].cpu().numpy()
+    packets = [{"indices": t.cpu().numpy(), "values": u.cpu().numpy()} for t, u in zip(idx, vs)]
+    w_np = wt.cpu().numpy()
+    t_c = oracle_time(lambda: oracle.topk_ef_step(g_np, np.zeros(w.n, np.float32),
+                                                  w.seg_offsets, w.seg_k))
+    t_a = oracle_time(lambda: oracle.sgd_apply(w_np, oracle.sparse_aggregate(packets, w.n),
+                                               w.eta))
+    dt = w.workers * t_c + t_a
     out["bert_large"] = {"ms_per_step": ms, "g_elems_per_s": w.workers * w.n / ms / 1e6,
                          "gbs": bytes_ / ms / 1e6,
-                         "schedule": "stream per worker" if streams else "one stream"}
+                         "schedule": "stream per worker" if streams else "one stream",
+                         "cpu_oracle": dict(cpu_line(w.workers * w.n, dt,
+                                                     f"one worker's compress timed ({t_c:.1f} s) "
+                                                     f"and counted {w.workers} times, plus the "
+                                                     f"receive side of {w.workers} packets "
+                                                     f"({t_a:.1f} s)"))}
     return out
 
 

@@ -53,6 +53,28 @@ inline void launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
   (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
 }
 
+// launch_pdl for a kernel whose CTAs form thread-block clusters of
+// `cluster` CTAs along x (the grid a multiple of it).
+template <typename... P, typename... A>
+inline void launch_cluster_pdl(void (*kernel)(P...), int cluster, dim3 grid, dim3 block,
+                               size_t smem, cudaStream_t s, A&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
 // Profiling hook: record the thread's start/stop event for `kernel_id`
 // around a launch, if set.
 void prof_begin(int kernel_id, cudaStream_t s);
@@ -259,7 +281,7 @@ __device__ __forceinline__ uint64_t lookback_warp(uint64_t* states, int64_t tile
 // its low 31 bits (so float bit patterns give |x| keys): after the call,
 // gt = #keys > T and need = k - gt (>= 1 keys equal to T are taken, lowest
 // positions first).  Digits: bits 30..20 (2048 bins), 19..10, 9..0.
-// `hist` holds 2048 words of shared memory, `scratch` >= 40 words.
+// `hist` holds 2048 words of shared memory, `scratch` >= 41 words.
 // All threads of the block must call it.
 // ---------------------------------------------------------------------------
 
@@ -301,35 +323,58 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* hist, int nbins, 
   __syncthreads();
 }
 
-// The same over keys produced by `key_at(i)` (i < n, 64-bit), e.g. read
-// from global memory; eight keys per thread are loaded before any is
-// counted, so a global source keeps eight loads in flight per thread.
+// The same over keys produced by `key_at(i)` (i < n < 2^31), e.g. read from
+// global memory; eight keys per thread are loaded before any is counted, so
+// a global source keeps eight loads in flight per thread.  With `sub` (room
+// for `sub_cap` keys of shared memory) the second digit pass also copies the
+// keys it counts -- those sharing the first digit with the k-th key -- into
+// `sub`, and if they fit, the third pass reads only them.
 template <typename KeyAt>
-__device__ __forceinline__ SelectResult block_radix_select_at(int64_t n, uint32_t k, uint32_t* hist,
-                                                              uint32_t* scratch, KeyAt key_at) {
+__device__ __forceinline__ SelectResult block_radix_select_at(int n, uint32_t k, uint32_t* hist,
+                                                              uint32_t* scratch, KeyAt key_at,
+                                                              uint32_t* sub = nullptr,
+                                                              int sub_cap = 0) {
   uint32_t prefix = 0, krem = k, gt = 0;
+  uint32_t* sub_count = scratch + 40;
+  int m = -1;  // keys in sub for the last pass (-1: read all n keys)
   for (int p = 0; p < 3; ++p) {
     // digits: bits 30..20, 19..10, 9..0
     const int shift = 20 - 10 * p, width = p == 0 ? 11 : 10;
     const int nb = 1 << width;
     const int hi = shift + width;  // bits above this digit are fixed
+    const bool collect = sub != nullptr && p == 1;
     for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+    if (collect && threadIdx.x == 0) *sub_count = 0;
     __syncthreads();
-    for (int64_t i0 = 0; i0 < n; i0 += 8 * (int64_t)blockDim.x) {
+    const bool from_sub = p == 2 && m >= 0;
+    const int len = from_sub ? m : n;
+    for (int i0 = 0; i0 < len; i0 += 8 * (int)blockDim.x) {
       uint32_t key[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int64_t i = i0 + u * (int64_t)blockDim.x + threadIdx.x;
-        key[u] = i < n ? key_at(i) & 0x7FFFFFFFu : 0u;
+        const int i = i0 + u * (int)blockDim.x + (int)threadIdx.x;
+        key[u] = i < len ? (from_sub ? sub[i] : key_at(i)) & 0x7FFFFFFFu : 0u;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int64_t i = i0 + u * (int64_t)blockDim.x + threadIdx.x;
-        const bool in = i < n && (hi >= 31 || (key[u] >> hi) == (prefix >> hi));
+        const int i = i0 + u * (int)blockDim.x + (int)threadIdx.x;
+        const bool in = i < len && (hi >= 31 || (key[u] >> hi) == (prefix >> hi));
         hist_add(hist, (key[u] >> shift) & (nb - 1), in);
+        if (collect) {
+          const unsigned mk = __ballot_sync(kFull, in);
+          if (mk != 0u) {  // warp-uniform
+            const int first = __ffs(mk) - 1;
+            uint32_t base = 0;
+            if ((int)(threadIdx.x & 31u) == first) base = atomicAdd(sub_count, (uint32_t)__popc(mk));
+            base = __shfl_sync(kFull, base, first);
+            const uint32_t pos = base + __popc(mk & lanemask_lt());
+            if (in && pos < (uint32_t)sub_cap) sub[pos] = key[u];
+          }
+        }
       }
     }
     __syncthreads();
+    if (collect) m = *sub_count <= (uint32_t)sub_cap ? (int)*sub_count : -1;
     uint32_t bin, above;
     block_find_bin(hist, nb, krem, scratch, &bin, &above);
     prefix |= bin << shift;
@@ -340,9 +385,11 @@ __device__ __forceinline__ SelectResult block_radix_select_at(int64_t n, uint32_
 }
 
 __device__ __forceinline__ SelectResult block_radix_select(const uint32_t* keys, int n, uint32_t k,
-                                                           uint32_t* hist, uint32_t* scratch) {
-  return block_radix_select_at((int64_t)n, k, hist, scratch,
-                               [keys](int64_t i) { return keys[i]; });
+                                                           uint32_t* hist, uint32_t* scratch,
+                                                           uint32_t* sub = nullptr,
+                                                           int sub_cap = 0) {
+  return block_radix_select_at(n, k, hist, scratch, [keys](int i) { return keys[i]; }, sub,
+                               sub_cap);
 }
 
 }  // namespace ef

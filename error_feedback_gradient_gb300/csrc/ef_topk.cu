@@ -8,7 +8,8 @@
 // ordered emit).  Longer segments take the streaming path, batched over the
 // streaming segments of a call:
 //   1. sample   (up to 128 CTAs per segment): up to 4096 blocks of 64
-//      contiguous elements (at most 1/16 of the segment) are compensated,
+//      contiguous elements (at most 1/16 of the segment, each in the middle
+//      of one of as many equal slots) are compensated,
 //      and one histogram of the top 13 bits of their keys gives a
 //      conservative lower threshold T_lo: the lower edge of the bin holding
 //      the rank-th largest sampled key.  Only a speed-up: the result never
@@ -21,10 +22,12 @@
 //      between k and its capacity -> select on the list; otherwise (T_lo too
 //      high or overflow) -> select on the whole segment, which is always
 //      correct, only slower, once g is back in e at the listed candidates.
-// A compact batch (every list expected to fit one CTA's shared memory, as
-// for the tensors of a layerwise model) ends with
-//   3c. finish  one CTA per segment selects on its list and emits it, in
-//      shared memory; the same launch runs the call's small segments.
+// A compact batch (every list expected to fit kFinishCap entries, as for
+// the tensors of a layerwise model) ends with
+//   3c. finish  one thread-block cluster per segment selects on its list
+//      and emits it, the list spread over the cluster's shared memory.
+// The call's small segments run as extra CTAs of the first batch's sampling
+// launch, in the shadow of the sampling.
 // Other batches end with
 //   3. restore, then select (x3): radix select on 11/10/10-bit digits of the
 //      keys of each list, shared-memory histograms merged into one per
@@ -41,6 +44,7 @@
 //      already holds +0 at every candidate, so emit writes g back at the
 //      candidates not taken (with a tight T_lo far fewer than k scattered
 //      writes); on a whole-segment list it writes e = +0 at the taken ones.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -57,18 +61,22 @@
 namespace ef {
 namespace {
 
-constexpr int kSmallMax = 32768;
+// Segments of at most kSmallMax elements are finished by one CTA from the
+// whole segment; longer ones are sampled and finished from their candidate
+// list, which for a one-CTA finish costs far less than the segment itself
+// (a 32768-element segment at k = 1 % lists about 500 candidates).
+constexpr int kSmallMax = 4096;
 constexpr int kSmallThreads = 1024;
 constexpr int kStreamWarps = 8;                 // fused pass: warps that stream the tile
 constexpr int kWarpSpan = 4096;                 // elements per streaming warp per tile
-constexpr int kTile = kStreamWarps * kWarpSpan;  // 32768 elements per fused-pass tile
-// Batches whose 32768-element tiles would occupy under half of the
-// persistent grid use 8192-element tiles, so that more SMs stream; larger
-// batches keep the longer tiles (fewer per-tile barriers and look-backs,
-// which cost more than a partial last round: 161 ResNet-50 tensors took
-// 0.155 ms per step with the long tiles and 0.177 ms with the short).
+// The fused pass picks its tile per batch among 32768, 16384 and 8192
+// elements: the one with the least rounds of the persistent grid times
+// (tile + kTileCost), kTileCost standing for a tile's fixed cost (ticket,
+// barriers, look-back) in elements; ties go to the longer tile.
+constexpr int kWarpSpanMid = 2048;
 constexpr int kWarpSpanSmall = 1024;
 constexpr int kTileSmall = kStreamWarps * kWarpSpanSmall;
+constexpr int64_t kTileCost = 4096;
 constexpr int kStreamThreads = kStreamWarps * 32;
 constexpr int kFusedThreads = kStreamThreads + 32;  // + one scan warp
 constexpr int kStageCap = 256;                  // staged candidates per warp per buffer
@@ -92,6 +100,7 @@ constexpr int kFinishCap = kSelSmall;
 constexpr int64_t kCompactLen = int64_t(1) << 22;
 
 static_assert(kWarpSpan % (128 * kBatch) == 0, "tile layout");
+static_assert(kWarpSpanMid % (128 * kBatch) == 0, "tile layout");
 static_assert(kWarpSpanSmall % (128 * kBatch) == 0, "tile layout");
 static_assert(kEmitThreads / 32 * 16 * 32 == kChunk, "emit layout");
 static_assert(kChunk % kSelThreads == 0, "select layout");
@@ -152,13 +161,10 @@ __host__ __device__ __forceinline__ int64_t sample_blocks(int64_t len) {
   return b < kSampleBlocksMax ? b : kSampleBlocksMax;
 }
 
-// First element of sample block `b` of `nblk`: the blocks are centred on
-// evenly spaced points and do not overlap (spacing >= 16 blocks).
-__host__ __device__ __forceinline__ int64_t sample_block_start(int64_t len, int64_t nblk,
-                                                             int64_t b) {
-  int64_t p = ((2 * b + 1) * len) / (2 * nblk) - kSampleBlock / 2;
-  p = p < 0 ? 0 : p;
-  return p > len - kSampleBlock ? len - kSampleBlock : p;
+// The segment is cut into nblk equal slots of spacing = floor(len / nblk)
+// (>= 1024) elements; sample block b sits in the middle of slot b.
+__host__ __device__ __forceinline__ int64_t sample_block_start(int64_t spacing, int64_t b) {
+  return b * spacing + (spacing - kSampleBlock) / 2;
 }
 
 struct alignas(256) Ctl {
@@ -198,35 +204,42 @@ __device__ __forceinline__ void emit_one(const IO& io, int64_t gidx, int64_t lid
 // count `need` are known: an entry is taken when key > T, or key == T and
 // fewer than `need` equal keys precede it; its packet position is
 // #(key > T before it) + min(#(key == T before it), need).  Warp w owns the
-// contiguous range [w * span, (w + 1) * span); one pass counts (greater,
-// equal) per warp, a scan of the warp counts gives each warp its offsets,
-// and a second pass emits with ballots.  `bits_at(j)` gives entry j's float
-// bits, `loc_at(j)` its local index in the segment.  On a candidate list
+// contiguous range [w * span, (w + 1) * span) of the CTA's entries.
+// block_count: one pass counts (greater, equal) per warp into shm[0..31] and
+// shm[32..63] and returns the CTA's totals.  block_emit: a scan of the warp
+// counts, on top of `base_gt` / `base_eq` (the entries before this CTA's,
+// when several CTAs share a list), gives each warp its offsets, and a second
+// pass emits with ballots.  `bits_at(j)` gives entry j's float bits,
+// `loc_at(j)` its local index in the segment.  On a candidate list
 // (`on_list`) e already holds +0 at every entry, so the entries not taken get
 // their value back in e; otherwise e is set to +0 at the taken entries.
-// Eight entries per lane are loaded before any is counted.  `shm` holds 64
-// words of shared memory.
-template <typename BitsAt, typename LocAt>
-__device__ __forceinline__ void block_ordered_emit(const IO& io, int64_t n, uint32_t T,
-                                                   uint32_t need, int64_t seg_off,
-                                                   int64_t out_off, int64_t k, bool on_list,
-                                                   uint32_t* shm, BitsAt bits_at, LocAt loc_at) {
-  constexpr int kRound = 8 * 32;
+// Eight entries per lane are loaded before any is counted.
+constexpr int kRound = 8 * 32;
+
+__device__ __forceinline__ void warp_span(int n, int* w0, int* w1) {
+  const int nwarps = blockDim.x >> 5;
+  const int span = ((n + nwarps - 1) / nwarps + kRound - 1) / kRound * kRound;
+  *w0 = (int)min((int64_t)(threadIdx.x >> 5) * span, (int64_t)n);
+  *w1 = (int)min((int64_t)*w0 + span, (int64_t)n);
+}
+
+template <typename BitsAt>
+__device__ __forceinline__ uint2 block_count(int n, uint32_t T, uint32_t* shm, BitsAt bits_at) {
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
-  const int64_t span = ((n + nwarps - 1) / nwarps + kRound - 1) / kRound * kRound;
-  const int64_t w0 = min((int64_t)warp * span, n), w1 = min(w0 + span, n);
+  int w0, w1;
+  warp_span(n, &w0, &w1);
   uint32_t cg = 0, ce = 0;
-  for (int64_t b = w0; b < w1; b += kRound) {
+  for (int b = w0; b < w1; b += kRound) {
     uint32_t v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int64_t j = b + u * 32 + lane;
+      const int j = b + u * 32 + (int)lane;
       v[u] = j < w1 ? bits_at(j) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int64_t j = b + u * 32 + lane;
+      const int j = b + u * 32 + (int)lane;
       const uint32_t key = v[u] & 0x7FFFFFFFu;
       cg += j < w1 && key > T;
       ce += j < w1 && key == T;
@@ -237,37 +250,55 @@ __device__ __forceinline__ void block_ordered_emit(const IO& io, int64_t n, uint
     cg += __shfl_xor_sync(kFull, cg, o);
     ce += __shfl_xor_sync(kFull, ce, o);
   }
-  uint32_t* wgt = shm;
-  uint32_t* weq = shm + 32;
   if (lane == 0) {
-    wgt[warp] = cg;
-    weq[warp] = ce;
+    shm[warp] = cg;
+    shm[32 + warp] = ce;
   }
   __syncthreads();
+  uint32_t tg = 0, te = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    tg += shm[w];
+    te += shm[32 + w];
+  }
+  return make_uint2(tg, te);
+}
+
+template <typename BitsAt, typename LocAt>
+__device__ __forceinline__ void block_emit(const IO& io, int n, uint32_t T, uint32_t need,
+                                           uint32_t base_gt, uint32_t base_eq, int64_t seg_off,
+                                           int64_t out_off, int64_t k, bool on_list,
+                                           uint32_t* shm, BitsAt bits_at, LocAt loc_at) {
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int w0, w1;
+  warp_span(n, &w0, &w1);
+  __syncthreads();  // every thread has read the warp counts (block_count)
+  uint32_t* wgt = shm;
+  uint32_t* weq = shm + 32;
   if (warp == 0) {
     const uint32_t g = lane < (unsigned)nwarps ? wgt[lane] : 0u;
     const uint32_t q = lane < (unsigned)nwarps ? weq[lane] : 0u;
     const uint32_t ig = warp_incl_scan(g), iq = warp_incl_scan(q);
     if (lane < (unsigned)nwarps) {
-      wgt[lane] = ig - g;
-      weq[lane] = iq - q;
+      wgt[lane] = base_gt + ig - g;
+      weq[lane] = base_eq + iq - q;
     }
   }
   __syncthreads();
   uint32_t run_gt = wgt[warp], run_eq = weq[warp];
   const unsigned lm = lanemask_lt();
-  for (int64_t b = w0; b < w1; b += kRound) {
+  for (int b = w0; b < w1; b += kRound) {
     uint32_t v[8];
-    int64_t loc[8];  // every entry's location is loaded with its bits, before any is used
+    int loc[8];  // every entry's location is loaded with its bits, before any is used
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int64_t j = b + u * 32 + lane;
+      const int j = b + u * 32 + (int)lane;
       v[u] = j < w1 ? bits_at(j) : 0u;
       loc[u] = j < w1 ? loc_at(j) : 0;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int64_t j = b + u * 32 + lane;
+      const int j = b + u * 32 + (int)lane;
       const uint32_t key = v[u] & 0x7FFFFFFFu;
       const bool gt = j < w1 && key > T;
       const bool eq = j < w1 && key == T;
@@ -287,18 +318,32 @@ __device__ __forceinline__ void block_ordered_emit(const IO& io, int64_t n, uint
   }
 }
 
+template <typename BitsAt, typename LocAt>
+__device__ __forceinline__ void block_ordered_emit(const IO& io, int n, uint32_t T,
+                                                   uint32_t need, int64_t seg_off,
+                                                   int64_t out_off, int64_t k, bool on_list,
+                                                   uint32_t* shm, BitsAt bits_at, LocAt loc_at) {
+  (void)block_count(n, T, shm, bits_at);
+  block_emit(io, n, T, need, 0u, 0u, seg_off, out_off, k, on_list, shm, bits_at, loc_at);
+}
+
 // ---------------------------------------------------------------------------
 // small segments: one CTA holds the whole segment
 // ---------------------------------------------------------------------------
 
-// One segment of at most kSmallMax elements by one CTA of kSmallThreads:
-// g = g_raw + e into e and into shared memory, radix select there, ordered
-// emit.  `sm` holds keys_words + 2048 + 64 words of shared memory.
+// Shared memory of a one-CTA select: keys_words of keys, then these.
+constexpr int kSubCap = 8192;  // keys kept for the last digit pass
+constexpr int kSelectExtraWords = 2048 + 64 + kSubCap;  // histogram, scratch, sub
+
+// One segment of at most kSmallMax elements by one CTA: g = g_raw + e into
+// e and into shared memory, radix select there, ordered emit.  `sm` holds
+// keys_words + 2048 + 64 + sub_cap words of shared memory.
 __device__ __forceinline__ void small_segment(const SmallSeg& sg, const IO& io, uint32_t* sm,
-                                              int keys_words) {
+                                              int keys_words, int sub_cap = kSubCap) {
   uint32_t* gbits = sm;
   uint32_t* hist = sm + keys_words;
   uint32_t* scratch = hist + 2048;
+  uint32_t* sub = scratch + 64;
   const int len = sg.len;
   const float* gr = io.g_raw + sg.off;
   float* e = io.e + sg.off;
@@ -323,10 +368,10 @@ __device__ __forceinline__ void small_segment(const SmallSeg& sg, const IO& io, 
   }
   __syncthreads();
   if (sg.k == 0) return;  // uniform across the CTA
-  const SelectResult r = block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch);
+  const SelectResult r =
+      block_radix_select(gbits, len, (uint32_t)sg.k, hist, scratch, sub, sub_cap);
   block_ordered_emit(io, len, r.T, r.need, sg.off, sg.out_off, sg.k, false, scratch,
-                     [gbits](int64_t i) { return gbits[i]; },
-                     [](int64_t i) { return i; });
+                     [gbits](int i) { return gbits[i]; }, [](int i) { return i; });
 }
 
 __global__ void __launch_bounds__(kSmallThreads)
@@ -343,18 +388,25 @@ topk_small(SmallBatch b, IO io, int keys_words) {
 constexpr int kSampleCtasMax = 128;  // CTAs per segment in each sampling pass, at most
 constexpr int kSampleThreads = 256;
 constexpr int kSampleUnroll = 4;     // sample blocks per warp in flight
+// rounds of kSampleUnroll blocks per warp: more rounds, fewer CTAs to pay
+// for zeroing and merging the histogram
+constexpr int kSampleRounds = 4;
 // The sampled lower threshold T_lo is the lower edge of a bin of the top 13
 // key bits (8 exponent + 5 mantissa bits): a bin spans at most 1/32 of its
 // value, so T_lo sits at most that far below the sampled rank's key.
 constexpr int kSampleBits = 13;
 constexpr int kSampleShift = 31 - kSampleBits;
 constexpr int kSampleBins = 1 << kSampleBits;
+// the sampling kernel's shared words: its histogram, or the whole of a small
+// segment run by the same launch (keys, histogram, scratch, last-pass keys)
+constexpr int kSampleSmem = kSampleBins + 2048 + 64;
+static_assert(kSampleBins % (4 * kSampleThreads) == 0, "sample histogram layout");
 
 // Compensated keys of sample blocks `bi` .. of this warp: lane l holds
 // elements l and l + 32 of each block.
 __device__ __forceinline__ void sample_keys(const IO& io, const LargeSeg& d, int64_t nblk,
-                                            int64_t b0, int64_t stride, unsigned lane,
-                                            uint32_t (&key)[kSampleUnroll][2],
+                                            int64_t spacing, int64_t b0, int64_t stride,
+                                            unsigned lane, uint32_t (&key)[kSampleUnroll][2],
                                             bool (&ok)[kSampleUnroll]) {
   float gv[kSampleUnroll][2], ev[kSampleUnroll][2];
 #pragma unroll
@@ -362,7 +414,7 @@ __device__ __forceinline__ void sample_keys(const IO& io, const LargeSeg& d, int
     const int64_t bi = b0 + u * stride;
     ok[u] = bi < nblk;
     if (ok[u]) {
-      const int64_t p = d.off + sample_block_start(d.len, nblk, bi) + lane;
+      const int64_t p = d.off + sample_block_start(spacing, bi) + lane;
       gv[u][0] = io.g_raw[p];
       gv[u][1] = io.g_raw[p + 32];
       ev[u][0] = io.e[p];
@@ -421,11 +473,18 @@ __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& 
 // passes.  A segment that does not sample gets its state from its one CTA.
 __global__ void __launch_bounds__(kSampleThreads)
 topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss,
-            SegState* st) {
+            SegState* st, SmallBatch sb) {
   pdl_wait();
-  __shared__ uint32_t sh[kSampleBins];
+  __shared__ __align__(16) uint32_t sh[kSampleSmem];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
+  if ((int)blockIdx.x >= grid.base[nseg]) {
+    // a small segment folded into this launch: keys, histogram, scratch and
+    // the last pass's keys all in `sh`
+    small_segment(sb.seg[blockIdx.x - grid.base[nseg]], io, sh, kSmallMax,
+                  kSampleSmem - kSmallMax - 2048 - 64);
+    return;
+  }
   int q, ctas;
   const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
   const LargeSeg d = b.seg[s];
@@ -434,25 +493,38 @@ topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, Sam
     if (q == 0 && threadIdx.x == 0) init_state(st, s, d, d.rank <= 0 ? kNoCandidate : 0u);
     return;
   }
+  const int64_t spacing = d.len / nblk;
   const unsigned lane = lane_id();
   const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
   const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
-  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x) sh[i] = 0;
+  uint4* sh4 = reinterpret_cast<uint4*>(sh);
+#pragma unroll
+  for (int r = 0; r < kSampleBins / 4 / kSampleThreads; ++r)
+    sh4[r * kSampleThreads + threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   for (int64_t b0 = gw; b0 < nblk; b0 += kWarps * kSampleUnroll) {  // warp-uniform
     uint32_t key[kSampleUnroll][2];
     bool ok[kSampleUnroll];
-    sample_keys(io, d, nblk, b0, kWarps, lane, key, ok);
+    sample_keys(io, d, nblk, spacing, b0, kWarps, lane, key, ok);
 #pragma unroll
     for (int u = 0; u < kSampleUnroll; ++u) {
-      hist_add(sh, key[u][0] >> kSampleShift, ok[u]);
-      hist_add(sh, key[u][1] >> kSampleShift, ok[u]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) hist_add(sh, key[u][h] >> kSampleShift, ok[u]);
     }
   }
   __syncthreads();
+  // merge the nonzero bins into the segment's global histogram, four bins
+  // per 16-byte read
   uint32_t* gh = hist0 + (int64_t)s * kSampleBins;
-  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x)
-    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+#pragma unroll
+  for (int r = 0; r < kSampleBins / 4 / kSampleThreads; ++r) {
+    const int i4 = r * kSampleThreads + threadIdx.x;
+    const uint4 c = sh4[i4];
+    if (c.x) atomicAdd(&gh[4 * i4], c.x);
+    if (c.y) atomicAdd(&gh[4 * i4 + 1], c.y);
+    if (c.z) atomicAdd(&gh[4 * i4 + 2], c.z);
+    if (c.w) atomicAdd(&gh[4 * i4 + 3], c.w);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -461,8 +533,15 @@ topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, Sam
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x)
-    sh[i] = *reinterpret_cast<volatile uint32_t*>(&gh[i]);
+  // the merged histogram, read from L2 (__ldcg: not from this SM's L1) with
+  // all of a thread's loads in flight at once
+  const uint4* gh4 = reinterpret_cast<const uint4*>(gh);
+  uint4 v[kSampleBins / 4 / kSampleThreads];
+#pragma unroll
+  for (int r = 0; r < kSampleBins / 4 / kSampleThreads; ++r)
+    v[r] = __ldcg(&gh4[r * kSampleThreads + threadIdx.x]);
+#pragma unroll
+  for (int r = 0; r < kSampleBins / 4 / kSampleThreads; ++r) sh4[r * kSampleThreads + threadIdx.x] = v[r];
   __syncthreads();
   uint32_t bin, above;
   block_find_bin(sh, kSampleBins, (uint32_t)d.rank, scratch, &bin, &above);
@@ -777,20 +856,29 @@ topk_select_small(IO io, SegState* st, const uint2* cand) {
   uint32_t* keys = sm;
   uint32_t* hist = sm + kSelSmall;
   uint32_t* scratch = hist + 2048;
+  uint32_t* sub = scratch + 64;
   const int seg = blockIdx.x;
   const ListRef l = list_ref(st, seg);
   const int64_t k = st[seg].d.k;
   if (k == 0 || l.len == 0 || l.len > kSelSmall) return;
   const int len = (int)l.len;
-  if (l.mode == 0) {
-    const uint2* cl = cand + l.cand_base;
-    for (int j = threadIdx.x; j < len; j += blockDim.x) keys[j] = cl[j].y;
-  } else {
-    const float* el = io.e + l.off;
-    for (int j = threadIdx.x; j < len; j += blockDim.x) keys[j] = __float_as_uint(el[j]);
+  // eight loads in flight per thread
+  for (int j0 = 0; j0 < len; j0 += 8 * kSmallThreads) {
+    uint32_t y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
+      y[u] = j >= len ? 0u
+                      : (l.mode == 0 ? cand[l.cand_base + j].y : __float_as_uint(io.e[l.off + j]));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
+      if (j < len) keys[j] = y[u];
+    }
   }
   __syncthreads();
-  const SelectResult r = block_radix_select(keys, len, (uint32_t)k, hist, scratch);
+  const SelectResult r = block_radix_select(keys, len, (uint32_t)k, hist, scratch, sub, kSubCap);
   if (threadIdx.x == 0) {
     st[seg].prefix = r.T;
     st[seg].krem = r.need;
@@ -880,9 +968,19 @@ topk_select(IO io, SegState* st, int nseg, const uint2* cand, uint32_t* ghist, C
     if (s_last) {
       __threadfence();
       uint32_t* gh = ghist + (int64_t)seg * 2048;
-      for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        sh[b] = *reinterpret_cast<volatile uint32_t*>(&gh[b]);
-        gh[b] = 0;
+      uint32_t v[2048 / kSelThreads];
+#pragma unroll
+      for (int r = 0; r < 2048 / kSelThreads; ++r) {
+        const int b = r * kSelThreads + threadIdx.x;
+        v[r] = b < nb ? __ldcg(&gh[b]) : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < 2048 / kSelThreads; ++r) {
+        const int b = r * kSelThreads + threadIdx.x;
+        if (b < nb) {
+          sh[b] = v[r];
+          gh[b] = 0;
+        }
       }
       __syncthreads();
       uint32_t bin, above;
@@ -1010,70 +1108,211 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
   }
 }
 
-// The last kernel of a compact batch, whose every streaming segment has a
-// candidate list that fits one CTA's shared memory (capacity kFinishCap):
-// blocks [0, nlarge) finish one such segment each -- select on the list and
-// ordered emit, both in shared memory -- and blocks [nlarge, gridDim.x) each
-// run one small segment folded into this launch.  A segment whose fused pass
-// fell back to the whole segment (list incomplete or T_lo above the k-th
-// key) is finished by its CTA from global memory: g goes back into e at the
-// staged candidates, then the radix select and the emit read e directly.
-// That path exists for correctness only; a compact segment is at most
-// kCompactLen elements long.
-__global__ void __launch_bounds__(kSmallThreads)
-topk_finish(SmallBatch sb, int nlarge, IO io, const SegState* st, const uint2* cand,
-            int keys_words) {
-  pdl_wait();
-  extern __shared__ uint32_t sm[];
-  if ((int)blockIdx.x >= nlarge) {
-    small_segment(sb.seg[blockIdx.x - nlarge], io, sm, keys_words);
-    return;
-  }
-  const int s = blockIdx.x;
-  const LargeSeg d = st[s].d;
-  const uint32_t mode = st[s].mode;
-  const int64_t len = st[s].list_len;
-  if (d.k == 0 || len == 0) return;  // uniform across the CTA
-  uint32_t* keys = sm;
-  uint32_t* hist = sm + keys_words;
-  uint32_t* scratch = hist + 2048;
-  const uint2* cl = cand + d.cand_base;
-  float* es = io.e + d.off;
-  if (mode == 0) {
-    // the candidate list: k <= len <= cap <= kFinishCap entries, eight loads
-    // in flight per thread
-    for (int j0 = 0; j0 < (int)len; j0 += 8 * kSmallThreads) {
-      uint32_t y[8];
+namespace cg = cooperative_groups;
+
+constexpr int kFinishThreads = 512;  // per CTA; a cluster of C CTAs shares one item
+
+// Radix select over the entries of one item split across the C CTAs of a
+// thread-block cluster (C = 1: one CTA).  Each CTA counts the keys of its
+// own share (`key_at(i)`, i < n) into its histogram; after a cluster
+// barrier every CTA sums the C histograms through distributed shared memory
+// and finds the same bin, so all CTAs agree on T, gt and need.  Histograms
+// alternate between two buffers: a CTA clears the buffer of pass p + 2 only
+// after the barrier of pass p + 1, when every CTA has finished reading it.
+// The second pass copies this CTA's keys that share the first digit with
+// the k-th key into `sub` (room for sub_cap), and the third reads only them
+// when they fit.  Shared memory: hist2 = 2 x 2048, tot = 2048, scratch = 64
+// words.
+template <int C, typename KeyAt>
+__device__ __forceinline__ SelectResult cluster_radix_select(int n, uint32_t k, uint32_t* hist2,
+                                                             uint32_t* tot, uint32_t* scratch,
+                                                             uint32_t* sub, int sub_cap,
+                                                             KeyAt key_at) {
+  uint32_t prefix = 0, krem = k, gt = 0;
+  uint32_t* sub_count = scratch + 40;
+  int m = -1;  // keys in sub for the last pass (-1: read all n keys)
+  for (int p = 0; p < 3; ++p) {
+    // digits: bits 30..20, 19..10, 9..0
+    const int shift = 20 - 10 * p, width = p == 0 ? 11 : 10;
+    const int nb = 1 << width;
+    const int hi = shift + width;  // bits above this digit are fixed
+    uint32_t* hist = hist2 + (p & 1) * 2048;
+    const bool collect = p == 1;
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+    if (collect && threadIdx.x == 0) *sub_count = 0;
+    __syncthreads();
+    const bool from_sub = p == 2 && m >= 0;
+    const int len = from_sub ? m : n;
+    for (int i0 = 0; i0 < len; i0 += 8 * (int)blockDim.x) {
+      uint32_t key[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
-        y[u] = j < (int)len ? cl[j].y : 0u;
+        const int i = i0 + u * (int)blockDim.x + (int)threadIdx.x;
+        key[u] = i < len ? (from_sub ? sub[i] : key_at(i)) & 0x7FFFFFFFu : 0u;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * kSmallThreads + (int)threadIdx.x;
-        if (j < (int)len) keys[j] = y[u];
+        const int i = i0 + u * (int)blockDim.x + (int)threadIdx.x;
+        const bool in = i < len && (hi >= 31 || (key[u] >> hi) == (prefix >> hi));
+        hist_add(hist, (key[u] >> shift) & (nb - 1), in);
+        if (collect) {
+          const unsigned mk = __ballot_sync(kFull, in);
+          if (mk != 0u) {  // warp-uniform
+            const int first = __ffs(mk) - 1;
+            uint32_t base = 0;
+            if ((int)(threadIdx.x & 31u) == first) base = atomicAdd(sub_count, (uint32_t)__popc(mk));
+            base = __shfl_sync(kFull, base, first);
+            const uint32_t pos = base + __popc(mk & lanemask_lt());
+            if (in && pos < (uint32_t)sub_cap) sub[pos] = key[u];
+          }
+        }
       }
     }
     __syncthreads();
-    const SelectResult r = block_radix_select(keys, (int)len, (uint32_t)d.k, hist, scratch);
-    block_ordered_emit(io, len, r.T, r.need, d.off, d.out_off, d.k, true, scratch,
-                       [keys](int64_t j) { return keys[j]; },
-                       [cl](int64_t j) { return (int64_t)cl[j].x; });
+    if (collect) m = *sub_count <= (uint32_t)sub_cap ? (int)*sub_count : -1;
+    uint32_t* h = hist;
+    if (C > 1) {
+      cg::cluster_group cl = cg::this_cluster();
+      cl.sync();
+      for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int q = 0; q < C; ++q) t += cl.map_shared_rank(hist, q)[b];
+        tot[b] = t;
+      }
+      __syncthreads();
+      h = tot;
+    }
+    uint32_t bin, above;
+    block_find_bin(h, nb, krem, scratch, &bin, &above);
+    prefix |= bin << shift;
+    gt += above;
+    krem -= above;
+  }
+  return SelectResult{prefix, gt, krem};
+}
+
+// The (greater, equal) counts of the cluster's CTAs before this one, from
+// each CTA's totals (`mine`, published in scratch[62..63]; block_count's
+// warp counts use scratch[0..15] and [32..47] with kFinishThreads threads).
+static_assert(kFinishThreads <= 512, "cluster totals sit above the warp counts");
+template <int C>
+__device__ __forceinline__ uint2 cluster_base(uint2 mine, uint32_t* scratch) {
+  if (C == 1) return make_uint2(0u, 0u);
+  cg::cluster_group cl = cg::this_cluster();
+  if (threadIdx.x == 0) {
+    scratch[62] = mine.x;
+    scratch[63] = mine.y;
+  }
+  cl.sync();
+  uint32_t bg = 0, be = 0;
+  const unsigned r = cl.block_rank();
+  for (unsigned q = 0; q < r; ++q) {
+    const uint32_t* o = cl.map_shared_rank(scratch, q);
+    bg += o[62];
+    be += o[63];
+  }
+  cl.sync();  // no CTA leaves while another still reads its totals
+  return make_uint2(bg, be);
+}
+
+// The last kernel of a compact batch, whose every streaming segment has a
+// candidate list that fits kFinishCap entries.  Segment i = blockIdx.x / C
+// is finished by one cluster of C CTAs, each taking a contiguous share of
+// its list: select on the list and ordered emit.  A segment whose fused pass
+// fell back to the whole segment (list incomplete or T_lo above the k-th
+// key) is finished from global memory: the cluster puts g back into e at
+// the staged candidates, then selects and emits reading e directly (a
+// correctness path; such a segment is at most kCompactLen elements long).
+// Shared memory per CTA: part_words keys, the same again (at most kSubCap)
+// for the last select pass, and the select's 6208 words of histograms and
+// scratch.
+template <int C>
+__global__ void __launch_bounds__(kFinishThreads)
+topk_finish(IO io, const SegState* st, const uint2* cand, int part_words) {
+  pdl_wait();
+  extern __shared__ uint32_t sm[];
+  const int sub_cap = min(part_words, kSubCap);
+  uint32_t* keys = sm;
+  uint32_t* sub = keys + part_words;
+  uint32_t* hist2 = sub + sub_cap;
+  uint32_t* tot = hist2 + 2 * 2048;
+  uint32_t* scratch = tot + 2048;
+  const int item = (int)blockIdx.x / C, rank = (int)blockIdx.x % C;
+  const LargeSeg d = st[item].d;
+  const uint32_t mode = st[item].mode;
+  const int64_t list_len = st[item].list_len;
+  if (d.k == 0 || list_len == 0) return;  // uniform across the cluster
+  const uint2* cl = cand + d.cand_base;
+  float* es = io.e + d.off;
+  if (mode == 0) {
+    // the candidate list: k <= len <= cap <= kFinishCap entries; this CTA's
+    // share [lo, lo + n), loaded with eight loads in flight per thread
+    const int len = (int)list_len;
+    const int per = (len + C - 1) / C;
+    const int lo = min(rank * per, len), n = min(per, len - lo);
+    const uint2* my = cl + lo;
+    for (int j0 = 0; j0 < n; j0 += 8 * kFinishThreads) {
+      uint32_t y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kFinishThreads + (int)threadIdx.x;
+        y[u] = j < n ? my[j].y : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kFinishThreads + (int)threadIdx.x;
+        if (j < n) keys[j] = y[u];
+      }
+    }
+    __syncthreads();
+    auto key_at = [keys](int i) { return keys[i]; };
+    const SelectResult r = cluster_radix_select<C>(n, (uint32_t)d.k, hist2, tot, scratch, sub,
+                                                   sub_cap, key_at);
+    const uint2 mine = block_count(n, r.T, scratch, key_at);
+    const uint2 base = cluster_base<C>(mine, scratch);
+    block_emit(io, n, r.T, r.need, base.x, base.y, d.off, d.out_off, d.k, true, scratch, key_at,
+               [my](int j) { return (int)my[j].x; });
     return;
   }
-  const int64_t c = st[s].cand_count;  // <= 0: no candidates, or a reported error
-  const int64_t m = c > 0 ? min(c, d.cap) : 0;
-  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+  // whole segment: this cluster's CTAs put g back at their share of the
+  // staged candidates, then select and emit their share of the segment
+  const int64_t c = st[item].cand_count;  // <= 0: no candidates, or a reported error
+  const int64_t mlist = c > 0 ? min(c, d.cap) : 0;
+  for (int64_t j = (int64_t)rank * kFinishThreads + threadIdx.x; j < mlist;
+       j += (int64_t)C * kFinishThreads) {
     const uint2 v = cl[j];
     if (v.x != kNoEntry && (int64_t)v.x < d.len) es[v.x] = __uint_as_float(v.y);
   }
-  __syncthreads();  // the block's writes to e are visible to the block after this
-  const SelectResult r = block_radix_select_at(
-      d.len, (uint32_t)d.k, hist, scratch, [es](int64_t i) { return __float_as_uint(es[i]); });
-  block_ordered_emit(io, d.len, r.T, r.need, d.off, d.out_off, d.k, false, scratch,
-                     [es](int64_t i) { return __float_as_uint(es[i]); },
-                     [](int64_t i) { return i; });
+  __threadfence();
+  if (C > 1) cg::this_cluster().sync();
+  else __syncthreads();
+  const int len = (int)d.len;  // at most kCompactLen
+  const int per = (len + C - 1) / C;
+  const int lo = min(rank * per, len), n = min(per, len - lo);
+  const float* mine_e = es + lo;
+  auto key_at = [mine_e](int i) { return __float_as_uint(mine_e[i]); };
+  const SelectResult r = cluster_radix_select<C>(n, (uint32_t)d.k, hist2, tot, scratch, sub,
+                                                 sub_cap, key_at);
+  const uint2 mine = block_count(n, r.T, scratch, key_at);
+  const uint2 base = cluster_base<C>(mine, scratch);
+  block_emit(io, n, r.T, r.need, base.x, base.y, d.off, d.out_off, d.k, false, scratch, key_at,
+             [lo](int i) { return lo + i; });
+}
+
+// Shared memory of a topk_finish<C> CTA for keys of up to part_words words,
+// and the share of an item of up to `len` entries.
+size_t finish_smem_words(int part_words) {
+  return (size_t)part_words + (size_t)std::min(part_words, kSubCap) + 2 * 2048 + 2048 + 64;
+}
+int finish_part_words(int cluster, int len) { return ((len + cluster - 1) / cluster + 3) & ~3; }
+
+// Cluster size of a finish launch over `items` items: wide clusters while
+// the grid stays within about one round of the GPU's SMs.
+int finish_cluster(int items, int sms) {
+  if (items * 8 <= 2 * sms) return 8;
+  if (items * 4 <= 2 * sms) return 4;
+  return 2;
 }
 
 // ---------------------------------------------------------------------------
@@ -1091,7 +1330,7 @@ struct Batch {
 struct Plan {
   std::vector<SmallSeg> small;  // longest first
   std::vector<Batch> batches;
-  size_t small_folded = 0;  // small segments run by the first compact batch's topk_finish
+  size_t small_folded = 0;  // small segments run by the first batch's sampling launch
   int64_t total_k = 0;
   // workspace regions (byte offsets); batches reuse the same regions
   size_t off_ctl = 0, off_st = 0, off_sstate = 0, off_hist0 = 0, off_hist = 0;
@@ -1154,7 +1393,7 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
       d.cap = compact ? std::min<int64_t>(len, kFinishCap) : std::min<int64_t>(len, 4 * k + 65536);
       d.cand_base = c.cand_total;
       c.cand_total += d.cap;
-      c.max_tiles += (len + kTileSmall - 1) / kTileSmall + 1;  // either tile size
+      c.max_tiles += (len + kTileSmall - 1) / kTileSmall + 1;  // any tile size
       c.max_chunks += (len + kChunk - 1) / kChunk;
       c.segs.push_back(d);
       if ((int)c.segs.size() == kMaxLarge) {
@@ -1165,15 +1404,15 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     }
     out_off += k;
   }
-  // compact batches first: the first one also runs the longest small segments
+  // compact batches first; the first batch's sampling launch also runs the
+  // longest small segments
   for (int i = 1; i >= 0; --i)
     if (!cur[i].segs.empty()) p->batches.push_back(cur[i]);
   std::stable_partition(p->batches.begin(), p->batches.end(),
                         [](const Batch& b) { return b.compact; });
   std::stable_sort(p->small.begin(), p->small.end(),
                    [](const SmallSeg& x, const SmallSeg& y) { return x.len > y.len; });
-  if (!p->batches.empty() && p->batches[0].compact)
-    p->small_folded = std::min<size_t>(p->small.size(), kMaxSmall);
+  if (!p->batches.empty()) p->small_folded = std::min<size_t>(p->small.size(), kMaxSmall);
   p->total_k = out_off;
 
   int64_t tiles = 0, chunks = 0, cands = 0, segs = 0;
@@ -1217,16 +1456,22 @@ ef_status g_attr_status[64];
 ef_status set_attributes(int dev) {
   if (dev < 0 || dev >= 64) return EF_ERR_ARCH;
   std::call_once(g_attr_once[dev], [&]() {
-    const int small_smem = (kSmallMax + 2048 + 64) * 4;
+    const int small_smem = (kSmallMax + kSelectExtraWords) * 4;
     cudaError_t e1 = cudaFuncSetAttribute(topk_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           small_smem);
-    const int sel_smem = (kSelSmall + 2048 + 64) * 4;
+    const int sel_smem = (kSelSmall + kSelectExtraWords) * 4;
     cudaError_t e2 = cudaFuncSetAttribute(topk_select_small,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
-    cudaError_t e3 = cudaFuncSetAttribute(topk_finish,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          std::max(small_smem, sel_smem));
-    cudaError_t bad = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    cudaError_t bad = e1 != cudaSuccess ? e1 : e2;
+    const int fin[3][2] = {{2, 0}, {4, 0}, {8, 0}};
+    for (const auto& f : fin) {
+      const int words = (int)finish_smem_words(finish_part_words(f[0], kFinishCap));
+      cudaError_t e = cudaSuccess;
+      if (f[0] == 2) e = cudaFuncSetAttribute(topk_finish<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, words * 4);
+      if (f[0] == 4) e = cudaFuncSetAttribute(topk_finish<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, words * 4);
+      if (f[0] == 8) e = cudaFuncSetAttribute(topk_finish<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, words * 4);
+      if (bad == cudaSuccess) bad = e;
+    }
     g_attr_status[dev] = bad == cudaSuccess ? EF_OK : cuda_fail(bad);
   });
   return g_attr_status[dev];
@@ -1321,7 +1566,7 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
       maxlen = std::max(maxlen, sb.seg[i].len);
     }
     const int keys_words = (maxlen + 3) & ~3;
-    const size_t smem = (size_t)(keys_words + 2048 + 64) * 4;
+    const size_t smem = (size_t)(keys_words + kSelectExtraWords) * 4;
     launch_pdl(topk_small, (unsigned)cnt, kSmallThreads, smem, s, sb, io, keys_words);
     if ((st = check_launch()) != EF_OK) return st;
   }
@@ -1356,32 +1601,47 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
       return n_t;
     };
     const int64_t cap_ctas = (int64_t)dev.sms * kFusedCtasPerSm;
-    int64_t tiles = count_tiles(kTile);
-    const bool small_tiles = 2 * tiles <= cap_ctas;
-    if (small_tiles) tiles = count_tiles(kTileSmall);
+    int span = kWarpSpanSmall;
+    int64_t best = INT64_MAX;
+    for (int sp : {kWarpSpan, kWarpSpanMid, kWarpSpanSmall}) {
+      const int64_t tile = (int64_t)kStreamWarps * sp;
+      const int64_t cost = (count_tiles(tile) + cap_ctas - 1) / cap_ctas * (tile + kTileCost);
+      if (cost < best) {
+        best = cost;
+        span = sp;
+      }
+    }
+    const int64_t tiles = count_tiles((int64_t)kStreamWarps * span);
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
-    // sampling CTAs per segment: one round of sample loads per warp (32
-    // blocks per CTA), at most kSampleCtasMax; one for a segment that
-    // does not sample (it sets the segment's state)
+    // sampling CTAs per segment: kSampleRounds rounds of sample loads per
+    // warp (32 blocks per round per CTA), at most kSampleCtasMax; one for a
+    // segment that does not sample (it sets the segment's state)
     SampleGrid sg;
     sg.base[0] = 0;
     for (int i = 0; i < nsg; ++i) {
       const LargeSeg& d = lb.seg[i];
       const int64_t nblk = sample_blocks(d.len);
-      const int64_t per = (int64_t)(kSampleThreads / 32) * kSampleUnroll;
+      const int64_t per = (int64_t)(kSampleThreads / 32) * kSampleUnroll * kSampleRounds;
       const int64_t c = (d.rank > 0 && d.rank <= nblk * kSampleBlock)
                             ? std::min<int64_t>(kSampleCtasMax, (nblk + per - 1) / per)
                             : 1;
       sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
     }
-    launch_pdl(topk_sample, sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io, hist0, sstate,
-               sst);
+    // the first batch's sampling launch also runs the folded small segments
+    SmallBatch sb;
+    const size_t nsmall = first_batch ? p.small_folded : 0;
+    for (size_t i = 0; i < nsmall; ++i) sb.seg[i] = p.small[i];
+    launch_pdl(topk_sample, (unsigned)(sg.base[nsg] + nsmall), kSampleThreads, 0, s, lb, sg, nsg,
+               io, hist0, sstate, sst, sb);
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
-    if (small_tiles)
+    if (span == kWarpSpanSmall)
       launch_pdl(topk_fused<kWarpSpanSmall>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles,
+                 tstate, cand, ctl, phase, vec);
+    else if (span == kWarpSpanMid)
+      launch_pdl(topk_fused<kWarpSpanMid>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles,
                  tstate, cand, ctl, phase, vec);
     else
       launch_pdl(topk_fused<kWarpSpan>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate,
@@ -1389,22 +1649,22 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
     if (b.compact) {
-      // one CTA per segment, plus the folded small segments (longest first)
-      SmallBatch sb;
-      const size_t nsmall = first_batch ? p.small_folded : 0;
-      int keys_words = kFinishCap;
-      for (size_t i = 0; i < nsmall; ++i) {
-        sb.seg[i] = p.small[i];
-        keys_words = std::max(keys_words, (p.small[i].len + 3) & ~3);
-      }
-      const size_t smem = (size_t)(keys_words + 2048 + 64) * 4;
-      launch_pdl(topk_finish, (unsigned)(nsg + nsmall), kSmallThreads, smem, s, sb, nsg, io, sst,
-                 cand, keys_words);
+      // one cluster per segment
+      const int cl = finish_cluster(nsg, dev.sms);
+      const int part = finish_part_words(cl, kFinishCap);
+      const size_t smem = finish_smem_words(part) * 4;
+      const unsigned grid = (unsigned)(nsg * cl);
+      if (cl == 8)
+        launch_cluster_pdl(topk_finish<8>, 8, grid, kFinishThreads, smem, s, io, sst, cand, part);
+      else if (cl == 4)
+        launch_cluster_pdl(topk_finish<4>, 4, grid, kFinishThreads, smem, s, io, sst, cand, part);
+      else
+        launch_cluster_pdl(topk_finish<2>, 2, grid, kFinishThreads, smem, s, io, sst, cand, part);
       if ((st = check_launch()) != EF_OK) return st;
     } else {
       launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
       if ((st = check_launch()) != EF_OK) return st;
-      launch_pdl(topk_select_small, nsg, kSmallThreads, (size_t)(kSelSmall + 2048 + 64) * 4, s,
+      launch_pdl(topk_select_small, nsg, kSmallThreads, (size_t)(kSelSmall + kSelectExtraWords) * 4, s,
                  io, sst, cand);
       if ((st = check_launch()) != EF_OK) return st;
       const int sgrid =

@@ -346,6 +346,10 @@ EF_API ef_status ef_randk_compress(const float* g_raw, float* e, int64_t n, int3
  * out_bits [ceil(n/32)] uint32: bit i%32 of word i/32 is element i's bit;
  *          padding bits 0.  Must not overlap g or eps; g and eps must not
  *          overlap.
+ * Device status: none can arise.  The kernels have no inter-block waits and
+ * every address they touch follows from n alone (no index is read from
+ * memory), so this call and sign_aggregate_apply take no workspace and have
+ * no device-side status word; argument errors are returned directly.
  * ---------------------------------------------------------------------- */
 EF_API ef_status ef_sign_compress(const float* g, float* eps, int64_t n, float beta1,
                            uint32_t* out_bits, void* stream);

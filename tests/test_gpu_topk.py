@@ -85,11 +85,12 @@ def test_unaligned_addresses():
 
 def _sample_block_starts(n):
     """Starts of the sampled blocks of a streaming segment of n elements:
-    min(4096, n // 1024) blocks of 64 contiguous elements centred on evenly
-    spaced points (the documented sampling rule of the library)."""
+    min(4096, n // 1024) blocks of 64 contiguous elements, block b in the
+    middle of the b-th of that many equal slots of n // nblk elements (the
+    documented sampling rule of the library)."""
     nblk = min(4096, n // 1024)
-    b = np.arange(nblk, dtype=np.int64)
-    return np.clip((2 * b + 1) * n // (2 * nblk) - 32, 0, n - 64)
+    sp = n // nblk
+    return np.arange(nblk, dtype=np.int64) * sp + (sp - 64) // 2
 
 
 def test_sampled_threshold_too_high_falls_back():
