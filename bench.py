@@ -1001,7 +1001,8 @@ def run_case(args):
     isolation (--case): 'topk' (one tensor of n elements, top-0.1 %),
     'aggregate' (4 workers' int32 packets of 0.1 % over n, with G and SGD),
     'randk' (random sparsification of one tensor, expected 0.1 %), 'resnet50'
-    (the layerwise top-k step over the 161 ResNet-50 gradient tensors), 'sign'
+    (the layerwise top-k step over the 161 ResNet-50 gradient tensors),
+    'topk_2p20' (the 2^20-element top-1 % step with its receive side), 'sign'
     (1-bit compression of 4 workers' gradients of n elements, then their
     sign aggregate with G and SGD), 'q8' (top-0.1 % with 8-bit values, then
     the receiver's dequantisation) or 'codec' (a top-0.1 % packet of n
@@ -1035,6 +1036,22 @@ def run_case(args):
                          device=dev)
         for _ in range(3):
             efg.sparse_aggregate_apply(vals, ix, None, [k] * W, n, 0.1, G, w, ws)
+    elif args.case == "topk_2p20":
+        w = wl.workload("topk_2p20")
+        n, k = w.n, w.total_k
+        g = w.gradient(0, 1, dev)
+        e = torch.zeros_like(g)
+        v = torch.empty(k, device=dev)
+        ix = torch.empty(k, dtype=torch.int32, device=dev)
+        ws = torch.empty(efg.topk_workspace_size(n, w.seg_offsets, w.seg_k), dtype=torch.uint8,
+                         device=dev)
+        wa = torch.empty(efg.aggregate_workspace_size(1, efg.IDX_INT32, n), dtype=torch.uint8,
+                         device=dev)
+        G = torch.empty_like(g)
+        wt = w.weights(dev)
+        for _ in range(3):
+            efg.topk_compress(g, e, w.seg_offsets, w.seg_k, v, ix, None, ws)
+            efg.sparse_aggregate_apply([v], [ix], None, [k], n, w.eta, G, wt, wa)
     elif args.case == "resnet50":
         w = wl.workload("resnet50")
         n, k = w.n, w.total_k
@@ -1127,8 +1144,8 @@ def main(argv=None):
     p.add_argument("--exchange", choices=["allgather", "range"], default=None,
                    help="time the exchanged step instead: one worker per rank, top-k, "
                         "packet exchange across the ranks, receive side")
-    p.add_argument("--case", choices=["topk", "aggregate", "randk", "resnet50", "sign", "q8",
-                                       "codec"],
+    p.add_argument("--case", choices=["topk", "aggregate", "randk", "resnet50", "topk_2p20",
+                                       "sign", "q8", "codec"],
                    default=None,
                    help="run one entry point alone (three calls at --n) for profiling")
     args = p.parse_args(argv)

@@ -9,11 +9,13 @@
 // streaming segments of a call:
 //   1. sample   (up to 128 CTAs per segment): up to 4096 blocks of 64
 //      contiguous elements (at most 1/16 of the segment, each in the middle
-//      of one of as many equal slots) are compensated,
-//      and one histogram of the top 13 bits of their keys gives a
-//      conservative lower threshold T_lo: the lower edge of the bin holding
-//      the rank-th largest sampled key.  Only a speed-up: the result never
-//      depends on it.
+//      of one of as many equal slots) are compensated, and a histogram of
+//      their keys gives a conservative lower threshold T_lo.  In a compact
+//      batch (below) one pass over the top 13 key bits, T_lo = the lower
+//      edge of the 13-bit bin holding the rank-th largest sampled key; in
+//      other batches two short passes (top 11 bits, then the next 10 inside
+//      the chosen bin), T_lo = the lower edge of that 21-bit bin.  Only a
+//      speed-up: the result never depends on it.
 //   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e,
 //      except that a key >= T_lo is written as +0 and appended, in index
 //      order, to a per-segment candidate list (warp ballots and a bounded
@@ -149,9 +151,11 @@ struct SegState {
   int64_t cand_count;       // candidates found by the fused pass (-1: unknown)
 };
 
-// Per-segment state of the sampling pass (in the cleared control area).
+// Per-segment state of the sampling passes (in the cleared control area).
 struct SampleState {
-  uint32_t done;  // CTAs finished
+  uint32_t done[2];  // CTAs finished in the first / second pass
+  uint32_t b0;       // two-pass form: top-11-bit bin holding the rank-th sampled key
+  uint32_t r1;       // that key's rank inside the bin
 };
 
 // Sample blocks of a segment of `len` elements (> kSmallMax): at most 1/16
@@ -471,19 +475,28 @@ __device__ __forceinline__ void init_state(SegState* st, int s, const LargeSeg& 
 // edge of the bin holding the rank-th largest sampled key (so at least
 // `rank` sampled keys are >= T_lo) and the segment's state for the later
 // passes.  A segment that does not sample gets its state from its one CTA.
+// Small segments ride in the same launch only when a call has them
+// (kSmall): the launch without them keeps the shared memory to the
+// histogram and the parameters to the segment table, so that it holds as
+// little as possible of the SMs that other streams' streaming passes share.
+struct NoSmall {};
+
+template <bool kSmall, typename Smalls>
 __global__ void __launch_bounds__(kSampleThreads)
 topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, SampleState* ss,
-            SegState* st, SmallBatch sb) {
+            SegState* st, Smalls sb) {
   pdl_wait();
-  __shared__ __align__(16) uint32_t sh[kSampleSmem];
+  __shared__ __align__(16) uint32_t sh[kSmall ? kSampleSmem : kSampleBins];
   __shared__ uint32_t scratch[64];
   __shared__ int s_last;
-  if ((int)blockIdx.x >= grid.base[nseg]) {
-    // a small segment folded into this launch: keys, histogram, scratch and
-    // the last pass's keys all in `sh`
-    small_segment(sb.seg[blockIdx.x - grid.base[nseg]], io, sh, kSmallMax,
-                  kSampleSmem - kSmallMax - 2048 - 64);
-    return;
+  if constexpr (kSmall) {
+    if ((int)blockIdx.x >= grid.base[nseg]) {
+      // a small segment folded into this launch: keys, histogram, scratch
+      // and the last pass's keys all in `sh`
+      small_segment(sb.seg[blockIdx.x - grid.base[nseg]], io, sh, kSmallMax,
+                    kSampleSmem - kSmallMax - 2048 - 64);
+      return;
+    }
   }
   int q, ctas;
   const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
@@ -528,7 +541,7 @@ topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, Sam
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(&ss[s].done, 1u) == (uint32_t)ctas - 1;
+    s_last = atomicAdd(&ss[s].done[0], 1u) == (uint32_t)ctas - 1;
   }
   __syncthreads();
   if (!s_last) return;
@@ -549,6 +562,121 @@ topk_sample(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0, Sam
   // its nonzeros instead of overflowing; with fewer than k of them the
   // whole-segment select takes over as for any T_lo above the k-th key)
   if (threadIdx.x == 0) init_state(st, s, d, max(bin << kSampleShift, 1u));
+}
+
+// The two-pass form of the sampling, for batches whose lists are long (a
+// flat tensor of many million elements): one round of sample loads per warp
+// and small histograms (2048, then 1024 bins) in two short launches.  T_lo
+// is the lower edge of the 21-bit bin holding the rank-th largest sampled
+// key.  With several such calls on concurrent streams (one per worker)
+// this form keeps the streams' streaming passes overlapped: the one-pass
+// 8192-bin form measured 452 against 475 G elements/s on the four-worker
+// 2^31 step, though alone it is as fast.
+constexpr int kCoarseBins = 2048;
+constexpr int kFineBins = 1024;
+
+__global__ void __launch_bounds__(kSampleThreads)
+topk_sample_coarse(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist0,
+                   SampleState* ss) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ uint32_t sh[kCoarseBins];
+  __shared__ uint32_t scratch[64];
+  __shared__ int s_last;
+  int q, ctas;
+  const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
+  const LargeSeg& d = b.seg[s];
+  const int64_t nblk = sample_blocks(d.len);
+  if (!samples_needed(d, nblk)) return;  // uniform across the CTA
+  const int64_t spacing = d.len / nblk;
+  const unsigned lane = lane_id();
+  const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
+  const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  for (int64_t b0 = gw; b0 < nblk; b0 += kWarps * kSampleUnroll) {  // warp-uniform
+    uint32_t key[kSampleUnroll][2];
+    bool ok[kSampleUnroll];
+    sample_keys(io, d, nblk, spacing, b0, kWarps, lane, key, ok);
+#pragma unroll
+    for (int u = 0; u < kSampleUnroll; ++u) {
+      hist_add(sh, key[u][0] >> 20, ok[u]);
+      hist_add(sh, key[u][1] >> 20, ok[u]);
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = hist0 + (int64_t)s * kSampleBins;
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ss[s].done[0], 1u) == (uint32_t)ctas - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) sh[i] = __ldcg(&gh[i]);
+  __syncthreads();
+  uint32_t bin, above;
+  block_find_bin(sh, kCoarseBins, (uint32_t)d.rank, scratch, &bin, &above);
+  if (threadIdx.x == 0) {
+    ss[s].b0 = bin;
+    ss[s].r1 = (uint32_t)d.rank - above;
+  }
+}
+
+__global__ void __launch_bounds__(kSampleThreads)
+topk_sample_fine(LargeBatch b, SampleGrid grid, int nseg, IO io, uint32_t* hist1,
+                 SampleState* ss, SegState* st) {
+  pdl_wait();
+  __shared__ uint32_t sh[kFineBins];
+  __shared__ uint32_t scratch[64];
+  __shared__ int s_last;
+  int q, ctas;
+  const int s = sample_seg(grid, nseg, blockIdx.x, &q, &ctas);
+  const LargeSeg d = b.seg[s];
+  const int64_t nblk = sample_blocks(d.len);
+  if (!samples_needed(d, nblk)) {
+    if (q == 0 && threadIdx.x == 0) init_state(st, s, d, d.rank <= 0 ? kNoCandidate : 0u);
+    return;
+  }
+  const int64_t spacing = d.len / nblk;
+  const uint32_t b0 = __ldcg(&ss[s].b0);
+  const unsigned lane = lane_id();
+  const int64_t gw = (int64_t)q * (kSampleThreads / 32) + (threadIdx.x >> 5);
+  const int64_t kWarps = (int64_t)ctas * (kSampleThreads / 32);
+  for (int i = threadIdx.x; i < kFineBins; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  for (int64_t bb = gw; bb < nblk; bb += kWarps * kSampleUnroll) {  // warp-uniform
+    uint32_t key[kSampleUnroll][2];
+    bool ok[kSampleUnroll];
+    sample_keys(io, d, nblk, spacing, bb, kWarps, lane, key, ok);
+#pragma unroll
+    for (int u = 0; u < kSampleUnroll; ++u) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        hist_add(sh, (key[u][h] >> 10) & (kFineBins - 1), ok[u] && (key[u][h] >> 20) == b0);
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = hist1 + (int64_t)s * kFineBins;
+  for (int i = threadIdx.x; i < kFineBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ss[s].done[1], 1u) == (uint32_t)ctas - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kFineBins; i += blockDim.x) sh[i] = __ldcg(&gh[i]);
+  __syncthreads();
+  uint32_t bin, above;
+  block_find_bin(sh, kFineBins, __ldcg(&ss[s].r1), scratch, &bin, &above);
+  // T_lo >= 1, as in the one-pass form
+  if (threadIdx.x == 0) init_state(st, s, d, max((b0 << 20) | (bin << 10), 1u));
 }
 
 __device__ __forceinline__ int find_seg(const int64_t* base, int nseg, int64_t x) {
@@ -1330,10 +1458,10 @@ struct Batch {
 struct Plan {
   std::vector<SmallSeg> small;  // longest first
   std::vector<Batch> batches;
-  size_t small_folded = 0;  // small segments run by the first batch's sampling launch
+  size_t small_folded = 0;  // small segments run by the first compact batch's sampling launch
   int64_t total_k = 0;
   // workspace regions (byte offsets); batches reuse the same regions
-  size_t off_ctl = 0, off_st = 0, off_sstate = 0, off_hist0 = 0, off_hist = 0;
+  size_t off_ctl = 0, off_st = 0, off_sstate = 0, off_hist0 = 0, off_hist1 = 0, off_hist = 0;
   size_t off_tiles = 0, off_chunks = 0, off_cand = 0;
   size_t ctl_clear_bytes = 0;  // bytes cleared from off_ctl before each batch
   size_t bytes = 0;
@@ -1412,7 +1540,8 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
                         [](const Batch& b) { return b.compact; });
   std::stable_sort(p->small.begin(), p->small.end(),
                    [](const SmallSeg& x, const SmallSeg& y) { return x.len > y.len; });
-  if (!p->batches.empty()) p->small_folded = std::min<size_t>(p->small.size(), kMaxSmall);
+  if (!p->batches.empty() && p->batches[0].compact)
+    p->small_folded = std::min<size_t>(p->small.size(), kMaxSmall);
   p->total_k = out_off;
 
   int64_t tiles = 0, chunks = 0, cands = 0, segs = 0;
@@ -1436,6 +1565,8 @@ ef_status make_plan(int64_t n, int32_t nseg, const int64_t* offs, const int64_t*
     off = round_up(off + sizeof(SampleState) * segs, 256);
     p->off_hist0 = off;
     off = round_up(off + (size_t)segs * kSampleBins * 4, 256);
+    p->off_hist1 = off;
+    if (general) off = round_up(off + (size_t)segs * kFineBins * 4, 256);
     p->off_hist = off;
     if (general) off = round_up(off + (size_t)segs * 2048 * 4, 256);
     p->off_tiles = off;
@@ -1615,25 +1746,40 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
     if (err != cudaSuccess) return cuda_fail(err);
     // sampling CTAs per segment: kSampleRounds rounds of sample loads per
-    // warp (32 blocks per round per CTA), at most kSampleCtasMax; one for a
-    // segment that does not sample (it sets the segment's state)
+    // warp in a compact batch, one otherwise (32 blocks per round per CTA),
+    // at most kSampleCtasMax; one for a segment that does not sample (it
+    // sets the segment's state)
     SampleGrid sg;
     sg.base[0] = 0;
     for (int i = 0; i < nsg; ++i) {
       const LargeSeg& d = lb.seg[i];
       const int64_t nblk = sample_blocks(d.len);
-      const int64_t per = (int64_t)(kSampleThreads / 32) * kSampleUnroll * kSampleRounds;
+      const int64_t per =
+          (int64_t)(kSampleThreads / 32) * kSampleUnroll * (b.compact ? kSampleRounds : 1);
       const int64_t c = (d.rank > 0 && d.rank <= nblk * kSampleBlock)
                             ? std::min<int64_t>(kSampleCtasMax, (nblk + per - 1) / per)
                             : 1;
       sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
     }
-    // the first batch's sampling launch also runs the folded small segments
-    SmallBatch sb;
     const size_t nsmall = first_batch ? p.small_folded : 0;
-    for (size_t i = 0; i < nsmall; ++i) sb.seg[i] = p.small[i];
-    launch_pdl(topk_sample, (unsigned)(sg.base[nsg] + nsmall), kSampleThreads, 0, s, lb, sg, nsg,
-               io, hist0, sstate, sst, sb);
+    if (!b.compact) {
+      // long lists: the two short sampling passes
+      uint32_t* hist1 = reinterpret_cast<uint32_t*>(ws + p.off_hist1);
+      launch_pdl(topk_sample_coarse, (unsigned)sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg,
+                 io, hist0, sstate);
+      if ((st = check_launch()) != EF_OK) return st;
+      launch_pdl(topk_sample_fine, (unsigned)sg.base[nsg], kSampleThreads, 0, s, lb, sg, nsg, io,
+                 hist1, sstate, sst);
+    } else if (nsmall > 0) {
+      // the first compact batch's sampling launch also runs the folded small segments
+      SmallBatch sb;
+      for (size_t i = 0; i < nsmall; ++i) sb.seg[i] = p.small[i];
+      launch_pdl(topk_sample<true, SmallBatch>, (unsigned)(sg.base[nsg] + nsmall), kSampleThreads,
+                 0, s, lb, sg, nsg, io, hist0, sstate, sst, sb);
+    } else {
+      launch_pdl(topk_sample<false, NoSmall>, (unsigned)sg.base[nsg], kSampleThreads, 0, s, lb, sg,
+                 nsg, io, hist0, sstate, sst, NoSmall{});
+    }
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
