@@ -39,22 +39,24 @@ if ROOT not in sys.path:
 METRIC = "G grad elements/s per EF compress+apply step; HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "G grad elements/s"
 
-# DRAM traffic of one topk_fused launch from one ncu capture (--set full,
-# slab workload at n = 2^26 per worker, see profiles/): 536.96 MB read +
-# 224.00 MB written = 11.339 bytes per element.  Reported, scaled by n, only
-# while the captured code still hashes to what was captured (the kernel's
-# region of ef_topk.cu, from its staging struct to the end of the kernel, and
-# the shared device header); otherwise null.  (Reads scale with n exactly;
-# the writes fall short of 12 B by the dirty lines still in L2 when the
-# captured launch ends.)
-FUSED_TRAFFIC_PER_ELEMENT = 11.339
+# DRAM traffic of one topk_fused launch from one ncu capture (--set full of
+# the second launch of `bench.py --case topk --n 139460608`, the 32768-element
+# tile form the slab uses; see profiles/): 1115.91 MB read + 517.20 MB
+# written = 11.710 bytes per element.  Reported, scaled by n, only while the
+# captured code still hashes to what was captured (the kernel's region of
+# ef_topk.cu, from its staging struct to the end of the kernel, and the
+# shared device header); otherwise null.  (Reads scale with n exactly; the
+# writes fall short of 4 B per element by the dirty lines still in L2 when
+# the captured launch ends, about 40 MB at this size, so the scaled figure
+# slightly understates a full-size launch.)
+FUSED_TRAFFIC_PER_ELEMENT = 11.710
 FUSED_TRAFFIC_SOURCES = {
     # (file, first marker, end marker or None for the whole file): sha256
     ("error_feedback_gradient_gb300/csrc/ef_topk.cu", "struct FusedStage {",
      "// A segment's select list:"):
         "ac3e3b1803607664f19791741692b953ed06478e7763f53ce3f180224be6bb55",
     ("error_feedback_gradient_gb300/csrc/ef_common.cuh", None, None):
-        "2bbcf9705edd30ef00918744e5b1800515cb99aba3bd167ee166c761eb82a3cc",
+        "390ccd36b92770dc4c6cea7187d128e4a7949b1c543abff90ab0aaf87c4b3931",
 }
 
 
@@ -467,15 +469,25 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = load_peaks()
     n = s.n
     kernels = {}
-    names = {1: "topk_fused", 2: "sign_compress", 3: "sparse_aggregate_apply",
-             4: "sign_aggregate_apply"}
-    kb = {1: 12 * n, 2: 12.125 * n, 3: None, 4: ab["sign_apply"]}
+    names = {1: "topk_fused", 2: "sign_compress", 4: "sign_aggregate_apply"}
+    kb = {1: 12 * n, 2: 12.125 * n, 4: ab["sign_apply"]}
+    # the step calls sparse_aggregate_apply twice, int32 packets then bitmap
+    # packets; the hook records them in that order
+    if 3 in per:
+        ts = per.pop(3)
+        for i, fmt in enumerate(("int32", "bitmap")):
+            names[30 + i] = f"sparse_aggregate_apply_{fmt}"
+            kb[30 + i] = ab[f"aggregate_{fmt}"]
+            per[30 + i] = ts[i::2]
     for kid, ts in per.items():
         avg = statistics.mean(ts)
         d = {"launches_per_step": len(ts) // max(1, args.prof_steps), "avg_ms": avg}
         if kb.get(kid):
             d["algorithmic_bytes"] = kb[kid]
             d["achieved_gbs"] = kb[kid] / (avg * 1e-3) / 1e9
+            d["frac_of_peak"] = d["achieved_gbs"] / load_peaks()[0]
+        if kid in (30, 31):
+            d["note"] = "the apply kernel alone; the run-boundary pass before it is not timed"
         kernels[names[kid]] = d
     top = kernels["topk_fused"]
     roofline = {"bound": "hbm", "kernel": "topk_fused",
