@@ -19,11 +19,13 @@
 //   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e,
 //      except that a key >= T_lo is written as +0 and appended, in index
 //      order, to a per-segment candidate list (warp ballots and a bounded
-//      decoupled look-back).  A candidate that finds no room in a staging
-//      buffer or the list keeps g in e.  The last CTA checks each list:
-//      between k and its capacity -> select on the list; otherwise (T_lo too
-//      high or overflow) -> select on the whole segment, which is always
-//      correct, only slower, once g is back in e at the listed candidates.
+//      decoupled look-back).  A warp's span whose candidates overflow its
+//      staging buffer is rescanned from L2 by the scan warp, so the list
+//      stays complete; a candidate past the list's capacity keeps g in e.
+//      The last CTA checks each list: between k and its capacity -> select
+//      on the list; otherwise (T_lo too high, or the list over capacity) ->
+//      select on the whole segment, which is always correct, only slower,
+//      once g is back in e at the listed candidates.
 // A compact batch (every list expected to fit kFinishCap entries, as for
 // the tensors of a layerwise model) ends with
 //   3c. finish  one thread-block cluster per segment selects on its list
@@ -866,7 +868,6 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
       const uint32_t c = lane < kStreamWarps ? sg.cnt[b][lane] : 0u;
       const uint32_t inc = warp_incl_scan(c);
       const uint32_t agg = __shfl_sync(kFull, inc, 31);
-      if (__any_sync(kFull, c > kStageCap) && lane == 0) atomicOr(&st[seg].overflow, 1u);
       const uint64_t excl = lookback_warp(tstate, tile, s_base[seg], agg, io.status);
       if (agg) {
         const int64_t cap = st[seg].d.cap;
@@ -883,9 +884,47 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
             else
               es[v.x] = __uint_as_float(v.y);  // no room in the list: e keeps g
           }
-          // list slots of candidates that found no staging slot
-          for (uint32_t j = kStageCap + lane; j < ct && base + j < cap; j += 32)
-            out[base + j] = make_uint2(kNoEntry, 0u);
+          if (ct > kStageCap && base + kStageCap < cap) {  // warp-uniform
+            // The candidates that found no staging slot (a span whose
+            // candidates cluster) still hold g in e, after the last staged
+            // one.  Staged candidates hold +0 and T_lo >= 1, so a rescan of
+            // the rest of the span from L2 finds exactly them, in index
+            // order: they fill list slots base + kStageCap on and get +0 in
+            // e like every listed candidate (past the capacity they keep g).
+            // Once the slots lie past the capacity there is nothing to fill:
+            // the list is over capacity and the whole-segment select runs.
+            const uint32_t t_lo = st[seg].t_lo;
+            const int64_t w0 = (st[seg].d.q_first + (tile - s_base[seg])) *
+                                   (int64_t)(kStreamWarps * kSpan) +
+                               (int64_t)w * kSpan - phase;
+            const int64_t end = min(w0 + kSpan, st[seg].d.off + st[seg].d.len) - st[seg].d.off;
+            int64_t pos = base + kStageCap;
+            uint32_t found = 0;
+            for (int64_t i0 = (int64_t)sg.cand[b][w][kStageCap - 1].x + 1; i0 < end; i0 += 128) {
+              float v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * 32 + lane;
+                v[u] = i < end ? __ldcg(es + i) : 0.0f;
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * 32 + lane;
+                const bool cnd = i < end && abs_key(v[u]) >= t_lo;
+                const unsigned m = __ballot_sync(kFull, cnd);
+                const int64_t p = pos + __popc(m & lanemask_lt());
+                if (cnd && p < cap) {
+                  out[p] = make_uint2((uint32_t)i, __float_as_uint(v[u]));
+                  es[i] = 0.0f;
+                }
+                pos += __popc(m);
+                found += __popc(m);
+              }
+            }
+            // a count that does not match would leave the list incomplete:
+            // the whole-segment select then takes over
+            if (found != ct - kStageCap && lane == 0) atomicOr(&st[seg].overflow, 1u);
+          }
         }
       }
       __syncwarp();

@@ -1,4 +1,4 @@
-"""The packet exchange's rank logic on CPU: two gloo ranks run
+"""The packet exchange's rank logic on CPU: two and three gloo ranks run
 ``Exchange.allgather_apply`` (int32 and bitmap packets) and
 ``Exchange.range_apply`` ("梯度稀疏化：只传输重要的梯度元素", §详细算法流程
 step 5 and §与Allreduce的融合).
@@ -14,6 +14,7 @@ import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.multiprocessing as mp
 
@@ -135,8 +136,8 @@ def _expect(world, n, k, w0, steps=1):
     return G, w
 
 
-def test_two_gloo_ranks_exchange_packets():
-    world, n, k = 2, 10_007, 400
+@pytest.mark.parametrize("world,n,k", [(2, 10_007, 400), (3, 5_000, 300)])
+def test_gloo_ranks_exchange_packets(world, n, k):
     from error_feedback_gradient_gb300 import exchange as ex
     res = _run(world, n, k)
     w0 = (np.random.default_rng(7).standard_normal(ex.padded_length(n, world)) * 0.02).astype(F32)

@@ -121,6 +121,20 @@ def test_candidate_list_over_capacity_falls_back(fmt):
     check_topk_step(torch.from_numpy(g_np).to(DEV), torch.zeros(n, device=DEV), [0, n], [k], fmt)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(3_000_000, 3000), (5_000_000, 5000)])
+def test_clustered_candidates_overflow_a_warps_staging(n, k, fmt):
+    """The largest values sit in one contiguous run, as when a few rows of a
+    gradient carry all the large entries: one warp's span holds far more
+    candidates than its staging buffer.  A segment of 3 M elements is in a
+    compact batch, one of 5 M in a general one."""
+    rng = np.random.default_rng(n % 997)
+    g_np = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    start = n // 3 + 7
+    g_np[start:start + 2 * k] = (0.5 + rng.random(2 * k)).astype(np.float32)
+    check_topk_step(torch.from_numpy(g_np).to(DEV), torch.zeros(n, device=DEV), [0, n], [k], fmt)
+
+
 def test_multistep_carries_residual():
     n, k = 500_000, 500
     e = torch.zeros(n, device=DEV)
