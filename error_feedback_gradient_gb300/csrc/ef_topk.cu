@@ -76,7 +76,9 @@ constexpr int kWarpSpan = 4096;                 // elements per streaming warp p
 // The fused pass picks its tile per batch among 32768, 16384 and 8192
 // elements: the one with the least rounds of the persistent grid times
 // (tile + kTileCost), kTileCost standing for a tile's fixed cost (ticket,
-// barriers, look-back) in elements; ties go to the longer tile.
+// barriers, look-back) in elements; ties go to the longer tile.  (4096-element
+// tiles measured slower wherever the rule would pick them: the 2^20-element
+// call 42.8 against 38.8 us with 8192, their look-back chains twice as long.)
 constexpr int kWarpSpanMid = 2048;
 constexpr int kWarpSpanSmall = 1024;
 constexpr int kTileSmall = kStreamWarps * kWarpSpanSmall;
@@ -94,7 +96,6 @@ constexpr int kEmitThreads = 256;  // 8 warps x 16 rounds x 32 lanes = kChunk
 constexpr int kMaxLarge = 128;     // segments per streaming batch
 constexpr int kMaxSmall = 512;     // segments per small-path launch
 constexpr uint32_t kNoCandidate = 0x80000000u;  // above every 31-bit key
-constexpr uint32_t kNoEntry = 0xFFFFFFFFu;      // candidate-list slot of an unstaged candidate
 constexpr int kSelSmall = 32768;  // lists up to this length are selected by one CTA
 // Compact batches: every streaming segment is at most kCompactLen elements
 // and its expected candidate list at most half of kFinishCap entries, so one
@@ -733,22 +734,57 @@ struct FusedStage {
   int64_t next[2];                         // ticket broadcast to the streaming warps
 };
 
+// What the fused pass left for segment s: its candidate count c (-1 if the
+// last tile's state holds no inclusive prefix: a reported error), and
+// which list its select runs on (mode 0: the candidate list, of c entries;
+// mode 1: the whole segment, when the list is short of k, over capacity or
+// incomplete).  `last_tile_state` is the state word of its last tile.
+struct SegOutcome {
+  uint32_t mode;
+  int64_t len, count;
+};
+__device__ __forceinline__ SegOutcome seg_outcome(const LargeSeg& d, uint64_t last_tile_state,
+                                                  uint32_t overflow) {
+  SegOutcome o;
+  const uint64_t w = last_tile_state;
+  o.count = (w >> 62) == 2 ? (int64_t)(w & kPayloadMask) : -1;
+  o.mode = (o.count >= d.k && o.count <= d.cap && !overflow) ? 0u : 1u;
+  o.len = o.mode == 0 ? o.count : d.len;
+  if (d.k == 0) {
+    o.mode = 0;
+    o.len = 0;
+  }
+  return o;
+}
+
 // The HBM pass.  Warps 0..7 stream tiles (ticket order): g = g_raw + e is
 // written over e, and every element with key >= T_lo of its segment is
 // staged in shared memory in index order.  Warp 8 takes each filled staging
 // buffer, resolves the tile's offset in its segment's candidate list with the
 // bounded decoupled look-back, and writes the candidates out; two buffers let
-// the streaming warps run one tile ahead of it.
-template <int kSpan>
+// the streaming warps run one tile ahead of it.  For a general batch the
+// last CTA to finish records each segment's outcome for the select passes;
+// in a compact batch (kCompact) topk_finish derives it itself.
+template <int kSpan, bool kCompact>
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
            uint2* cand, Ctl* ctl, int phase, int vec) {
   pdl_wait();
   __shared__ int64_t s_base[kMaxLarge + 1];
+  // the segments' fields a tile needs, so that starting a tile reads no
+  // global memory
+  __shared__ int64_t s_off[kMaxLarge], s_len[kMaxLarge], s_qf[kMaxLarge];
+  __shared__ uint32_t s_tlo[kMaxLarge];
   __shared__ FusedStage sg;
   __shared__ int s_last;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_base[i] = st[i].d.tile_base;
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) {
+    s_base[i] = st[i].d.tile_base;
+    s_off[i] = st[i].d.off;
+    s_len[i] = st[i].d.len;
+    s_qf[i] = st[i].d.q_first;
+    s_tlo[i] = st[i].t_lo;
+  }
   if (threadIdx.x == 0) s_base[nseg] = total_tiles;
   __syncthreads();
 
@@ -772,15 +808,15 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
         break;
       }
       const int seg = find_seg(s_base, nseg, tile);
-      const int64_t a = st[seg].d.off;
-      const uint32_t t_lo = st[seg].t_lo;
-      // this warp's 2048-element window, as pointers and 32-bit offsets
-      const int64_t w0 = (st[seg].d.q_first + (tile - s_base[seg])) * (kStreamWarps * kSpan) +
+      const int64_t a = s_off[seg];
+      const uint32_t t_lo = s_tlo[seg];
+      // this warp's window, as pointers and 32-bit offsets
+      const int64_t w0 = (s_qf[seg] + (tile - s_base[seg])) * (kStreamWarps * kSpan) +
                          (int64_t)warp * kSpan - phase;
       const float* gp = io.g_raw + w0;
       float* ep = io.e + w0;
       const int lo = (int)max((int64_t)-4, min(a - w0, (int64_t)kSpan));
-      const int hi = (int)max((int64_t)-4, min(a + st[seg].d.len - w0, (int64_t)kSpan + 4));
+      const int hi = (int)max((int64_t)-4, min(a + s_len[seg] - w0, (int64_t)kSpan + 4));
       const uint32_t loc0 = (uint32_t)(w0 - a);  // local index of window offset 0 (mod 2^32)
       uint2* stage = sg.cand[b][warp];
       uint32_t count = 0;
@@ -868,7 +904,11 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
       const uint32_t c = lane < kStreamWarps ? sg.cnt[b][lane] : 0u;
       const uint32_t inc = warp_incl_scan(c);
       const uint32_t agg = __shfl_sync(kFull, inc, 31);
-      const uint64_t excl = lookback_warp(tstate, tile, s_base[seg], agg, io.status);
+      uint64_t excl;
+      if constexpr (kCompact)  // topk_finish reads the states after the kernel ends
+        excl = lookback_warp_short<4>(tstate, tile, s_base[seg], agg, io.status);
+      else
+        excl = lookback_warp(tstate, tile, s_base[seg], agg, io.status);
       if (agg) {
         const int64_t cap = st[seg].d.cap;
         float* es = io.e + st[seg].d.off;
@@ -933,6 +973,7 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
   }
 
   // The last CTA to finish decides, per segment, which list the select runs on.
+  if (kCompact) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -942,16 +983,12 @@ topk_fused(IO io, SegState* st, int nseg, int64_t total_tiles, uint64_t* tstate,
   if (!s_last) return;
   __threadfence();
   for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
-    const LargeSeg& d = st[s].d;
-    const uint64_t w = ld_acquire(&tstate[s_base[s + 1] - 1]);
-    const int64_t c = (w >> 62) == 2 ? (int64_t)(w & kPayloadMask) : -1;
-    const uint32_t ovf = *reinterpret_cast<volatile uint32_t*>(&st[s].overflow);
-    uint32_t mode = (c >= d.k && c <= d.cap && !ovf) ? 0u : 1u;
-    int64_t len = mode == 0 ? c : d.len;
-    if (d.k == 0) { mode = 0; len = 0; }
-    st[s].mode = mode;
-    st[s].list_len = len;
-    st[s].cand_count = c;
+    const SegOutcome o =
+        seg_outcome(st[s].d, ld_acquire(&tstate[s_base[s + 1] - 1]),
+                    *reinterpret_cast<volatile uint32_t*>(&st[s].overflow));
+    st[s].mode = o.mode;
+    st[s].list_len = o.len;
+    st[s].cand_count = o.count;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -985,8 +1022,8 @@ constexpr int kRestoreThreads = 256;
 // A segment whose select runs on the whole segment (mode 1) reads its keys
 // from e, which must then hold g everywhere: g is put back at the candidates
 // the fused pass staged and wrote as +0, from the candidate list (its first
-// min(candidates, capacity) slots; slots of never-staged candidates hold
-// kNoEntry).  Segments selecting on their list are left alone.
+// min(candidates, capacity) slots, every one written by the fused pass).
+// Segments selecting on their list are left alone.
 // The segments' states are read in one parallel round into shared memory,
 // so a batch without such a segment costs one load per thread.
 __global__ void __launch_bounds__(kRestoreThreads)
@@ -1008,7 +1045,7 @@ topk_restore(IO io, const SegState* st, int nseg, const uint2* cand) {
     float* es = io.e + st[s].d.off;
     for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < m; j += nthr) {
       const uint2 v = l[j];
-      if (v.x != kNoEntry && (int64_t)v.x < len) es[v.x] = __uint_as_float(v.y);
+      if ((int64_t)v.x < len) es[v.x] = __uint_as_float(v.y);
     }
   }
 }
@@ -1339,13 +1376,28 @@ __device__ __forceinline__ SelectResult cluster_radix_select(int n, uint32_t k, 
     if (collect) m = *sub_count <= (uint32_t)sub_cap ? (int)*sub_count : -1;
     uint32_t* h = hist;
     if (C > 1) {
+      // the C histograms summed through distributed shared memory, all of a
+      // thread's remote loads in flight at once
       cg::cluster_group cl = cg::this_cluster();
       cl.sync();
-      for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+      constexpr int kPer = 2048 / kFinishThreads;
+      const uint32_t* rh[C];
+#pragma unroll
+      for (int q = 0; q < C; ++q) rh[q] = cl.map_shared_rank(hist, q);
+      uint32_t v[kPer][C];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int b = u * kFinishThreads + (int)threadIdx.x;
+#pragma unroll
+        for (int q = 0; q < C; ++q) v[u][q] = b < nb ? rh[q][b] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int b = u * kFinishThreads + (int)threadIdx.x;
         uint32_t t = 0;
 #pragma unroll
-        for (int q = 0; q < C; ++q) t += cl.map_shared_rank(hist, q)[b];
-        tot[b] = t;
+        for (int q = 0; q < C; ++q) t += v[u][q];
+        if (b < nb) tot[b] = t;
       }
       __syncthreads();
       h = tot;
@@ -1363,6 +1415,7 @@ __device__ __forceinline__ SelectResult cluster_radix_select(int n, uint32_t k, 
 // each CTA's totals (`mine`, published in scratch[62..63]; block_count's
 // warp counts use scratch[0..15] and [32..47] with kFinishThreads threads).
 static_assert(kFinishThreads <= 512, "cluster totals sit above the warp counts");
+static_assert(2048 % kFinishThreads == 0, "cluster histogram reduction layout");
 template <int C>
 __device__ __forceinline__ uint2 cluster_base(uint2 mine, uint32_t* scratch) {
   if (C == 1) return make_uint2(0u, 0u);
@@ -1396,7 +1449,8 @@ __device__ __forceinline__ uint2 cluster_base(uint2 mine, uint32_t* scratch) {
 // scratch.
 template <int C>
 __global__ void __launch_bounds__(kFinishThreads)
-topk_finish(IO io, const SegState* st, const uint2* cand, int part_words) {
+topk_finish(IO io, const SegState* st, int nseg, const uint64_t* tstate, int64_t total_tiles,
+            const uint2* cand, int part_words) {
   pdl_wait();
   extern __shared__ uint32_t sm[];
   const int sub_cap = min(part_words, kSubCap);
@@ -1407,8 +1461,10 @@ topk_finish(IO io, const SegState* st, const uint2* cand, int part_words) {
   uint32_t* scratch = tot + 2048;
   const int item = (int)blockIdx.x / C, rank = (int)blockIdx.x % C;
   const LargeSeg d = st[item].d;
-  const uint32_t mode = st[item].mode;
-  const int64_t list_len = st[item].list_len;
+  const int64_t next_tile = item + 1 < nseg ? st[item + 1].d.tile_base : total_tiles;
+  const SegOutcome o = seg_outcome(d, tstate[next_tile - 1], st[item].overflow);
+  const uint32_t mode = o.mode;
+  const int64_t list_len = o.len;
   if (d.k == 0 || list_len == 0) return;  // uniform across the cluster
   const uint2* cl = cand + d.cand_base;
   float* es = io.e + d.off;
@@ -1444,12 +1500,12 @@ topk_finish(IO io, const SegState* st, const uint2* cand, int part_words) {
   }
   // whole segment: this cluster's CTAs put g back at their share of the
   // staged candidates, then select and emit their share of the segment
-  const int64_t c = st[item].cand_count;  // <= 0: no candidates, or a reported error
+  const int64_t c = o.count;  // <= 0: no candidates, or a reported error
   const int64_t mlist = c > 0 ? min(c, d.cap) : 0;
   for (int64_t j = (int64_t)rank * kFinishThreads + threadIdx.x; j < mlist;
        j += (int64_t)C * kFinishThreads) {
     const uint2 v = cl[j];
-    if (v.x != kNoEntry && (int64_t)v.x < d.len) es[v.x] = __uint_as_float(v.y);
+    if ((int64_t)v.x < d.len) es[v.x] = __uint_as_float(v.y);
   }
   __threadfence();
   if (C > 1) cg::this_cluster().sync();
@@ -1716,7 +1772,13 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
   if ((st = set_attributes(devid)) != EF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  cudaError_t err = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
+  // the status word, and with it a compact first batch's control region
+  // (which follows it directly): one memset less in a short call (1.6 us
+  // of a 2^20-element call), while calls that stream long lists on several
+  // streams at once measured 0.15 % slower with the merged memset
+  const bool merged = !p.batches.empty() && p.batches[0].compact;
+  const size_t clear0 = merged ? p.off_ctl + p.ctl_clear_bytes : sizeof(WsHeader);
+  cudaError_t err = cudaMemsetAsync(ws, 0, clear0, s);
   if (err != cudaSuccess) return cuda_fail(err);
   if (n == 0) return EF_OK;
   if (bitmap) {
@@ -1782,8 +1844,10 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
       }
     }
     const int64_t tiles = count_tiles((int64_t)kStreamWarps * span);
-    err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
-    if (err != cudaSuccess) return cuda_fail(err);
+    if (!(first_batch && merged)) {
+      err = cudaMemsetAsync(ws + p.off_ctl, 0, p.ctl_clear_bytes, s);
+      if (err != cudaSuccess) return cuda_fail(err);
+    }
     // sampling CTAs per segment: kSampleRounds rounds of sample loads per
     // warp in a compact batch, one otherwise (32 blocks per round per CTA),
     // at most kSampleCtasMax; one for a segment that does not sample (it
@@ -1822,15 +1886,19 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     if ((st = check_launch()) != EF_OK) return st;
     const int fgrid = (int)std::min<int64_t>(tiles, (int64_t)dev.sms * kFusedCtasPerSm);
     prof_begin(EF_KERNEL_TOPK_FUSED, s);
-    if (span == kWarpSpanSmall)
-      launch_pdl(topk_fused<kWarpSpanSmall>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles,
-                 tstate, cand, ctl, phase, vec);
-    else if (span == kWarpSpanMid)
-      launch_pdl(topk_fused<kWarpSpanMid>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles,
-                 tstate, cand, ctl, phase, vec);
-    else
-      launch_pdl(topk_fused<kWarpSpan>, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate,
-                 cand, ctl, phase, vec);
+    auto fused = [&](auto kernel) {
+      launch_pdl(kernel, fgrid, kFusedThreads, 0, s, io, sst, nsg, tiles, tstate, cand, ctl, phase,
+                 vec);
+    };
+    if (b.compact) {
+      if (span == kWarpSpanSmall) fused(topk_fused<kWarpSpanSmall, true>);
+      else if (span == kWarpSpanMid) fused(topk_fused<kWarpSpanMid, true>);
+      else fused(topk_fused<kWarpSpan, true>);
+    } else {
+      if (span == kWarpSpanSmall) fused(topk_fused<kWarpSpanSmall, false>);
+      else if (span == kWarpSpanMid) fused(topk_fused<kWarpSpanMid, false>);
+      else fused(topk_fused<kWarpSpan, false>);
+    }
     if ((st = check_launch()) != EF_OK) return st;
     prof_end(EF_KERNEL_TOPK_FUSED, s);
     if (b.compact) {
@@ -1840,11 +1908,14 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
       const size_t smem = finish_smem_words(part) * 4;
       const unsigned grid = (unsigned)(nsg * cl);
       if (cl == 8)
-        launch_cluster_pdl(topk_finish<8>, 8, grid, kFinishThreads, smem, s, io, sst, cand, part);
+        launch_cluster_pdl(topk_finish<8>, 8, grid, kFinishThreads, smem, s, io, sst, nsg,
+                           tstate, tiles, cand, part);
       else if (cl == 4)
-        launch_cluster_pdl(topk_finish<4>, 4, grid, kFinishThreads, smem, s, io, sst, cand, part);
+        launch_cluster_pdl(topk_finish<4>, 4, grid, kFinishThreads, smem, s, io, sst, nsg,
+                           tstate, tiles, cand, part);
       else
-        launch_cluster_pdl(topk_finish<2>, 2, grid, kFinishThreads, smem, s, io, sst, cand, part);
+        launch_cluster_pdl(topk_finish<2>, 2, grid, kFinishThreads, smem, s, io, sst, nsg,
+                           tstate, tiles, cand, part);
       if ((st = check_launch()) != EF_OK) return st;
     } else {
       launch_pdl(topk_restore, dev.sms * 2, kRestoreThreads, 0, s, io, sst, nsg, cand);
