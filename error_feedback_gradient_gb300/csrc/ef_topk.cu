@@ -1315,6 +1315,7 @@ topk_emit(IO io, SegState* st, int nseg, const uint2* cand, uint64_t* cstate, Ct
 namespace cg = cooperative_groups;
 
 constexpr int kFinishThreads = 512;  // per CTA; a cluster of C CTAs shares one item
+constexpr uint32_t kNoDigit = 0xFFFFFFFFu;  // a key that a digit pass does not count
 
 // Radix select over the entries of one item split across the C CTAs of a
 // thread-block cluster (C = 1: one CTA).  Each CTA counts the keys of its
@@ -1411,6 +1412,81 @@ __device__ __forceinline__ SelectResult cluster_radix_select(int n, uint32_t k, 
   return SelectResult{prefix, gt, krem};
 }
 
+// One cluster-wide digit pass: every CTA counts digit(i) of its keys with
+// in(i) set into `hist` (2048 words, cleared here), the C histograms are
+// summed through distributed shared memory into `tot`, and the bin holding
+// rank krem is found.  Returns (bin, keys above it).
+template <int C, typename DigitAt>
+__device__ __forceinline__ uint2 cluster_digit_pass(int n, int nb, uint32_t krem, uint32_t* hist,
+                                                    uint32_t* tot, uint32_t* scratch,
+                                                    DigitAt digit_at) {
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < n; i0 += 8 * (int)blockDim.x) {
+    uint32_t dg[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * (int)blockDim.x + (int)threadIdx.x;
+      dg[u] = i < n ? digit_at(i) : kNoDigit;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) hist_add(hist, dg[u], dg[u] != kNoDigit);
+  }
+  __syncthreads();
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+  constexpr int kPer = 2048 / kFinishThreads;
+  const uint32_t* rh[C];
+#pragma unroll
+  for (int q = 0; q < C; ++q) rh[q] = cl.map_shared_rank(hist, q);
+  uint32_t v[kPer][C];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int b = u * kFinishThreads + (int)threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < C; ++q) v[u][q] = b < nb ? rh[q][b] : 0u;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int b = u * kFinishThreads + (int)threadIdx.x;
+    uint32_t t = 0;
+#pragma unroll
+    for (int q = 0; q < C; ++q) t += v[u][q];
+    if (b < nb) tot[b] = t;
+  }
+  __syncthreads();
+  uint32_t bin, above;
+  block_find_bin(tot, nb, krem, scratch, &bin, &above);
+  return make_uint2(bin, above);
+}
+
+// Select on a candidate list whose keys are all >= t_lo (the sampled lower
+// threshold), in two cluster passes instead of three: the k-th key lies a
+// little above t_lo, so the first digit is taken relative to it,
+// d0 = min((key - t_lo) >> 11, 2047) -- the top bin gathering every key at
+// least 2047 * 2^11 above t_lo -- and the second digit is the low 11 bits
+// of key - t_lo.  If the k-th key falls in the top bin (t_lo far below it)
+// the result is not usable and *ok is false on every CTA of the cluster
+// (they all find the same bin).  Buffers as in cluster_radix_select.
+template <int C, typename KeyAt>
+__device__ __forceinline__ SelectResult cluster_window_select(int n, uint32_t k, uint32_t t_lo,
+                                                              uint32_t* hist2, uint32_t* tot,
+                                                              uint32_t* scratch, KeyAt key_at,
+                                                              bool* ok) {
+  const uint2 r0 = cluster_digit_pass<C>(n, 2048, k, hist2, tot, scratch, [&](int i) {
+    const uint32_t off = (key_at(i) & 0x7FFFFFFFu) - t_lo;
+    return min(off >> 11, 2047u);
+  });
+  *ok = r0.x < 2047u;
+  if (!*ok) return SelectResult{0u, 0u, 0u};
+  const uint32_t krem = k - r0.y;
+  const uint2 r1 = cluster_digit_pass<C>(n, 2048, krem, hist2 + 2048, tot, scratch, [&](int i) {
+    const uint32_t off = (key_at(i) & 0x7FFFFFFFu) - t_lo;
+    return (off >> 11) == r0.x ? (off & 2047u) : kNoDigit;
+  });
+  return SelectResult{t_lo + (r0.x << 11) + r1.x, r0.y + r1.y, krem - r1.y};
+}
+
 // The (greater, equal) counts of the cluster's CTAs before this one, from
 // each CTA's totals (`mine`, published in scratch[62..63]; block_count's
 // warp counts use scratch[0..15] and [32..47] with kFinishThreads threads).
@@ -1490,8 +1566,17 @@ topk_finish(IO io, const SegState* st, int nseg, const uint64_t* tstate, int64_t
     }
     __syncthreads();
     auto key_at = [keys](int i) { return keys[i]; };
-    const SelectResult r = cluster_radix_select<C>(n, (uint32_t)d.k, hist2, tot, scratch, sub,
-                                                   sub_cap, key_at);
+    // two passes relative to T_lo; three from the top bits if the k-th key
+    // lies far above T_lo (every CTA takes the same branch)
+    bool ok = false;
+    SelectResult r;
+    if (C > 1)
+      r = cluster_window_select<C>(n, (uint32_t)d.k, st[item].t_lo, hist2, tot, scratch, key_at,
+                                   &ok);
+    if (!ok) {
+      if (C > 1) cg::this_cluster().sync();  // no CTA still reads this one's histograms
+      r = cluster_radix_select<C>(n, (uint32_t)d.k, hist2, tot, scratch, sub, sub_cap, key_at);
+    }
     const uint2 mine = block_count(n, r.T, scratch, key_at);
     const uint2 base = cluster_base<C>(mine, scratch);
     block_emit(io, n, r.T, r.need, base.x, base.y, d.off, d.out_off, d.k, true, scratch, key_at,

@@ -108,6 +108,25 @@ def test_sampled_threshold_too_high_falls_back():
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_kth_key_far_above_sampled_threshold(fmt):
+    """The k largest values (about 1.0) sit off the sampled blocks, among
+    small lognormal ones (about 1e-4), so the sampled threshold comes from
+    the small values: the candidate list (about 23 k entries) still fits,
+    but the k-th key lies some 2^26 key units above the threshold.  The
+    finish's two-pass select, whose first digit counts from the threshold,
+    cannot place it and must hand over to the three-pass select."""
+    n, k = 1 << 20, 10486
+    rng = np.random.default_rng(5)
+    g_np = (1e-4 * np.exp(rng.standard_normal(n))).astype(np.float32)
+    starts = _sample_block_starts(n)
+    sampled = np.zeros(n, bool)
+    sampled[(starts[:, None] + np.arange(64)[None, :]).ravel()] = True
+    big = rng.choice(np.flatnonzero(~sampled), k, replace=False)
+    g_np[big] = (1.0 + rng.random(k)).astype(np.float32)
+    check_topk_step(torch.from_numpy(g_np).to(DEV), torch.zeros(n, device=DEV), [0, n], [k], fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_candidate_list_over_capacity_falls_back(fmt):
     """5 % of the elements tie at the largest value: every one is a
     candidate (about 200 per 4096-element warp span, within the staging
