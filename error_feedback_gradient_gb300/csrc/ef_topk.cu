@@ -1936,19 +1936,25 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
     // sampling CTAs per segment: kSampleRounds rounds of sample loads per
     // warp in a compact batch, one otherwise (32 blocks per round per CTA),
     // at most kSampleCtasMax; one for a segment that does not sample (it
-    // sets the segment's state)
-    SampleGrid sg;
-    sg.base[0] = 0;
-    for (int i = 0; i < nsg; ++i) {
-      const LargeSeg& d = lb.seg[i];
-      const int64_t nblk = sample_blocks(d.len);
-      const int64_t per =
-          (int64_t)(kSampleThreads / 32) * kSampleUnroll * (b.compact ? kSampleRounds : 1);
-      const int64_t c = (d.rank > 0 && d.rank <= nblk * kSampleBlock)
-                            ? std::min<int64_t>(kSampleCtasMax, (nblk + per - 1) / per)
-                            : 1;
-      sg.base[i + 1] = sg.base[i] + (int32_t)std::max<int64_t>(1, c);
-    }
+    // sets the segment's state).  A compact batch whose one-round grid still
+    // fits one CTA per SM (a single tensor of a few million elements) takes
+    // one round too: its CTAs then wait for one load round trip, not four.
+    auto sample_grid = [&](int rounds) {
+      SampleGrid g;
+      g.base[0] = 0;
+      for (int i = 0; i < nsg; ++i) {
+        const LargeSeg& d = lb.seg[i];
+        const int64_t nblk = sample_blocks(d.len);
+        const int64_t per = (int64_t)(kSampleThreads / 32) * kSampleUnroll * rounds;
+        const int64_t c = (d.rank > 0 && d.rank <= nblk * kSampleBlock)
+                              ? std::min<int64_t>(kSampleCtasMax, (nblk + per - 1) / per)
+                              : 1;
+        g.base[i + 1] = g.base[i] + (int32_t)std::max<int64_t>(1, c);
+      }
+      return g;
+    };
+    SampleGrid sg = sample_grid(1);
+    if (b.compact && sg.base[nsg] > dev.sms) sg = sample_grid(kSampleRounds);
     const size_t nsmall = first_batch ? p.small_folded : 0;
     if (!b.compact) {
       // long lists: the two short sampling passes
