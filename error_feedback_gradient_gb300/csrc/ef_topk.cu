@@ -1412,16 +1412,14 @@ __device__ __forceinline__ SelectResult cluster_radix_select(int n, uint32_t k, 
   return SelectResult{prefix, gt, krem};
 }
 
-// One cluster-wide digit pass: every CTA counts digit(i) of its keys with
-// in(i) set into `hist` (2048 words, cleared here), the C histograms are
-// summed through distributed shared memory into `tot`, and the bin holding
-// rank krem is found.  Returns (bin, keys above it).
+// One cluster-wide digit pass: every CTA counts digit(i) of its keys (those
+// that are not kNoDigit) into `hist` (2048 words, all zero on entry), the C
+// histograms are summed through distributed shared memory into `tot`, and
+// the bin holding rank krem is found.  Returns (bin, keys above it).
 template <int C, typename DigitAt>
 __device__ __forceinline__ uint2 cluster_digit_pass(int n, int nb, uint32_t krem, uint32_t* hist,
                                                     uint32_t* tot, uint32_t* scratch,
                                                     DigitAt digit_at) {
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
-  __syncthreads();
   for (int i0 = 0; i0 < n; i0 += 8 * (int)blockDim.x) {
     uint32_t dg[8];
 #pragma unroll
@@ -1467,7 +1465,9 @@ __device__ __forceinline__ uint2 cluster_digit_pass(int n, int nb, uint32_t krem
 // least 2047 * 2^11 above t_lo -- and the second digit is the low 11 bits
 // of key - t_lo.  If the k-th key falls in the top bin (t_lo far below it)
 // the result is not usable and *ok is false on every CTA of the cluster
-// (they all find the same bin).  Buffers as in cluster_radix_select.
+// (they all find the same bin).  Buffers as in cluster_radix_select; both
+// histograms of hist2 are zero on entry (the caller clears them with its
+// own loads, before the barrier it has anyway).
 template <int C, typename KeyAt>
 __device__ __forceinline__ SelectResult cluster_window_select(int n, uint32_t k, uint32_t t_lo,
                                                               uint32_t* hist2, uint32_t* tot,
@@ -1508,8 +1508,18 @@ __device__ __forceinline__ uint2 cluster_base(uint2 mine, uint32_t* scratch) {
     bg += o[62];
     be += o[63];
   }
-  cl.sync();  // no CTA leaves while another still reads its totals
+  // no CTA may leave while another still reads its totals: arrive here and
+  // wait in cluster_leave() at the end of the kernel, so the emit runs while
+  // the barrier completes
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
   return make_uint2(bg, be);
+}
+
+// The other half of cluster_base's last barrier; every thread calls it once
+// before leaving.
+template <int C>
+__device__ __forceinline__ void cluster_leave() {
+  if (C > 1) asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // The last kernel of a compact batch, whose every streaming segment has a
@@ -1564,6 +1574,8 @@ topk_finish(IO io, const SegState* st, int nseg, const uint64_t* tstate, int64_t
         if (j < n) keys[j] = y[u];
       }
     }
+    // both histograms of the two-pass select start at zero
+    for (int b = threadIdx.x; b < 2 * 2048; b += kFinishThreads) hist2[b] = 0;
     __syncthreads();
     auto key_at = [keys](int i) { return keys[i]; };
     // two passes relative to T_lo; three from the top bits if the k-th key
@@ -1581,6 +1593,7 @@ topk_finish(IO io, const SegState* st, int nseg, const uint64_t* tstate, int64_t
     const uint2 base = cluster_base<C>(mine, scratch);
     block_emit(io, n, r.T, r.need, base.x, base.y, d.off, d.out_off, d.k, true, scratch, key_at,
                [my](int j) { return (int)my[j].x; });
+    cluster_leave<C>();
     return;
   }
   // whole segment: this cluster's CTAs put g back at their share of the
@@ -1606,6 +1619,7 @@ topk_finish(IO io, const SegState* st, int nseg, const uint64_t* tstate, int64_t
   const uint2 base = cluster_base<C>(mine, scratch);
   block_emit(io, n, r.T, r.need, base.x, base.y, d.off, d.out_off, d.k, false, scratch, key_at,
              [lo](int i) { return lo + i; });
+  cluster_leave<C>();
 }
 
 // Shared memory of a topk_finish<C> CTA for keys of up to part_words words,
