@@ -1461,23 +1461,25 @@ __device__ __forceinline__ uint2 cluster_digit_pass(int n, int nb, uint32_t krem
 // Select on a candidate list whose keys are all >= t_lo (the sampled lower
 // threshold), in two cluster passes instead of three: the k-th key lies a
 // little above t_lo, so the first digit is taken relative to it,
-// d0 = min((key - t_lo) >> 11, 2047) -- the top bin gathering every key at
-// least 2047 * 2^11 above t_lo -- and the second digit is the low 11 bits
-// of key - t_lo.  If the k-th key falls in the top bin (t_lo far below it)
+// d0 = min((key - t_lo) >> 11, kWinBins - 1) -- the top bin gathering every
+// key at least (kWinBins - 1) * 2^11 above t_lo, about an eighth of an
+// octave at the least -- and the second digit is the low 11 bits of
+// key - t_lo.  If the k-th key falls in the top bin (t_lo far below it)
 // the result is not usable and *ok is false on every CTA of the cluster
 // (they all find the same bin).  Buffers as in cluster_radix_select; both
 // histograms of hist2 are zero on entry (the caller clears them with its
 // own loads, before the barrier it has anyway).
+constexpr uint32_t kWinBins = 1024;  // first-digit bins of the two-pass select (the last: the rest)
 template <int C, typename KeyAt>
 __device__ __forceinline__ SelectResult cluster_window_select(int n, uint32_t k, uint32_t t_lo,
                                                               uint32_t* hist2, uint32_t* tot,
                                                               uint32_t* scratch, KeyAt key_at,
                                                               bool* ok) {
-  const uint2 r0 = cluster_digit_pass<C>(n, 2048, k, hist2, tot, scratch, [&](int i) {
+  const uint2 r0 = cluster_digit_pass<C>(n, kWinBins, k, hist2, tot, scratch, [&](int i) {
     const uint32_t off = (key_at(i) & 0x7FFFFFFFu) - t_lo;
-    return min(off >> 11, 2047u);
+    return min(off >> 11, kWinBins - 1u);
   });
-  *ok = r0.x < 2047u;
+  *ok = r0.x < kWinBins - 1u;
   if (!*ok) return SelectResult{0u, 0u, 0u};
   const uint32_t krem = k - r0.y;
   const uint2 r1 = cluster_digit_pass<C>(n, 2048, krem, hist2 + 2048, tot, scratch, [&](int i) {
