@@ -126,6 +126,44 @@ def test_kth_key_far_above_sampled_threshold(fmt):
     check_topk_step(torch.from_numpy(g_np).to(DEV), torch.zeros(n, device=DEV), [0, n], [k], fmt)
 
 
+def _values(kind, n, rng):
+    """Seeded gradient-like values of several shapes: very wide and very
+    narrow dynamic ranges, heavy ties, mostly zeros, both signed zeros."""
+    if kind == "lognormal_wide":
+        return (1e-3 * np.exp(6.0 * rng.standard_normal(n)) * rng.choice([-1, 1], n)).astype(np.float32)
+    if kind == "cauchy":
+        return (1e-4 * rng.standard_cauchy(n)).astype(np.float32)
+    if kind == "uniform_narrow":
+        return (1.0 + 1e-3 * rng.random(n)).astype(np.float32)
+    if kind == "few_values":
+        return (rng.integers(-4, 5, n) * 0.25).astype(np.float32)
+    if kind == "mostly_zero":
+        g = np.zeros(n, np.float32)
+        nz = rng.choice(n, n // 50, replace=False)
+        g[nz] = (rng.standard_normal(nz.size) * 1e-3).astype(np.float32)
+        return g
+    if kind == "signed_zeros":
+        g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        g[rng.random(n) < 0.5] = -0.0
+        return g
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("kind", ["lognormal_wide", "cauchy", "uniform_narrow", "few_values",
+                                  "mostly_zero", "signed_zeros"])
+@pytest.mark.parametrize("n,k", [(1_500_007, 10_000), (3_000_001, 3_000)])
+def test_compact_select_over_value_shapes(kind, n, k, fmt):
+    """One tensor in a compact batch (its list finished by a thread-block
+    cluster, the select counted from the sampled threshold) over values of
+    very different shapes: the k-th key far from or close to the
+    threshold, ties at the cut, zeros that must never be listed."""
+    rng = np.random.default_rng(sum(map(ord, kind)) * 7919 + n)
+    g = torch.from_numpy(_values(kind, n, rng)).to(DEV)
+    e = torch.from_numpy((_values(kind, n, rng) * np.float32(0.5)).astype(np.float32)).to(DEV)
+    check_topk_step(g, e, [0, n], [k], fmt)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_candidate_list_over_capacity_falls_back(fmt):
     """5 % of the elements tie at the largest value: every one is a
