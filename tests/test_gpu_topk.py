@@ -27,6 +27,31 @@ def test_small_segments(fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_small_segments_both_select_paths(fmt):
+    """Tensors of at most 4096 elements, finished by one CTA each: with a
+    small k the few keys at or above the k-th key's first-digit bin are
+    ranked directly; with a large k, an all-equal tensor or mostly zeros
+    (more than 256 such keys) the three-pass radix select runs."""
+    rng = np.random.default_rng(44)
+    parts, ks = [], []
+    parts.append(rng.standard_t(3, 4096) * 1e-3); ks.append(41)        # direct
+    parts.append(rng.standard_t(3, 4096) * 1e-3); ks.append(2000)      # radix
+    parts.append(np.full(3000, 0.25)); ks.append(7)                    # all equal: radix
+    z = np.zeros(4000); z[rng.choice(4000, 20, replace=False)] = 1e-3
+    parts.append(z); ks.append(50)                                     # zeros at the cut: radix
+    parts.append(rng.standard_t(3, 300) * 1e-3); ks.append(300)        # k = len, 300 keys: radix
+    parts.append(rng.standard_t(3, 200) * 1e-3); ks.append(200)        # k = len, 200 keys: direct
+    # residuals: zero on the all-equal and mostly-zero tensors, so that g
+    # keeps their ties and zeros
+    es = [rng.standard_t(3, p.size) * 1e-4 if i not in (2, 3) else np.zeros(p.size)
+          for i, p in enumerate(parts)]
+    g = torch.from_numpy(np.concatenate(parts).astype(np.float32)).to(DEV)
+    e = torch.from_numpy(np.concatenate(es).astype(np.float32)).to(DEV)
+    offs = wl.segments_from_sizes([p.size for p in parts])
+    check_topk_step(g, e, offs, ks, fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k", [(32769, 328), (100_003, 1000), (1 << 20, 10486),
                                  (3_000_017, 3000), (200_000, 1), (40_000, 40_000),
                                  (50_000, 0)])
