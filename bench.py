@@ -41,20 +41,20 @@ UNIT = "G grad elements/s"
 
 # DRAM traffic of one topk_fused launch from one ncu capture (--set full of
 # the second launch of `bench.py --case topk --n 139460608`, the 32768-element
-# tile form the slab uses; see profiles/): 1115.83 MB read + 510.30 MB
-# written = 11.660 bytes per element.  Reported, scaled by n, only while the
+# tile form the slab uses; see profiles/): 1115.82 MB read + 510.79 MB
+# written = 11.663 bytes per element.  Reported, scaled by n, only while the
 # captured code still hashes to what was captured (the kernel's region of
 # ef_topk.cu, from its staging struct to the end of the kernel, and the
 # shared device header); otherwise null.  (Reads scale with n exactly; the
 # writes fall short of 4 B per element by the dirty lines still in L2 when
 # the captured launch ends, about 47 MB at this size, so the scaled figure
 # slightly understates a full-size launch.)
-FUSED_TRAFFIC_PER_ELEMENT = 11.660
+FUSED_TRAFFIC_PER_ELEMENT = 11.663
 FUSED_TRAFFIC_SOURCES = {
     # (file, first marker, end marker or None for the whole file): sha256
     ("error_feedback_gradient_gb300/csrc/ef_topk.cu", "struct FusedStage {",
      "// A segment's select list:"):
-        "409a8c558f18aa64fe27fe9a362d7f8600f940b0d92fa16fe45401c41b3e4475",
+        "3753e85d6aa015f49e35a1dce9c4e04aa1c455146fca744b6913da4b58621f94",
     ("error_feedback_gradient_gb300/csrc/ef_common.cuh", None, None):
         "47c54bef91d740610d7262dd7a0102c11fdd086020fe4996e0643bfb02242e40",
 }
