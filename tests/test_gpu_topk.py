@@ -108,6 +108,18 @@ def test_unaligned_addresses():
     check_topk_step(base_g[2:n + 2], base_e[3:n + 3], [0, 5, 50_007, n], [1, 400, 700])
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_unaligned_addresses_long_list(fmt):
+    """The same two misalignments on a tensor of 5 M elements, whose list
+    is selected by the passes over the list (a general batch), not by a
+    thread-block cluster."""
+    n = 5_000_011
+    base_g = _t(n + 8, 18)
+    base_e = _t(n + 8, 19, 1e-4)
+    check_topk_step(base_g[1:n + 1], base_e[1:n + 1], [0, n], [5000], fmt)
+    check_topk_step(base_g[2:n + 2], base_e[3:n + 3], [0, n], [5000], fmt)
+
+
 def _sample_block_starts(n):
     """Starts of the sampled blocks of a streaming segment of n elements:
     min(4096, n // 1024) blocks of 64 contiguous elements, block b in the
