@@ -1,4 +1,4 @@
-"""The packet exchange's rank logic on CPU: two and three gloo ranks run
+"""The packet exchange's rank logic on CPU: two, three and four gloo ranks run
 ``Exchange.allgather_apply`` (int32 and bitmap packets) and
 ``Exchange.range_apply`` ("梯度稀疏化：只传输重要的梯度元素", §详细算法流程
 step 5 and §与Allreduce的融合).
@@ -136,7 +136,7 @@ def _expect(world, n, k, w0, steps=1):
     return G, w
 
 
-@pytest.mark.parametrize("world,n,k", [(2, 10_007, 400), (3, 5_000, 300)])
+@pytest.mark.parametrize("world,n,k", [(2, 10_007, 400), (3, 5_000, 300), (4, 7_001, 250)])
 def test_gloo_ranks_exchange_packets(world, n, k):
     from error_feedback_gradient_gb300 import exchange as ex
     res = _run(world, n, k)
