@@ -4,9 +4,11 @@
 //   e' = g off S, +0 on S;  packet = (g[i], i) for i in S, ascending i.
 //
 // Segments of at most kSmallMax elements are finished by one CTA each with
-// the whole segment in shared memory (compensate, 3-digit radix select,
-// ordered emit).  Longer segments take the streaming path, batched over the
-// streaming segments of a call:
+// the whole segment in shared memory: compensate, one pass over the top 11
+// key bits, then either a direct rank of the few keys at or above the k-th
+// key's bin (at most kSmallRank of them) or the 3-digit radix select and
+// the ordered emit.  Longer segments take the streaming path, batched over
+// the streaming segments of a call:
 //   1. sample   (up to 128 CTAs per segment): up to 4096 blocks of 64
 //      contiguous elements (at most 1/16 of the segment, each in the middle
 //      of one of as many equal slots) are compensated, and a histogram of
@@ -19,17 +21,23 @@
 //   2. fused    (the HBM pass, 12 B / element): g = g_raw + e written over e,
 //      except that a key >= T_lo is written as +0 and appended, in index
 //      order, to a per-segment candidate list (warp ballots and a bounded
-//      decoupled look-back).  A warp's span whose candidates overflow its
-//      staging buffer is rescanned from L2 by the scan warp, so the list
-//      stays complete; a candidate past the list's capacity keeps g in e.
-//      The last CTA checks each list: between k and its capacity -> select
-//      on the list; otherwise (T_lo too high, or the list over capacity) ->
-//      select on the whole segment, which is always correct, only slower,
-//      once g is back in e at the listed candidates.
+//      decoupled look-back; in a compact batch the look-back reads 128 tile
+//      states per round trip and publishes them by atomic exchange).  A
+//      warp's span whose candidates overflow its staging buffer is rescanned
+//      from L2 by the scan warp, so the list stays complete; a candidate past
+//      the list's capacity keeps g in e.  Each list is then checked: between
+//      k and its capacity -> select on the list; otherwise (T_lo too high,
+//      or the list over capacity) -> select on the whole segment, which is
+//      always correct, only slower, once g is back in e at the listed
+//      candidates.  (In other batches the last CTA records this; in a
+//      compact batch the finish derives it.)
 // A compact batch (every list expected to fit kFinishCap entries, as for
 // the tensors of a layerwise model) ends with
 //   3c. finish  one thread-block cluster per segment selects on its list
-//      and emits it, the list spread over the cluster's shared memory.
+//      and emits it, the list spread over the cluster's shared memory; the
+//      select takes two digit passes counted from T_lo (d0 = (key - T_lo)
+//      >> 11 capped at 1023, then the low 11 bits), or three from the top
+//      bits if the k-th key lies far above T_lo.
 // The call's small segments run as extra CTAs of the first batch's sampling
 // launch, in the shadow of the sampling.
 // Other batches end with
