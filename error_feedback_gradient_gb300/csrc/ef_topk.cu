@@ -1962,7 +1962,7 @@ ef_status topk_compress_impl(const float* g_raw, float* e, int64_t n, int32_t ns
   IO io{g_raw, e, out_values, bitmap ? nullptr : out_indices, bitmap ? out_bitmap : nullptr,
         reinterpret_cast<int32_t*>(ws), pos_out};
 
-  // small segments not folded into a compact batch's finish launch
+  // small segments not folded into the first compact batch's sampling launch
   for (size_t i0 = p.small_folded; i0 < p.small.size(); i0 += kMaxSmall) {
     const size_t cnt = std::min<size_t>(kMaxSmall, p.small.size() - i0);
     SmallBatch sb;
