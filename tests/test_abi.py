@@ -96,6 +96,30 @@ def test_topk_workspace_queries(lib):
     assert st == d["EF_ERR_SIZE"]                             # one segment > 2^31
 
 
+def test_topk_workspace_sizes_of_the_workloads(lib):
+    """What the header and the design state about workspace sizes: the
+    allocation-free entry point's scratch holds a BERT-large-sized flat
+    tensor at top-0.1 % and the layerwise ResNet-50 call, the 2^31 tensor's
+    workspace is about 76 MB, and the size never shrinks as k grows (the
+    candidate list's capacity is min(len, 4k + 65 536) per segment)."""
+    from error_feedback_gradient_gb300 import workloads as wl
+    d = _header_defines()
+    cap = d["EF_NOALLOC_SCRATCH_BYTES"]
+    n = 335_141_888
+    for fmt in (0, 1):
+        st, b = _ws_size(lib, n, [0, n], [wl.k_from_ratio(n, 1, 1000)], fmt)
+        assert st == d["EF_OK"] and b <= cap
+    offs, ks = wl.resnet50_segments()
+    st, b = _ws_size(lib, offs[-1], offs, ks)
+    assert st == d["EF_OK"] and b <= cap
+    n = 1 << 31
+    st, b = _ws_size(lib, n, [0, n], [wl.k_from_ratio(n, 1, 1000)])
+    assert st == d["EF_OK"] and 70e6 < b < 80e6
+    n = 1 << 24
+    sizes = [_ws_size(lib, n, [0, n], [k])[1] for k in (0, 1, 100, 10**4, 10**6, n // 4, n)]
+    assert sizes == sorted(sizes) and sizes[-1] > n * 8     # a list of every element fits
+
+
 def test_topk_rejects_before_device(lib):
     d = _header_defines()
     ws = ctypes.c_void_p(256 * 1000)           # never dereferenced: validation fails first
