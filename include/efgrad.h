@@ -12,9 +12,13 @@
  * ---------------------------------------
  * Memory.  Pointers named h_* are host memory; every other buffer pointer is
  *   device memory of the current CUDA device.  The caller owns all buffers.
- *   The library allocates no device memory, keeps no pointer after a call
- *   returns, and keeps no state between calls other than a per-thread
- *   profiling hook (ef_profile_events) and a per-thread last CUDA error.
+ *   The library allocates no device memory and keeps no caller pointer after
+ *   a call returns.  The state it keeps between calls: per thread, the last
+ *   CUDA error, a launch counter (ef_kernel_launches) and a profiling hook
+ *   (ef_profile_events); per device, a cached description of the device (SM
+ *   count, compute capability, shared-memory limit) and, for
+ *   ef_topk_compress_noalloc only, the address of its own static scratch
+ *   array.
  *   Scratch memory comes from a caller-provided workspace whose size the
  *   matching *_workspace_size query returns; it must be 256-byte aligned and
  *   may be reused by the next call on the same stream.
