@@ -136,7 +136,12 @@ def _expect(world, n, k, w0, steps=1):
     return G, w
 
 
-@pytest.mark.parametrize("world,n,k", [(2, 10_007, 400), (3, 5_000, 300), (4, 7_001, 250)])
+@pytest.mark.parametrize("world,n,k", [
+    (2, 10_007, 400), (3, 5_000, 300), (4, 7_001, 250),
+    (3, 1_500, 50),     # rank 2's range lies wholly past n
+    (2, 1_000, 0),      # empty packets
+    (2, 1_000, 1_000),  # every element in every packet
+])
 def test_gloo_ranks_exchange_packets(world, n, k):
     from error_feedback_gradient_gb300 import exchange as ex
     res = _run(world, n, k)
@@ -149,8 +154,8 @@ def test_gloo_ranks_exchange_packets(world, n, k):
             assert np.array_equal(g_got.view(np.uint32), G.view(np.uint32)), (r, key)
             assert np.array_equal(w_got.view(np.uint32), w1.view(np.uint32)), (r, key)
         g_sh, w_got, s = res[r]["range"]
-        a = r * s
-        n_r = min(n, a + s) - a
+        a = min(r * s, n)
+        n_r = max(0, min(n, a + s) - a)    # 0 for a range wholly past n
         assert np.array_equal(g_sh[:n_r].view(np.uint32), G[a:a + n_r].view(np.uint32)), r
         assert np.array_equal(w_got[:n].view(np.uint32), w2.view(np.uint32)), r
         assert np.array_equal(w_got[n:].view(np.uint32), w0[n:].view(np.uint32)), r
