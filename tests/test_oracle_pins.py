@@ -414,13 +414,18 @@ def test_aggregate_rejects_unsorted():
                                   "values": np.ones(2, F32)}], 5)
 
 
-def test_sign_aggregate_counts():
+def check_sign_aggregate_counts(aggregate=None):
+    aggregate = aggregate or oracle.sign_aggregate
     rng = random.Random(3)
     n, W = 77, 6
     flags = [[rng.random() < 0.5 for _ in range(n)] for _ in range(W)]
-    G = oracle.sign_aggregate([oracle.pack_bits(np.array(f)) for f in flags], n)
+    G = aggregate([oracle.pack_bits(np.array(f)) for f in flags], n)
     want = [sum(1 if flags[w][i] else -1 for w in range(W)) for i in range(n)]
     assert G.tolist() == [float(x) for x in want]
+
+
+def test_sign_aggregate_counts():
+    check_sign_aggregate_counts()
 
 
 # ---------------------------------------------------------------------------
@@ -742,6 +747,21 @@ def _sign_zero_is_zero(g, eps, beta1):
     return bits, e
 
 
+def _sign_decision_ignores_eps(g, eps, beta1):
+    # mistake: the sign taken of g alone, the error buffer only in the update
+    _, e = oracle.sign_ef_step(g, eps, beta1)
+    return oracle.pack_bits(~(np.asarray(g, F32) < 0)), e
+
+
+def _momentum_swapped_weights(m, ghat, beta1):
+    b1 = F32(beta1)
+    return ((F32(1) - b1) * np.asarray(m, F32) + b1 * np.asarray(ghat, F32)).astype(F32)
+
+
+def _sign_aggregate_bit_one_is_minus(bit_vectors, n):
+    return (-oracle.sign_aggregate(bit_vectors, n)).astype(F32)
+
+
 def _aggregate_reverse_order(packets, n):
     return oracle.sparse_aggregate(list(reversed(packets)), n)
 
@@ -843,6 +863,9 @@ def _split_counts_equal_too(indices, bounds):
     (check_pack_bits, {"pack": _pack_msb_first}),
     (check_sign_golden, {"sign_step": _sign_step_wrong_ema}),
     (check_sign_golden, {"sign_step": _sign_zero_is_zero}),
+    (check_sign_golden, {"sign_step": _sign_decision_ignores_eps}),
+    (check_sign_golden, {"momentum": _momentum_swapped_weights}),
+    (check_sign_aggregate_counts, {"aggregate": _sign_aggregate_bit_one_is_minus}),
     (check_aggregate_golden, {"aggregate": _aggregate_reverse_order}),
     (check_aggregate_golden, {"sgd": _sgd_wrong_sign}),
     (check_q8_golden, {"quantize": _q8_round_half_away}),
