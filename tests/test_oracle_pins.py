@@ -201,6 +201,38 @@ def test_topk_edge_cases():
         oracle.topk_ef_step(g, e, [0, 5], [6])
 
 
+def check_layerwise_bruteforce(step=None):
+    """A layerwise step against its definition written out independently:
+    g = RN32(g_raw + e) formed in float64 and rounded once (exact for a sum
+    of two floats, since 53 >= 2 * 24 + 2), each segment's top-k by the
+    brute-force sort, global indices ascending, and a residual that is g off
+    the selection and +0 on it."""
+    step = step or oracle.topk_ef_step
+    rng = np.random.default_rng(12)
+    sizes, ks = [9, 40, 1, 33, 16], [3, 4, 1, 0, 16]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    n = offs[-1]
+    levels = np.array([0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 0.25], F32)
+    for trial in range(4):
+        g_raw = rng.choice(levels, n).astype(F32) if trial % 2 else rng.standard_normal(n).astype(F32)
+        e = (rng.standard_normal(n) * 0.5).astype(F32)
+        g = (g_raw.astype(np.float64) + e.astype(np.float64)).astype(F32)
+        gl = [float(x) for x in g]
+        want = []
+        for s, k in enumerate(ks):
+            want += [offs[s] + i for i in _brute_topk(gl[offs[s]:offs[s + 1]], k)]
+        e_want = g.copy()
+        e_want[want] = F32(0.0)
+        out = step(g_raw, e, offs, ks)
+        assert out["indices"].tolist() == want
+        assert out["values"].view(np.uint32).tolist() == g[want].view(np.uint32).tolist()
+        assert out["e"].view(np.uint32).tolist() == e_want.view(np.uint32).tolist()
+
+
+def test_layerwise_bruteforce():
+    check_layerwise_bruteforce()
+
+
 def test_layerwise_equals_separate_tensors():
     """[SPARSE] §分层自适应Top-k: each tensor selects on its own, so one
     layerwise call equals one call per tensor (indices shifted)."""
@@ -747,6 +779,28 @@ def _sign_zero_is_zero(g, eps, beta1):
     return bits, e
 
 
+def _step_segment_local_indices(g_raw, e, offs, ks, idx_format="int32"):
+    out = oracle.topk_ef_step(g_raw, e, offs, ks, idx_format)
+    seg = np.searchsorted(np.asarray(offs), out["selected"], side="right") - 1
+    out["indices"] = (out["selected"] - np.asarray(offs)[seg]).astype(np.int32)
+    return out
+
+
+def _step_selects_over_the_whole_buffer(g_raw, e, offs, ks, idx_format="int32"):
+    n = len(g_raw)
+    return oracle.topk_ef_step(g_raw, e, [0, n], [sum(ks)], idx_format)
+
+
+def _step_compensates_with_minus(g_raw, e, offs, ks, idx_format="int32"):
+    return oracle.topk_ef_step(g_raw, (-np.asarray(e, F32)).astype(F32), offs, ks, idx_format)
+
+
+def _step_residual_keeps_selection(g_raw, e, offs, ks, idx_format="int32"):
+    out = oracle.topk_ef_step(g_raw, e, offs, ks, idx_format)
+    out["e"] = oracle.compensate(g_raw, e)
+    return out
+
+
 def _sign_decision_ignores_eps(g, eps, beta1):
     # mistake: the sign taken of g alone, the error buffer only in the update
     _, e = oracle.sign_ef_step(g, eps, beta1)
@@ -860,6 +914,10 @@ def _split_counts_equal_too(indices, bounds):
 @pytest.mark.parametrize("check,kwargs", [
     (check_topk_bruteforce, {"topk_indices": _topk_ties_to_higher_index}),
     (check_topk_bruteforce, {"topk_indices": _topk_signed_not_abs}),
+    (check_layerwise_bruteforce, {"step": _step_segment_local_indices}),
+    (check_layerwise_bruteforce, {"step": _step_selects_over_the_whole_buffer}),
+    (check_layerwise_bruteforce, {"step": _step_compensates_with_minus}),
+    (check_layerwise_bruteforce, {"step": _step_residual_keeps_selection}),
     (check_pack_bits, {"pack": _pack_msb_first}),
     (check_sign_golden, {"sign_step": _sign_step_wrong_ema}),
     (check_sign_golden, {"sign_step": _sign_zero_is_zero}),
