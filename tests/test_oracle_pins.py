@@ -816,6 +816,11 @@ def _sign_aggregate_bit_one_is_minus(bit_vectors, n):
     return (-oracle.sign_aggregate(bit_vectors, n)).astype(F32)
 
 
+def _aggregate_averages(packets, n):
+    # mistake: the receiver divides by the worker count (the pages add)
+    return (oracle.sparse_aggregate(packets, n) / F32(len(packets))).astype(F32)
+
+
 def _aggregate_reverse_order(packets, n):
     return oracle.sparse_aggregate(list(reversed(packets)), n)
 
@@ -925,6 +930,7 @@ def _split_counts_equal_too(indices, bounds):
     (check_sign_golden, {"momentum": _momentum_swapped_weights}),
     (check_sign_aggregate_counts, {"aggregate": _sign_aggregate_bit_one_is_minus}),
     (check_aggregate_golden, {"aggregate": _aggregate_reverse_order}),
+    (check_aggregate_golden, {"aggregate": _aggregate_averages}),
     (check_aggregate_golden, {"sgd": _sgd_wrong_sign}),
     (check_q8_golden, {"quantize": _q8_round_half_away}),
     (check_q8_golden, {"scale": _q8_scale_over_128}),
